@@ -1,0 +1,430 @@
+"""Benchmark of the fused LM-head exact sampler on GB300.
+
+Metric: fused LM-head sample microseconds per decode step and the fraction of
+the HBM / tensor-core roofline, versus batch, on a Llama-3-8B-shaped LM head
+(d = 4096, V = 128256; synthetic bf16 weights and hidden states -- no trained
+weights or datasets).  One step is one call of the public sampling entry point
+(fused kernel + cross-tile reduction) over one batch of hidden states with
+its own step counter.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--batch B] [--impl ours|reference]
+
+Prints ONE JSON line (rank 0).  Under torchrun (N > 1) every rank samples its
+own batch of B rows against a replicated W (data-parallel replicas, no
+collective on the data path); the timed region is bracketed by a barrier and
+a device synchronize, and the slowest rank's time is reported.
+"""
+
+import argparse
+import ctypes
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "fused LM-head sample µs/step & % of HBM/TC roofline vs batch (d4096,V128256)"
+UNIT = "us/step"
+SWEEP = (1, 2, 4, 8, 16, 32, 64)
+
+
+# ---------------------------------------------------------------- roofline
+def algorithmic_bytes(B, d, V, bias=False):
+    """Bytes one fused launch must move at minimum: W and h read once, the
+    temperatures read, and per row an int64 id + fp32 max written (plus the
+    fp32 bias when present).  The per-tile candidates are implementation
+    overhead and not counted."""
+    return 2 * V * d + 2 * B * d + 4 * B + 12 * B + (4 * B * V if bias else 0)
+
+
+def algorithmic_flops(B, d, V):
+    return 2 * B * d * V
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return {"hbm_gbs": float(pk["hbm_gbs"]), "bf16_tflops": float(pk["bf16_tflops"]),
+                "bf16_tflops_sustained": float(pk.get("bf16_tflops_sustained", pk["bf16_tflops"])),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback"}
+
+
+def roofline(B, d, V, kernel_us, peaks, bias=False):
+    """Roofline entry of the dominant (fused) kernel: bound = the slower of the
+    bytes at HBM peak and the FLOPs at bf16 tensor peak."""
+    nbytes = algorithmic_bytes(B, d, V, bias)
+    flops = algorithmic_flops(B, d, V)
+    t_hbm = nbytes / (peaks["hbm_gbs"] * 1e9)
+    t_tc = flops / (peaks["bf16_tflops"] * 1e12)
+    if t_hbm >= t_tc:
+        achieved = nbytes / (kernel_us * 1e-6) / 1e9
+        return {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                "algorithmic_bytes": nbytes, "roofline_us": round(t_hbm * 1e6, 2),
+                "peak_source": peaks["source"]}
+    achieved = flops / (kernel_us * 1e-6) / 1e12
+    return {"bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["bf16_tflops"],
+            "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
+            "algorithmic_flops": flops, "roofline_us": round(t_tc * 1e6, 2),
+            "peak_source": peaks["source"]}
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    """Samples SM clock and throttle reasons of one GPU during the timed
+    region, through NVML (ctypes; read-only queries) or, failing that, an
+    nvidia-smi subprocess."""
+
+    REASONS = {0x8: "hw_slowdown", 0x40: "hw_thermal_slowdown", 0x20: "sw_thermal_slowdown",
+               0x4: "sw_power_cap", 0x80: "hw_power_brake_slowdown", 0x1: "gpu_idle"}
+
+    def __init__(self, index):
+        self.index = index
+        self.samples = []
+        self.reasons = set()
+        self.max_mhz = None
+        self._stop = threading.Event()
+        self._thread = None
+        self._proc = None
+        self._nvml = None
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() == 0:
+                h = ctypes.c_void_p()
+                if nv.nvmlDeviceGetHandleByIndex_v2(index, ctypes.byref(h)) == 0:
+                    self._nvml, self._h = nv, h
+                    mx = ctypes.c_uint()
+                    if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
+                        self.max_mhz = mx.value
+        except OSError:
+            self._nvml = None
+
+    def _poll(self):
+        nv, h = self._nvml, self._h
+        clk = ctypes.c_uint()
+        rs = ctypes.c_ulonglong()
+        while not self._stop.is_set():
+            if nv.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0:
+                self.samples.append(clk.value)
+            if nv.nvmlDeviceGetCurrentClocksEventReasons(h, ctypes.byref(rs)) == 0:
+                for bit, name in self.REASONS.items():
+                    if rs.value & bit and name != "gpu_idle":
+                        self.reasons.add(name)
+            time.sleep(0.002)
+
+    def start(self):
+        if self._nvml is not None:
+            self._thread = threading.Thread(target=self._poll, daemon=True)
+            self._thread.start()
+        else:
+            try:
+                self._proc = subprocess.Popen(
+                    ["nvidia-smi", "-i", str(self.index),
+                     "--query-gpu=clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+                     "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+                     "clocks_event_reasons.sw_power_cap", "--format=csv,noheader,nounits", "-lms", "50"],
+                    stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            except OSError:
+                self._proc = None
+
+    def stop(self):
+        self._stop.set()
+        if self._thread is not None:
+            self._thread.join()
+        if self._proc is not None:
+            self._proc.terminate()
+            out, _ = self._proc.communicate()
+            names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+            for line in out.strip().splitlines():
+                f = [x.strip() for x in line.split(",")]
+                try:
+                    self.samples.append(int(f[0]))
+                    self.max_mhz = int(f[1])
+                except (ValueError, IndexError):
+                    continue
+                for n, v in zip(names, f[2:]):
+                    if v == "Active":
+                        self.reasons.add(n)
+
+    def summary(self):
+        return {"sm_mhz": statistics.median(self.samples) if self.samples else None,
+                "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons),
+                "samples": len(self.samples)}
+
+
+# ---------------------------------------------------------------- dist
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def max_over_ranks(x, dist, device=None):
+    """Largest value of ``x`` over all ranks (identity without a process group)."""
+    if dist is None or not dist.is_initialized():
+        return x
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(dist):
+    if dist is not None and dist.is_initialized():
+        dist.barrier()
+
+
+# ---------------------------------------------------------------- ours
+def _to_dev(a, torch):
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint16:
+        return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).cuda()
+    return torch.from_numpy(a).cuda()
+
+
+def time_steps(fs, torch, hd, Wd, td, seed, first_step, n, stream, events=True):
+    """Run n steps on ``stream``; return (total ms by events around all steps,
+    mean fused-kernel ms from per-step profile events)."""
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(n)] if events else []
+    stops = [torch.cuda.Event(enable_timing=True) for _ in range(n)] if events else []
+    ids = torch.empty(hd.shape[0], dtype=torch.int64, device="cuda")
+    mx = torch.empty(hd.shape[0], dtype=torch.float32, device="cuda")
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        t0.record(stream)
+        for i in range(n):
+            if events:
+                fs.profile_events(starts[i], stops[i])
+            fs.sample(hd, Wd, td, seed, first_step + i, out=(ids, mx), stream=stream)
+        t1.record(stream)
+    fs.profile_events(None, None)
+    torch.cuda.synchronize()
+    total = t0.elapsed_time(t1)
+    kern = statistics.mean(s.elapsed_time(e) for s, e in zip(starts, stops)) if events else None
+    return total, kern
+
+
+def run_ours(args):
+    import torch
+    from lm_head_exact_gb300 import binding as fs, synthetic
+
+    world, rank, local = dist_env()
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    fs.library()
+    peaks = load_peaks()
+    kind = "llama3_8b"
+    shape = synthetic.SHAPES[kind]
+    d, V = shape["d"], shape["V"]
+    B = args.batch
+    bmax = max(max(SWEEP), B)
+    # every rank gets its own batch rows (weak scaling); W is replicated
+    h_all = synthetic.normal_rows_bf16(synthetic.SEED_H, bmax * world, d, 1.0)
+    h_rank = h_all[rank * bmax:(rank + 1) * bmax]
+    W = synthetic.weights(kind)
+    Wd = _to_dev(W, torch)
+    hd_all = _to_dev(h_rank, torch)
+    temp_all = torch.ones(bmax, dtype=torch.float32, device="cuda")
+    stream = torch.cuda.Stream()
+    seed = synthetic.SAMPLING_SEED
+    fs.workspace_reserve(bmax, V, stream=stream)
+
+    hd, td = hd_all[:B], temp_all[:B]
+    # warm-up (untimed)
+    time_steps(fs, torch, hd, Wd, td, seed, 0, args.warmup, stream, events=False)
+    clocks = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    barrier(dist)
+    torch.cuda.synchronize()
+    if clocks:
+        clocks.start()
+    total_ms, kern_ms = time_steps(fs, torch, hd, Wd, td, seed, args.warmup, args.steps, stream)
+    torch.cuda.synchronize()
+    barrier(dist)
+    if clocks:
+        clocks.stop()
+    step_ms = max_over_ranks(total_ms / args.steps, dist, device="cuda")
+    kern_ms = max_over_ranks(kern_ms, dist, device="cuda")
+    launches = 2 * args.steps          # fused kernel + cross-tile reduction per step
+
+    # end to end through the host-buffer entry point: pinned h / temp in,
+    # ids / max out, every step
+    h_pin = torch.from_numpy(h_rank[:B].view(np.int16)).pin_memory()
+    t_pin = torch.ones(B, dtype=torch.float32).pin_memory()
+    ids_pin = torch.empty(B, dtype=torch.int64).pin_memory()
+    mx_pin = torch.empty(B, dtype=torch.float32).pin_memory()
+    for i in range(args.warmup):
+        fs.sample_host(h_pin, Wd, t_pin, seed, i, out_ids=ids_pin, out_max=mx_pin, stream=stream)
+    barrier(dist)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        fs.sample_host(h_pin, Wd, t_pin, seed, args.warmup + i, out_ids=ids_pin, out_max=mx_pin,
+                       stream=stream)
+    e2e_ms = (time.perf_counter() - t0) * 1e3 / args.steps
+    barrier(dist)
+    e2e_ms = max_over_ranks(e2e_ms, dist, device="cuda")
+
+    # batch sweep of the metric (same kernels, fewer steps per point)
+    sweep = []
+    if not args.no_sweep:
+        for b in SWEEP:
+            time_steps(fs, torch, hd_all[:b], Wd, temp_all[:b], seed, 0, 3, stream, events=False)
+            tot, km = time_steps(fs, torch, hd_all[:b], Wd, temp_all[:b], seed, 3, 20, stream)
+            rf = roofline(b, d, V, km * 1e3, peaks)
+            sweep.append({"B": b, "us_per_step": round(tot / 20 * 1e3, 2),
+                          "fused_kernel_us": round(km * 1e3, 2), "frac": rf["frac"],
+                          "bound": rf["bound"], "path": fs.path_for_batch(b)})
+
+    result = None
+    if rank == 0:
+        us = step_ms * 1e3
+        rf = roofline(B, d, V, kern_ms * 1e3, peaks)
+        rf["traffic"] = None
+        rf["kernel_us"] = round(kern_ms * 1e3, 2)
+        result = {
+            "metric": METRIC, "value": round(us, 2), "unit": UNIT, "higher_is_better": False,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(step_ms, 4), "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": f"llama3_8b LM head d={d} V={V} B={B} (Llama-3-8B-shaped, random init)",
+                       "global_batch": B * world, "per_gpu_batch": B, "d": d, "V": V,
+                       "parallelism": f"replicas{world}" if world > 1 else "single",
+                       "l2": "inputs larger than L2 (W is 1.05 GB); no flush",
+                       "tokens_per_s": round(B * world / (us * 1e-6), 1),
+                       "path": fs.path_for_batch(B)},
+            "roofline": rf,
+            "e2e": {"value": round(e2e_ms * 1e3, 2), "unit": UNIT,
+                    "h2d_bytes_per_step": B * d * 2 + B * 4, "d2h_bytes_per_step": B * 12},
+            "clocks": clocks.summary() if clocks else None,
+            "gpu_launches": launches,
+            "sweep": sweep,
+        }
+        if not args.no_cpu_baseline:
+            result["cpu_baseline"] = cpu_baseline(B, args.cpu_seconds)
+    if dist is not None:
+        dist.destroy_process_group()
+    return result
+
+
+# ---------------------------------------------------------------- oracle arm
+def _oracle_step(wl_h, W, temp, seed, step, vocab_rows):
+    """One oracle step on the first ``vocab_rows`` rows of W; returns seconds."""
+    from oracle import sampler
+    t0 = time.perf_counter()
+    sampler.sample(wl_h, W[:vocab_rows], temp, seed, step)
+    return time.perf_counter() - t0
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(B, seconds=20.0):
+    """The fp64 oracle, as it stands, timed on this host's cores on a bounded
+    sample: all B rows against a slice of the vocabulary, scaled to the full
+    vocabulary (the oracle's cost is linear in V)."""
+    from lm_head_exact_gb300 import synthetic
+    kind = "llama3_8b"
+    V = synthetic.SHAPES[kind]["V"]
+    W = synthetic.weights(kind)
+    h = synthetic.normal_rows_bf16(synthetic.SEED_H, B, synthetic.SHAPES[kind]["d"], 1.0)
+    temp = np.ones(B, np.float32)
+    rows = 4096
+    t = _oracle_step(h, W, temp, synthetic.SAMPLING_SEED, 0, rows)
+    # grow the slice until one sample costs about `seconds / 4`
+    while t < seconds / 4 and rows < V:
+        rows = min(V, rows * 2)
+        t = _oracle_step(h, W, temp, synthetic.SAMPLING_SEED, 0, rows)
+    reps, total = 1, t
+    while total < seconds * 0.75:
+        total += _oracle_step(h, W, temp, synthetic.SAMPLING_SEED, reps, rows)
+        reps += 1
+    per_step_us = total / reps * (V / rows) * 1e6
+    return {"value": round(per_step_us, 1), "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+            "sample": f"{reps} oracle steps of B={B} rows x {rows} of {V} vocabulary rows, "
+                      f"scaled x{V / rows:.2f} to the full vocabulary; numpy fp64 (BLAS threads = cores)"}
+
+
+def run_reference(args):
+    """Reference arm: the fp64 CPU oracle timed on the host cores, on this
+    benchmark's workload (each step a bounded vocabulary slice, scaled)."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return None
+    from lm_head_exact_gb300 import synthetic
+    kind = "llama3_8b"
+    d, V = synthetic.SHAPES[kind]["d"], synthetic.SHAPES[kind]["V"]
+    B = args.batch
+    W = synthetic.weights(kind)
+    h = synthetic.normal_rows_bf16(synthetic.SEED_H, B, d, 1.0)
+    temp = np.ones(B, np.float32)
+    budget = 150.0 / max(1, args.steps + args.warmup)     # seconds per step
+    rows = 2048
+    while rows < V and _oracle_step(h, W, temp, 1234, 0, min(V, rows * 2)) < budget:
+        rows = min(V, rows * 2)
+    for i in range(args.warmup):
+        _oracle_step(h, W, temp, 1234, i, rows)
+    t = sum(_oracle_step(h, W, temp, 1234, args.warmup + i, rows) for i in range(args.steps))
+    us = t / args.steps * (V / rows) * 1e6
+    sample = (f"B={B} rows x {rows} of {V} vocabulary rows per step, scaled x{V / rows:.2f}; "
+              f"numpy fp64 oracle")
+    return {"metric": METRIC, "value": round(us, 1), "unit": UNIT, "higher_is_better": False,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(us / 1e3, 3), "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": {"workload": f"llama3_8b LM head d={d} V={V} B={B} (Llama-3-8B-shaped, random init)",
+                       "global_batch": B, "d": d, "V": V, "parallelism": "single"},
+            "cpu_baseline": {"value": round(us, 1), "unit": UNIT, "cores": cpu_cores(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(us, 1), "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--batch", type=int, default=16)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=20.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    return args
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    res = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

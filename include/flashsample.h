@@ -1,0 +1,193 @@
+/*
+ * libflashsample -- exact categorical sampling fused into the LM-head matmul,
+ * for one NVIDIA GB300 (sm_103a).
+ *
+ * What it computes (FlashSampling: Fast and Memory-Efficient Exact Sampling;
+ * summary page, sections "Method" and "Key claims"; arXiv abstract):
+ *
+ *   logits[b, v] = sum_k h[b, k] * W[v, k]  (+ bias[b, v])
+ *   z[b, v]      = logits[b, v] / T[b] + g[b, v],   g = -log(-log u)
+ *   out_ids[b]   = argmax_v z[b, v],  out_max[b] = z[b, out_ids[b]]
+ *
+ * so out_ids[b] is an exact sample of softmax(logits[b, :] / T[b]).  The
+ * vocabulary is processed tile by tile on chip; only a per-row (max, argmax)
+ * per tile survives and a small reduction over tiles finishes the sample, so
+ * the B x V logits never reach device memory.
+ *
+ * Conventions shared by every entry point:
+ *  - h is bf16 [B, d] and W is bf16 [V, d], both row-major (d contiguous).
+ *    d must be a multiple of 8 and both base pointers 16-byte aligned
+ *    (FS_ERR_UNSUPPORTED otherwise).  B, V < 2^31.
+ *  - temp is fp32 [B].  T > 0: sample from softmax(logits / T).  T == 0:
+ *    greedy (argmax of the logits, no noise; out_max is the max logit).
+ *    T < 0 or NaN: no sample (out_ids = -1, out_max = -inf).
+ *  - Noise: u is drawn from Philox-4x32-10 (Salmon et al., SC'11) with key
+ *    (seed mod 2^32, seed >> 32) and counter (v >> 2, b, step mod 2^32,
+ *    step >> 32); word (v & 3) gives x and u = ((x >> 9) + 0.5) * 2^-23.  The
+ *    draw of (b, v, step) is fixed by the counter alone, so results do not
+ *    depend on tiling, chunking or the kernel chosen.
+ *  - Ties: equal z goes to the smaller vocabulary id.  NaN and -inf scores
+ *    never win; a row without any candidate returns id -1 and max -inf.
+ *  - Unless stated otherwise, pointers are DEVICE pointers owned by the
+ *    caller; the call validates arguments on the host, enqueues its kernels
+ *    on `stream` (a cudaStream_t; NULL is the legacy default stream) and
+ *    returns without synchronizing.  Results are valid once the stream has
+ *    reached that point.
+ *  - The library owns one workspace per (device, stream) that holds the
+ *    per-(row, tile) candidates.  It grows on demand, which is not allowed
+ *    inside CUDA-graph capture: call fs_workspace_reserve() first.
+ *  - Errors: argument problems return FS_ERR_INVALID_ARG / FS_ERR_UNSUPPORTED
+ *    before anything is enqueued; a failed CUDA call returns FS_ERR_CUDA.
+ *    fs_last_error() gives a human-readable detail of the last failure on
+ *    the calling thread.
+ */
+#ifndef FLASHSAMPLE_H_
+#define FLASHSAMPLE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Exported entry points (the library is built with hidden visibility). */
+#if defined(__GNUC__)
+#define FS_API __attribute__((visibility("default")))
+#else
+#define FS_API
+#endif
+
+typedef enum fs_status {
+  FS_OK = 0,
+  FS_ERR_INVALID_ARG = 1,     /* null pointer, negative size, bad flag combination */
+  FS_ERR_UNSUPPORTED = 2,     /* valid request the kernels do not handle (alignment, d % 8) */
+  FS_ERR_CUDA = 3,            /* a CUDA runtime call or kernel launch failed */
+  FS_ERR_WORKSPACE = 4,       /* workspace must grow but cannot (allocation failed, or capture active) */
+  FS_ERR_DEVICE_TIMEOUT = 5   /* a kernel gave up a bounded wait and flagged the device error word */
+} fs_status;
+
+/* Flags of fs_sample_chunked. */
+#define FS_CHUNK_FIRST 1      /* ignore the incoming carry: this chunk starts the row */
+#define FS_CHUNK_LAST 2       /* write out_ids / out_max after merging this chunk */
+
+/* Kernel families (fs_set_path). */
+#define FS_PATH_AUTO 0        /* chosen from the batch size B only */
+#define FS_PATH_SIMT 1        /* W-streaming CUDA-core path */
+#define FS_PATH_TC_VOCAB 2    /* tcgen05 tensor-core path, vocabulary rows on the MMA M axis */
+#define FS_PATH_TC_BATCH 3    /* tcgen05 tensor-core path, batch rows on the MMA M axis */
+
+/*
+ * One decode step of fused sampling (summary page, "Method"; arXiv abstract).
+ *   h [B, d] bf16, W [V, d] bf16, temp [B] fp32: inputs (device).
+ *   seed, step: noise stream (see conventions).
+ *   out_ids [B] int64, out_max [B] fp32: outputs (device).
+ *   stream: cudaStream_t to enqueue on.
+ * B == 0 is a no-op; V == 0 gives id -1 on every row.
+ */
+FS_API fs_status fs_sample(const void* h, const void* W, int64_t B, int64_t d, int64_t V,
+                    const float* temp, uint64_t seed, uint64_t step,
+                    int64_t* out_ids, float* out_max, void* stream);
+
+/*
+ * fs_sample with an optional fp32 bias added to the logits before the
+ * division by T.  bias (device, nullable) holds element (b, v) at
+ * bias[b * bias_row_stride + v]; bias_row_stride is 0 (one [V] vector shared
+ * by all rows) or >= V.
+ */
+FS_API fs_status fs_sample_ex(const void* h, const void* W, int64_t B, int64_t d, int64_t V,
+                       const float* temp, const float* bias, int64_t bias_row_stride,
+                       uint64_t seed, uint64_t step,
+                       int64_t* out_ids, float* out_max, void* stream);
+
+/*
+ * Grouped online (chunked) variant (arXiv abstract; summary page, "Method",
+ * last paragraph): one call per contiguous vocabulary chunk [v_begin, v_end),
+ * with a per-row (max, argmax) carry between calls.  The result of a full
+ * sequence of calls equals fs_sample on the whole vocabulary bit for bit,
+ * because the noise of (b, v) depends on the global id v only and the same
+ * kernel family (chosen from B) computes every logit.
+ *   W_chunk: rows [v_begin, v_end) of W, i.e. W + v_begin * d (device).
+ *   bias_chunk: bias columns of the chunk (element (b, j) for global id
+ *     v_begin + j at bias_chunk[b * bias_row_stride + j]) or NULL.
+ *   carry_max [B] fp32 and carry_ids [B] int64 (device, caller-owned):
+ *     read unless FS_CHUNK_FIRST, always updated (ids -1 = none yet).
+ *   flags: FS_CHUNK_FIRST and/or FS_CHUNK_LAST.  With FS_CHUNK_LAST,
+ *     out_ids / out_max are written (they may alias the carry arrays' roles
+ *     but not their memory); otherwise they may be NULL.
+ */
+FS_API fs_status fs_sample_chunked(const void* h, const void* W_chunk, int64_t B, int64_t d,
+                            int64_t v_begin, int64_t v_end, const float* temp,
+                            const float* bias_chunk, int64_t bias_row_stride,
+                            uint64_t seed, uint64_t step,
+                            float* carry_max, int64_t* carry_ids, int flags,
+                            int64_t* out_ids, float* out_max, void* stream);
+
+/*
+ * End-to-end convenience call with HOST buffers: copies h_host [B, d] bf16 and
+ * temp_host [B] fp32 to the device, samples against the device-resident
+ * W [V, d] (and optional device bias), copies out_ids_host [B] int64 and
+ * out_max_host [B] fp32 back, and synchronizes `stream` before returning.
+ * Host buffers should be pinned (cudaHostAlloc / cudaHostRegister) for the
+ * copies to be asynchronous; pageable memory works but is slower.  Device
+ * staging lives in the library workspace of (device, stream).
+ */
+FS_API fs_status fs_sample_host(const void* h_host, const void* W, int64_t B, int64_t d, int64_t V,
+                         const float* temp_host, const float* bias, int64_t bias_row_stride,
+                         uint64_t seed, uint64_t step,
+                         int64_t* out_ids_host, float* out_max_host, void* stream);
+
+/* Workspace bytes one call with (B, V) needs on the current device. */
+FS_API size_t fs_workspace_bytes(int64_t B, int64_t V);
+
+/*
+ * Grow the workspace of (current device, stream) to serve calls up to
+ * (B, V) without allocating; required before capturing calls in a CUDA graph.
+ */
+FS_API fs_status fs_workspace_reserve(int64_t B, int64_t V, void* stream);
+
+/* Free every workspace this library holds on the current device. */
+FS_API fs_status fs_workspace_release(void);
+
+/* Force a kernel family for later calls (FS_PATH_*); FS_PATH_AUTO restores
+ * the batch-size rule.  Process-wide. */
+FS_API fs_status fs_set_path(int path);
+
+/* The kernel family a call with batch size B would use under the current
+ * setting (FS_PATH_SIMT / FS_PATH_TC_VOCAB / FS_PATH_TC_BATCH). */
+FS_API int fs_path_for_batch(int64_t B);
+
+/*
+ * Timing hook: when both are non-NULL, every later sampling call on this
+ * thread records cudaEvent_t `start` on its stream just before the fused
+ * sampling kernel and `stop` just after it (the cross-tile reduction is
+ * outside the pair).  Pass NULL, NULL to stop.  Lets a caller time the
+ * dominant kernel inside a normal run without changing the work done.
+ */
+FS_API fs_status fs_profile_events(void* start, void* stop);
+
+/* Read and clear the device error word of the current device (synchronizes
+ * the device).  *code receives 0 when no kernel reported a problem. */
+FS_API fs_status fs_device_error(int* code);
+
+/* Static name of a status code. */
+FS_API const char* fs_status_string(fs_status s);
+
+/* Detail of the last failure on the calling thread ("" if none). */
+FS_API const char* fs_last_error(void);
+
+/*
+ * Noise inspection: for rows [row0, row0 + n_rows) and global vocabulary ids
+ * [v0, v0 + n_vocab), write the 32-bit Philox draw (words, nullable) and the
+ * Gumbel value the sampling kernels add (gumbel, nullable), row-major
+ * [n_rows, n_vocab], device pointers.  For parity tests of the noise stage.
+ */
+FS_API fs_status fs_debug_noise(uint64_t seed, uint64_t step, int64_t row0, int64_t n_rows,
+                         int64_t v0, int64_t n_vocab, uint32_t* words, float* gumbel,
+                         void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FLASHSAMPLE_H_ */

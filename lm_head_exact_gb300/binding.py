@@ -1,0 +1,240 @@
+"""ctypes binding of libflashsample (include/flashsample.h).
+
+Argument marshalling only: every step of sampling runs in the library's CUDA
+kernels.  PyTorch provides device memory and the current stream.  If the
+library is missing, or a tensor is not on a CUDA device, the call raises --
+there is no CPU fallback.
+"""
+
+import ctypes
+import os
+
+import numpy as np
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libflashsample.so")
+
+FS_OK = 0
+FS_CHUNK_FIRST = 1
+FS_CHUNK_LAST = 2
+FS_PATH_AUTO, FS_PATH_SIMT, FS_PATH_TC_VOCAB, FS_PATH_TC_BATCH = 0, 1, 2, 3
+
+_c_void_p = ctypes.c_void_p
+_i64 = ctypes.c_int64
+_u64 = ctypes.c_uint64
+_int = ctypes.c_int
+
+# name -> (restype, argtypes); mirrors include/flashsample.h
+SIGNATURES = {
+    "fs_sample": (_int, [_c_void_p, _c_void_p, _i64, _i64, _i64, _c_void_p, _u64, _u64,
+                         _c_void_p, _c_void_p, _c_void_p]),
+    "fs_sample_ex": (_int, [_c_void_p, _c_void_p, _i64, _i64, _i64, _c_void_p, _c_void_p, _i64,
+                            _u64, _u64, _c_void_p, _c_void_p, _c_void_p]),
+    "fs_sample_chunked": (_int, [_c_void_p, _c_void_p, _i64, _i64, _i64, _i64, _c_void_p,
+                                 _c_void_p, _i64, _u64, _u64, _c_void_p, _c_void_p, _int,
+                                 _c_void_p, _c_void_p, _c_void_p]),
+    "fs_sample_host": (_int, [_c_void_p, _c_void_p, _i64, _i64, _i64, _c_void_p, _c_void_p, _i64,
+                              _u64, _u64, _c_void_p, _c_void_p, _c_void_p]),
+    "fs_workspace_bytes": (ctypes.c_size_t, [_i64, _i64]),
+    "fs_workspace_reserve": (_int, [_i64, _i64, _c_void_p]),
+    "fs_workspace_release": (_int, []),
+    "fs_set_path": (_int, [_int]),
+    "fs_path_for_batch": (_int, [_i64]),
+    "fs_profile_events": (_int, [_c_void_p, _c_void_p]),
+    "fs_device_error": (_int, [ctypes.POINTER(_int)]),
+    "fs_status_string": (ctypes.c_char_p, [_int]),
+    "fs_last_error": (ctypes.c_char_p, []),
+    "fs_debug_noise": (_int, [_u64, _u64, _i64, _i64, _i64, _i64, _c_void_p, _c_void_p, _c_void_p]),
+}
+
+
+class FlashSampleError(RuntimeError):
+    """A libflashsample call returned a non-OK status (or the library is missing)."""
+
+    def __init__(self, status, detail):
+        self.status = status
+        super().__init__(f"{status}: {detail}")
+
+
+_lib = None
+
+
+def library():
+    """Load libflashsample.so (once) and declare its signatures."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise FlashSampleError("NOT_BUILT", f"{LIB_PATH} is missing; build it with "
+                                   "`python -m lm_head_exact_gb300.build` (there is no CPU fallback)")
+        lib = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def check(status):
+    if status != FS_OK:
+        lib = library()
+        raise FlashSampleError(lib.fs_status_string(status).decode(), lib.fs_last_error().decode())
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _stream_ptr(stream):
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dev(t, name, dtype=None, ndim=None):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise FlashSampleError("FS_ERR_INVALID_ARG", f"{name} must be a CUDA tensor (no CPU fallback)")
+    if dtype is not None and t.dtype != dtype:
+        raise FlashSampleError("FS_ERR_INVALID_ARG", f"{name} must be {dtype}, got {t.dtype}")
+    if ndim is not None and t.dim() != ndim:
+        raise FlashSampleError("FS_ERR_INVALID_ARG", f"{name} must have {ndim} dims")
+    if not t.is_contiguous():
+        raise FlashSampleError("FS_ERR_INVALID_ARG", f"{name} must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _bias_args(bias, B, V):
+    if bias is None:
+        return ctypes.c_void_p(0), 0
+    torch = _torch()
+    ptr = _dev(bias, "bias", torch.float32)
+    if bias.dim() == 1:
+        return ptr, 0
+    return ptr, bias.stride(0)
+
+
+def _outs(B, device, out):
+    torch = _torch()
+    if out is not None:
+        return out
+    return (torch.empty(B, dtype=torch.int64, device=device),
+            torch.empty(B, dtype=torch.float32, device=device))
+
+
+def sample(h, W, temp, seed, step, bias=None, out=None, stream=None):
+    """Fused LM-head exact sample of one decode step.
+
+    h: bf16 [B, d], W: bf16 [V, d], temp: fp32 [B] (CUDA tensors); bias:
+    optional fp32 [B, V] or [V].  Returns (ids int64 [B], max fp32 [B]) on
+    the device, enqueued on the current stream.
+    """
+    torch = _torch()
+    B, d = h.shape
+    V = W.shape[0]
+    ids, mx = _outs(B, h.device, out)
+    bptr, bstride = _bias_args(bias, B, V)
+    check(library().fs_sample_ex(_dev(h, "h", torch.bfloat16, 2), _dev(W, "W", torch.bfloat16, 2),
+                                 B, d, V, _dev(temp, "temp", torch.float32, 1), bptr, bstride,
+                                 seed, step, _dev(ids, "out_ids", torch.int64),
+                                 _dev(mx, "out_max", torch.float32), _stream_ptr(stream)))
+    return ids, mx
+
+
+def sample_ex(*args, **kwargs):
+    """Alias of ``sample`` (the bias argument maps to fs_sample_ex)."""
+    return sample(*args, **kwargs)
+
+
+def sample_chunked(h, W_chunk, v_begin, temp, seed, step, carry_max, carry_ids, first, last,
+                   bias_chunk=None, out=None, stream=None):
+    """One chunk [v_begin, v_begin + W_chunk.shape[0]) of the grouped online
+    variant; updates (carry_max, carry_ids) in place and, when ``last``,
+    returns (ids, max)."""
+    torch = _torch()
+    B, d = h.shape
+    v_end = v_begin + W_chunk.shape[0]
+    flags = (FS_CHUNK_FIRST if first else 0) | (FS_CHUNK_LAST if last else 0)
+    ids = mx = None
+    if last:
+        ids, mx = _outs(B, h.device, out)
+    bptr, bstride = _bias_args(bias_chunk, B, W_chunk.shape[0])
+    check(library().fs_sample_chunked(
+        _dev(h, "h", torch.bfloat16, 2), _dev(W_chunk, "W_chunk", torch.bfloat16, 2), B, d,
+        v_begin, v_end, _dev(temp, "temp", torch.float32, 1), bptr, bstride, seed, step,
+        _dev(carry_max, "carry_max", torch.float32), _dev(carry_ids, "carry_ids", torch.int64),
+        flags, _dev(ids, "out_ids") if last else ctypes.c_void_p(0),
+        _dev(mx, "out_max") if last else ctypes.c_void_p(0), _stream_ptr(stream)))
+    return (ids, mx) if last else None
+
+
+def sample_host(h_host, W, temp_host, seed, step, bias=None, out_ids=None, out_max=None,
+                stream=None):
+    """End-to-end call with host buffers (numpy arrays or CPU tensors; pinned
+    memory recommended): h_host bf16 bits uint16 [B, d] (or a bf16 tensor),
+    temp_host fp32 [B]; W (and bias) stay on the device.  Copies in, samples,
+    copies out and synchronizes.  Returns host (ids int64 [B], max fp32 [B])."""
+    torch = _torch()
+
+    def host_ptr(a, name):
+        if isinstance(a, np.ndarray):
+            if not a.flags["C_CONTIGUOUS"]:
+                raise FlashSampleError("FS_ERR_INVALID_ARG", f"{name} must be C-contiguous")
+            return ctypes.c_void_p(a.ctypes.data)
+        if isinstance(a, torch.Tensor) and not a.is_cuda and a.is_contiguous():
+            return ctypes.c_void_p(a.data_ptr())
+        raise FlashSampleError("FS_ERR_INVALID_ARG", f"{name} must be a contiguous host array")
+
+    B, d = h_host.shape
+    V = W.shape[0]
+    if out_ids is None:
+        out_ids = np.empty(B, dtype=np.int64)
+    if out_max is None:
+        out_max = np.empty(B, dtype=np.float32)
+    bptr, bstride = _bias_args(bias, B, V)
+    check(library().fs_sample_host(host_ptr(h_host, "h_host"), _dev(W, "W", torch.bfloat16, 2),
+                                   B, d, V, host_ptr(temp_host, "temp_host"), bptr, bstride,
+                                   seed, step, host_ptr(out_ids, "out_ids"),
+                                   host_ptr(out_max, "out_max"), _stream_ptr(stream)))
+    return out_ids, out_max
+
+
+def debug_noise(seed, step, row0, n_rows, v0, n_vocab, stream=None):
+    """(words uint32-as-int32 [n_rows, n_vocab], gumbel fp32 [n_rows, n_vocab])
+    exactly as the sampling kernels draw them."""
+    torch = _torch()
+    words = torch.empty((n_rows, n_vocab), dtype=torch.int32, device="cuda")
+    g = torch.empty((n_rows, n_vocab), dtype=torch.float32, device="cuda")
+    check(library().fs_debug_noise(seed, step, row0, n_rows, v0, n_vocab,
+                                   ctypes.c_void_p(words.data_ptr()), ctypes.c_void_p(g.data_ptr()),
+                                   _stream_ptr(stream)))
+    return words, g
+
+
+def set_path(path):
+    check(library().fs_set_path(path))
+
+
+def path_for_batch(B):
+    return library().fs_path_for_batch(B)
+
+
+def workspace_reserve(B, V, stream=None):
+    check(library().fs_workspace_reserve(B, V, _stream_ptr(stream)))
+
+
+def profile_events(start, stop):
+    """Record torch.cuda.Event ``start``/``stop`` around the fused kernel of
+    every later call on this thread (None, None to stop)."""
+    if start is None:
+        check(library().fs_profile_events(None, None))
+    else:
+        check(library().fs_profile_events(ctypes.c_void_p(start.cuda_event),
+                                          ctypes.c_void_p(stop.cuda_event)))
+
+
+def device_error():
+    code = ctypes.c_int(0)
+    check(library().fs_device_error(ctypes.byref(code)))
+    return code.value

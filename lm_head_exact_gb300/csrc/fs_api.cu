@@ -1,0 +1,423 @@
+// The C ABI of libflashsample: argument validation, per-(device, stream)
+// workspace, kernel-family dispatch by batch size, and the host-buffer
+// end-to-end entry point.  Declarations and contracts: include/flashsample.h.
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include "../../include/flashsample.h"
+#include "fs_internal.h"
+
+namespace fs {
+namespace {
+
+thread_local char g_last_error[512] = "";
+thread_local cudaEvent_t g_prof_start = nullptr;
+thread_local cudaEvent_t g_prof_stop = nullptr;
+std::atomic<int> g_forced_path{kPathAuto};
+
+fs_status fail(fs_status s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+fs_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(FS_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+// ---------------------------------------------------------------- workspace
+struct Workspace {
+  void* partials = nullptr;
+  size_t partial_bytes = 0;
+  void* staging = nullptr;      // device staging of fs_sample_host
+  size_t staging_bytes = 0;
+};
+
+std::mutex g_ws_mutex;
+std::map<std::pair<int, cudaStream_t>, Workspace> g_workspaces;
+
+int num_sms(int device) {
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess || sms <= 0)
+    sms = 148;
+  return sms;
+}
+
+// Upper bound of the candidates per row any kernel family produces for a
+// vocabulary of V rows (used to size reservations ahead of graph capture).
+int64_t max_parts(int64_t V, int device) {
+  const int64_t simt = std::min<int64_t>(static_cast<int64_t>(num_sms(device)) * 8, (V + 7) / 8);
+  return std::max<int64_t>(simt, 1);
+}
+
+size_t partial_bytes(int64_t B, int64_t parts) {
+  return static_cast<size_t>(std::max<int64_t>(B, 1)) * static_cast<size_t>(std::max<int64_t>(parts, 1)) *
+         sizeof(Partial);
+}
+
+bool capturing(cudaStream_t stream) {
+  cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &st) != cudaSuccess) return false;
+  return st != cudaStreamCaptureStatusNone;
+}
+
+// Make `*buf` hold at least `need` bytes; growth synchronizes the stream so
+// that no in-flight kernel still uses the old buffer.
+fs_status grow(void** buf, size_t* have, size_t need, cudaStream_t stream) {
+  if (*have >= need) return FS_OK;
+  if (capturing(stream))
+    return fail(FS_ERR_WORKSPACE, "workspace must grow to %zu bytes during stream capture; "
+                "call fs_workspace_reserve() before capturing", need);
+  if (*buf != nullptr) {
+    cudaStreamSynchronize(stream);
+    cudaFree(*buf);
+    *buf = nullptr;
+    *have = 0;
+  }
+  cudaError_t e = cudaMalloc(buf, need);
+  if (e != cudaSuccess) {
+    *buf = nullptr;
+    cudaGetLastError();
+    return fail(FS_ERR_WORKSPACE, "cudaMalloc(%zu) for the workspace failed: %s", need,
+                cudaGetErrorString(e));
+  }
+  *have = need;
+  return FS_OK;
+}
+
+fs_status current_device(int* dev) {
+  cudaError_t e = cudaGetDevice(dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  return FS_OK;
+}
+
+fs_status get_partials(cudaStream_t stream, size_t bytes, Partial** out) {
+  int dev;
+  fs_status s = current_device(&dev);
+  if (s != FS_OK) return s;
+  std::lock_guard<std::mutex> lock(g_ws_mutex);
+  Workspace& ws = g_workspaces[{dev, stream}];
+  s = grow(&ws.partials, &ws.partial_bytes, bytes, stream);
+  if (s != FS_OK) return s;
+  *out = static_cast<Partial*>(ws.partials);
+  return FS_OK;
+}
+
+// ---------------------------------------------------------------- checks
+fs_status check_device_ptr(const void* p, const char* name) {
+  if (p == nullptr) return fail(FS_ERR_INVALID_ARG, "%s is NULL", name);
+  cudaPointerAttributes attr;
+  cudaError_t e = cudaPointerGetAttributes(&attr, p);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return cuda_fail(e, "cudaPointerGetAttributes");
+  }
+  if (attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged)
+    return fail(FS_ERR_INVALID_ARG, "%s is not device memory", name);
+  int dev = -1;
+  cudaGetDevice(&dev);
+  if (attr.type == cudaMemoryTypeDevice && attr.device != dev)
+    return fail(FS_ERR_INVALID_ARG, "%s lives on device %d, current device is %d", name,
+                attr.device, dev);
+  return FS_OK;
+}
+
+fs_status check_aligned(const void* p, size_t a, const char* name) {
+  if (reinterpret_cast<uintptr_t>(p) % a != 0)
+    return fail(FS_ERR_UNSUPPORTED, "%s must be %zu-byte aligned", name, a);
+  return FS_OK;
+}
+
+#define FS_TRY(expr)                  \
+  do {                                \
+    fs_status _s = (expr);            \
+    if (_s != FS_OK) return _s;       \
+  } while (0)
+
+fs_status check_shapes(int64_t B, int64_t d, int64_t V) {
+  if (B < 0 || d <= 0 || V < 0) return fail(FS_ERR_INVALID_ARG, "need B >= 0, d > 0, V >= 0 (got %lld, %lld, %lld)",
+                                            (long long)B, (long long)d, (long long)V);
+  if (B >= (int64_t(1) << 31) || V >= (int64_t(1) << 31))
+    return fail(FS_ERR_UNSUPPORTED, "B and V must be < 2^31");
+  if (d % 8 != 0) return fail(FS_ERR_UNSUPPORTED, "d must be a multiple of 8 (got %lld)", (long long)d);
+  if (d > 65536) return fail(FS_ERR_UNSUPPORTED, "d must be <= 65536 (got %lld)", (long long)d);
+  return FS_OK;
+}
+
+fs_status check_problem(const Problem& p, bool need_out, const void* out_ids, const void* out_max) {
+  FS_TRY(check_shapes(p.B, p.d, p.V_local));
+  if (p.B == 0) return FS_OK;
+  FS_TRY(check_device_ptr(p.h, "h"));
+  FS_TRY(check_aligned(p.h, 16, "h"));
+  FS_TRY(check_device_ptr(p.temp, "temp"));
+  FS_TRY(check_aligned(p.temp, 4, "temp"));
+  if (p.V_local > 0) {
+    FS_TRY(check_device_ptr(p.W, "W"));
+    FS_TRY(check_aligned(p.W, 16, "W"));
+  }
+  if (p.bias != nullptr) {
+    if (p.bias_stride != 0 && p.bias_stride < p.V_local)
+      return fail(FS_ERR_INVALID_ARG, "bias_row_stride must be 0 or >= V");
+    if (p.bias_stride < 0) return fail(FS_ERR_INVALID_ARG, "bias_row_stride must be >= 0");
+    FS_TRY(check_device_ptr(p.bias, "bias"));
+    FS_TRY(check_aligned(p.bias, 4, "bias"));
+  }
+  if (need_out) {
+    FS_TRY(check_device_ptr(out_ids, "out_ids"));
+    FS_TRY(check_aligned(out_ids, 8, "out_ids"));
+    FS_TRY(check_device_ptr(out_max, "out_max"));
+    FS_TRY(check_aligned(out_max, 4, "out_max"));
+  }
+  return FS_OK;
+}
+
+int resolve_path(int64_t B) {
+  const int forced = g_forced_path.load();
+  if (forced != kPathAuto) return forced;
+  (void)B;
+  return kPathSimt;
+}
+
+// Fused kernel + cross-part reduction for one problem.
+fs_status run(const Problem& p, Finish f, cudaStream_t stream) {
+  if (p.B == 0) return FS_OK;
+  int dev;
+  FS_TRY(current_device(&dev));
+  const int path = resolve_path(p.B);
+  int n_parts = 0;
+  if (p.V_local > 0) {
+    switch (path) {
+      case kPathSimt:
+      default:
+        n_parts = simt_num_parts(p, dev);
+        break;
+    }
+  }
+  Partial* partials = nullptr;
+  FS_TRY(get_partials(stream, partial_bytes(p.B, n_parts), &partials));
+  f.partials = partials;
+  f.n_parts = n_parts;
+  if (p.V_local > 0) {
+    cudaError_t e = cudaSuccess;
+    if (g_prof_start != nullptr) {
+      e = cudaEventRecord(g_prof_start, stream);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord(start)");
+    }
+    switch (path) {
+      case kPathSimt:
+      default:
+        e = launch_simt(p, partials, n_parts, stream);
+        break;
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "fused sampling kernel launch");
+    if (g_prof_stop != nullptr) {
+      e = cudaEventRecord(g_prof_stop, stream);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord(stop)");
+    }
+  }
+  cudaError_t e = launch_reduce(f, p.B, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "reduction kernel launch");
+  return FS_OK;
+}
+
+}  // namespace
+}  // namespace fs
+
+using namespace fs;
+
+extern "C" {
+
+fs_status fs_sample_ex(const void* h, const void* W, int64_t B, int64_t d, int64_t V,
+                       const float* temp, const float* bias, int64_t bias_row_stride,
+                       uint64_t seed, uint64_t step,
+                       int64_t* out_ids, float* out_max, void* stream) {
+  g_last_error[0] = '\0';
+  Problem p{h, W, B, d, V, 0, temp, bias, bias_row_stride, seed, step};
+  FS_TRY(check_problem(p, true, out_ids, out_max));
+  Finish f{};
+  f.write_out = true;
+  f.out_ids = out_ids;
+  f.out_max = out_max;
+  return run(p, f, static_cast<cudaStream_t>(stream));
+}
+
+fs_status fs_sample(const void* h, const void* W, int64_t B, int64_t d, int64_t V,
+                    const float* temp, uint64_t seed, uint64_t step,
+                    int64_t* out_ids, float* out_max, void* stream) {
+  return fs_sample_ex(h, W, B, d, V, temp, nullptr, 0, seed, step, out_ids, out_max, stream);
+}
+
+fs_status fs_sample_chunked(const void* h, const void* W_chunk, int64_t B, int64_t d,
+                            int64_t v_begin, int64_t v_end, const float* temp,
+                            const float* bias_chunk, int64_t bias_row_stride,
+                            uint64_t seed, uint64_t step,
+                            float* carry_max, int64_t* carry_ids, int flags,
+                            int64_t* out_ids, float* out_max, void* stream) {
+  g_last_error[0] = '\0';
+  if (v_begin < 0 || v_end < v_begin)
+    return fail(FS_ERR_INVALID_ARG, "need 0 <= v_begin <= v_end (got %lld, %lld)",
+                (long long)v_begin, (long long)v_end);
+  if (v_end >= (int64_t(1) << 31)) return fail(FS_ERR_UNSUPPORTED, "v_end must be < 2^31");
+  if (flags & ~(FS_CHUNK_FIRST | FS_CHUNK_LAST)) return fail(FS_ERR_INVALID_ARG, "unknown flags 0x%x", flags);
+  const bool last = (flags & FS_CHUNK_LAST) != 0;
+  Problem p{h, W_chunk, B, d, v_end - v_begin, v_begin, temp, bias_chunk, bias_row_stride, seed, step};
+  FS_TRY(check_problem(p, last, out_ids, out_max));
+  if (B > 0) {
+    FS_TRY(check_device_ptr(carry_max, "carry_max"));
+    FS_TRY(check_aligned(carry_max, 4, "carry_max"));
+    FS_TRY(check_device_ptr(carry_ids, "carry_ids"));
+    FS_TRY(check_aligned(carry_ids, 8, "carry_ids"));
+  }
+  Finish f{};
+  f.carry_max = carry_max;
+  f.carry_ids = carry_ids;
+  f.carry_in = (flags & FS_CHUNK_FIRST) == 0;
+  f.write_out = last;
+  f.out_ids = out_ids;
+  f.out_max = out_max;
+  return run(p, f, static_cast<cudaStream_t>(stream));
+}
+
+fs_status fs_sample_host(const void* h_host, const void* W, int64_t B, int64_t d, int64_t V,
+                         const float* temp_host, const float* bias, int64_t bias_row_stride,
+                         uint64_t seed, uint64_t step,
+                         int64_t* out_ids_host, float* out_max_host, void* stream_) {
+  g_last_error[0] = '\0';
+  FS_TRY(check_shapes(B, d, V));
+  if (B == 0) return FS_OK;
+  if (!h_host || !temp_host || !out_ids_host || !out_max_host)
+    return fail(FS_ERR_INVALID_ARG, "host buffers must not be NULL");
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  int dev;
+  FS_TRY(current_device(&dev));
+  const size_t h_bytes = static_cast<size_t>(B) * d * 2;
+  const size_t off_temp = (h_bytes + 255) & ~size_t(255);
+  const size_t off_ids = off_temp + ((static_cast<size_t>(B) * 4 + 255) & ~size_t(255));
+  const size_t off_max = off_ids + ((static_cast<size_t>(B) * 8 + 255) & ~size_t(255));
+  const size_t total = off_max + static_cast<size_t>(B) * 4;
+  char* staging = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_ws_mutex);
+    Workspace& ws = g_workspaces[{dev, stream}];
+    FS_TRY(grow(&ws.staging, &ws.staging_bytes, total, stream));
+    staging = static_cast<char*>(ws.staging);
+  }
+  cudaError_t e = cudaMemcpyAsync(staging, h_host, h_bytes, cudaMemcpyHostToDevice, stream);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(staging + off_temp, temp_host, static_cast<size_t>(B) * 4,
+                        cudaMemcpyHostToDevice, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "host-to-device copy");
+  fs_status s = fs_sample_ex(staging, W, B, d, V, reinterpret_cast<const float*>(staging + off_temp),
+                             bias, bias_row_stride, seed, step,
+                             reinterpret_cast<int64_t*>(staging + off_ids),
+                             reinterpret_cast<float*>(staging + off_max), stream);
+  if (s != FS_OK) return s;
+  e = cudaMemcpyAsync(out_ids_host, staging + off_ids, static_cast<size_t>(B) * 8,
+                      cudaMemcpyDeviceToHost, stream);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(out_max_host, staging + off_max, static_cast<size_t>(B) * 4,
+                        cudaMemcpyDeviceToHost, stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return cuda_fail(e, "device-to-host copy");
+  return FS_OK;
+}
+
+size_t fs_workspace_bytes(int64_t B, int64_t V) {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  return partial_bytes(B, max_parts(V, dev));
+}
+
+fs_status fs_workspace_reserve(int64_t B, int64_t V, void* stream) {
+  g_last_error[0] = '\0';
+  if (B < 0 || V < 0) return fail(FS_ERR_INVALID_ARG, "need B >= 0 and V >= 0");
+  int dev;
+  FS_TRY(current_device(&dev));
+  Partial* p = nullptr;
+  return get_partials(static_cast<cudaStream_t>(stream), partial_bytes(B, max_parts(V, dev)), &p);
+}
+
+fs_status fs_workspace_release(void) {
+  int dev;
+  FS_TRY(current_device(&dev));
+  std::lock_guard<std::mutex> lock(g_ws_mutex);
+  for (auto it = g_workspaces.begin(); it != g_workspaces.end();) {
+    if (it->first.first == dev) {
+      cudaStreamSynchronize(it->first.second);
+      if (it->second.partials) cudaFree(it->second.partials);
+      if (it->second.staging) cudaFree(it->second.staging);
+      it = g_workspaces.erase(it);
+    } else {
+      ++it;
+    }
+  }
+  return FS_OK;
+}
+
+fs_status fs_set_path(int path) {
+  if (path < FS_PATH_AUTO || path > FS_PATH_TC_BATCH) return fail(FS_ERR_INVALID_ARG, "unknown path %d", path);
+  if (path == FS_PATH_TC_VOCAB || path == FS_PATH_TC_BATCH)
+    return fail(FS_ERR_UNSUPPORTED, "kernel family %d is not built in this library", path);
+  g_forced_path.store(path);
+  return FS_OK;
+}
+
+int fs_path_for_batch(int64_t B) { return resolve_path(B); }
+
+fs_status fs_profile_events(void* start, void* stop) {
+  if ((start == nullptr) != (stop == nullptr))
+    return fail(FS_ERR_INVALID_ARG, "pass both events or neither");
+  g_prof_start = static_cast<cudaEvent_t>(start);
+  g_prof_stop = static_cast<cudaEvent_t>(stop);
+  return FS_OK;
+}
+
+fs_status fs_device_error(int* code) {
+  if (code == nullptr) return fail(FS_ERR_INVALID_ARG, "code is NULL");
+  *code = 0;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+  return FS_OK;
+}
+
+const char* fs_status_string(fs_status s) {
+  switch (s) {
+    case FS_OK: return "FS_OK";
+    case FS_ERR_INVALID_ARG: return "FS_ERR_INVALID_ARG";
+    case FS_ERR_UNSUPPORTED: return "FS_ERR_UNSUPPORTED";
+    case FS_ERR_CUDA: return "FS_ERR_CUDA";
+    case FS_ERR_WORKSPACE: return "FS_ERR_WORKSPACE";
+    case FS_ERR_DEVICE_TIMEOUT: return "FS_ERR_DEVICE_TIMEOUT";
+  }
+  return "FS_STATUS_UNKNOWN";
+}
+
+const char* fs_last_error(void) { return g_last_error; }
+
+fs_status fs_debug_noise(uint64_t seed, uint64_t step, int64_t row0, int64_t n_rows,
+                         int64_t v0, int64_t n_vocab, uint32_t* words, float* gumbel,
+                         void* stream) {
+  g_last_error[0] = '\0';
+  if (row0 < 0 || n_rows < 0 || v0 < 0 || n_vocab < 0)
+    return fail(FS_ERR_INVALID_ARG, "negative range");
+  if (row0 + n_rows > (int64_t(1) << 32) || v0 + n_vocab > (int64_t(1) << 31))
+    return fail(FS_ERR_UNSUPPORTED, "rows must be < 2^32 and vocabulary ids < 2^31");
+  if (n_rows * n_vocab == 0) return FS_OK;
+  if (words) FS_TRY(check_device_ptr(words, "words"));
+  if (gumbel) FS_TRY(check_device_ptr(gumbel, "gumbel"));
+  cudaError_t e = launch_debug_noise(seed, step, row0, n_rows, v0, n_vocab, words, gumbel,
+                                     static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "noise kernel launch");
+  return FS_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,183 @@
+// SIMT fused LM-head sampler: the W-streaming path for very small batches.
+//
+// FlashSampling: Fast and Memory-Efficient Exact Sampling -- summary page,
+// "Method": logits are formed on chip, perturbed with Gumbel noise, and only a
+// per-row (max, argmax) survives; the B x V logits never reach HBM.
+//
+// Design: every warp owns whole vocabulary rows.  A row of W (d bf16) is read
+// once with 16-byte coalesced loads, dotted against the (at most BG) rows of h
+// that the block keeps in shared memory, and reduced across the warp.  Lanes
+// 0..BG-1 then own one batch row each: they scale by 1/T, add the row's
+// Philox-Gumbel draw and keep the running (max, argmax) in registers.  Each
+// block writes one candidate per batch row to the partial buffer; the
+// cross-part reduction kernel finishes the sample.
+#include <algorithm>
+
+#include "fs_internal.h"
+
+namespace fs {
+namespace {
+
+constexpr int kSimtThreads = 256;
+constexpr int kSimtWarps = kSimtThreads / 32;
+constexpr int kSimtUnroll = 4;
+
+__device__ __forceinline__ void bf16x2_to_f32(uint32_t w, float& lo, float& hi) {
+  lo = __uint_as_float(w << 16);
+  hi = __uint_as_float(w & 0xffff0000u);
+}
+
+__device__ __forceinline__ float dot8(uint4 a, uint4 b, float acc) {
+  float a0, a1, b0, b1;
+  bf16x2_to_f32(a.x, a0, a1); bf16x2_to_f32(b.x, b0, b1);
+  acc = fmaf(a0, b0, acc); acc = fmaf(a1, b1, acc);
+  bf16x2_to_f32(a.y, a0, a1); bf16x2_to_f32(b.y, b0, b1);
+  acc = fmaf(a0, b0, acc); acc = fmaf(a1, b1, acc);
+  bf16x2_to_f32(a.z, a0, a1); bf16x2_to_f32(b.z, b0, b1);
+  acc = fmaf(a0, b0, acc); acc = fmaf(a1, b1, acc);
+  bf16x2_to_f32(a.w, a0, a1); bf16x2_to_f32(b.w, b0, b1);
+  acc = fmaf(a0, b0, acc); acc = fmaf(a1, b1, acc);
+  return acc;
+}
+
+template <int BG>
+__global__ void __launch_bounds__(kSimtThreads)
+simt_fused_kernel(Problem p, Partial* __restrict__ partials, int n_parts) {
+  extern __shared__ uint4 smem_h[];            // [BG][d/8] bf16x8 packets
+  __shared__ Best warp_best[kSimtWarps][BG];
+
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int64_t n16 = p.d / 8;                 // 16-byte packets per row
+  const int64_t n_groups = (p.B + BG - 1) / BG;
+  const PhiloxKey key{static_cast<uint32_t>(p.seed), static_cast<uint32_t>(p.seed >> 32)};
+  const uint32_t step_lo = static_cast<uint32_t>(p.step);
+  const uint32_t step_hi = static_cast<uint32_t>(p.step >> 32);
+  const uint4* hg = reinterpret_cast<const uint4*>(p.h);
+  const uint4* Wg = reinterpret_cast<const uint4*>(p.W);
+  const int64_t warp_stride = static_cast<int64_t>(n_parts) * kSimtWarps;
+
+  for (int64_t g = blockIdx.y; g < n_groups; g += gridDim.y) {
+    const int64_t b0 = g * BG;
+    __syncthreads();                           // previous group's readers are done
+    // Stage this group's rows of h (zero rows past the batch).
+    for (int64_t i = threadIdx.x; i < BG * n16; i += kSimtThreads) {
+      const int64_t r = i / n16;
+      smem_h[i] = (b0 + r < p.B) ? hg[(b0 + r) * n16 + (i - r * n16)] : make_uint4(0, 0, 0, 0);
+    }
+
+    // Lane l < BG owns batch row b0 + l for the epilogue.
+    const int64_t my_b = b0 + lane;
+    const bool owns_row = lane < BG && my_b < p.B;
+    const RowTemp rt = row_temp(owns_row ? p.temp[my_b] : -1.0f);
+    Best best = best_none();
+    __syncthreads();
+
+    for (int64_t v = static_cast<int64_t>(blockIdx.x) * kSimtWarps + warp; v < p.V_local;
+         v += warp_stride) {
+      const uint4* wrow = Wg + v * n16;
+      float acc[BG];
+#pragma unroll
+      for (int b = 0; b < BG; ++b) acc[b] = 0.0f;
+
+      int64_t i = lane;
+      for (; i + 32 * (kSimtUnroll - 1) < n16; i += 32 * kSimtUnroll) {
+        uint4 w[kSimtUnroll];
+#pragma unroll
+        for (int u = 0; u < kSimtUnroll; ++u) w[u] = __ldg(wrow + i + 32 * u);
+#pragma unroll
+        for (int u = 0; u < kSimtUnroll; ++u) {
+#pragma unroll
+          for (int b = 0; b < BG; ++b) acc[b] = dot8(w[u], smem_h[b * n16 + i + 32 * u], acc[b]);
+        }
+      }
+      for (; i < n16; i += 32) {
+        const uint4 w = __ldg(wrow + i);
+#pragma unroll
+        for (int b = 0; b < BG; ++b) acc[b] = dot8(w, smem_h[b * n16 + i], acc[b]);
+      }
+#pragma unroll
+      for (int b = 0; b < BG; ++b) {
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) acc[b] += __shfl_xor_sync(0xffffffffu, acc[b], off);
+      }
+
+      if (owns_row && rt.mode != kRowInvalid) {
+        float logit = 0.0f;
+#pragma unroll
+        for (int b = 0; b < BG; ++b)
+          if (lane == b) logit = acc[b];
+        if (p.bias != nullptr) logit += p.bias[my_b * p.bias_stride + v];
+        const int64_t vg = p.v_offset + v;
+        float z = logit;
+        if (rt.mode == kRowSample) {
+          const uint4 words = noise_words(key, static_cast<uint32_t>(vg >> 2),
+                                          static_cast<uint32_t>(my_b), step_lo, step_hi);
+          z = fmaf(logit, rt.inv_t, gumbel_from_word(word_of(words, static_cast<uint32_t>(vg & 3))));
+        }
+        if (z > best.z) {  // ids rise within a warp, so strict > keeps the smaller id on ties
+          best.z = z;
+          best.id = static_cast<int32_t>(vg);
+        }
+      }
+    }
+
+    if (lane < BG) warp_best[warp][lane] = best;
+    __syncthreads();
+    if (threadIdx.x < BG && b0 + threadIdx.x < p.B) {
+      Best r = warp_best[0][threadIdx.x];
+#pragma unroll
+      for (int w = 1; w < kSimtWarps; ++w) r = combine(r, warp_best[w][threadIdx.x]);
+      Partial out;
+      out.z = r.z;
+      out.id = r.id;
+      partials[(b0 + threadIdx.x) * n_parts + blockIdx.x] = out;
+    }
+  }
+}
+
+int pick_group(int64_t B, int64_t d) {
+  int bg = 8;
+  while (bg > 1 && (bg / 2 >= B || static_cast<int64_t>(bg) * d * 2 > 128 * 1024)) bg /= 2;
+  return bg;
+}
+
+template <int BG>
+cudaError_t launch_group(const Problem& p, Partial* partials, int n_parts, cudaStream_t stream) {
+  const size_t smem = static_cast<size_t>(BG) * p.d * 2;
+  cudaError_t e = cudaFuncSetAttribute(simt_fused_kernel<BG>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  const int64_t groups = (p.B + BG - 1) / BG;
+  dim3 grid(n_parts, static_cast<unsigned>(std::min<int64_t>(groups, 65535)));
+  simt_fused_kernel<BG><<<grid, kSimtThreads, smem, stream>>>(p, partials, n_parts);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int simt_num_parts(const Problem& p, int device) {
+  int sms = 0;
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
+  if (sms <= 0) sms = 148;
+  const int bg = pick_group(p.B, p.d);
+  const int64_t smem = static_cast<int64_t>(bg) * p.d * 2;
+  int per_sm = static_cast<int>(std::min<int64_t>(2048 / kSimtThreads, (200 * 1024) / std::max<int64_t>(smem, 1)));
+  per_sm = std::max(per_sm, 1);
+  int64_t parts = static_cast<int64_t>(sms) * per_sm;
+  // never more blocks than 8-row groups of the vocabulary
+  parts = std::min<int64_t>(parts, std::max<int64_t>(1, (p.V_local + kSimtWarps - 1) / kSimtWarps));
+  return static_cast<int>(parts);
+}
+
+cudaError_t launch_simt(const Problem& p, Partial* partials, int n_parts, cudaStream_t stream) {
+  switch (pick_group(p.B, p.d)) {
+    case 1: return launch_group<1>(p, partials, n_parts, stream);
+    case 2: return launch_group<2>(p, partials, n_parts, stream);
+    case 4: return launch_group<4>(p, partials, n_parts, stream);
+    default: return launch_group<8>(p, partials, n_parts, stream);
+  }
+}
+
+}  // namespace fs

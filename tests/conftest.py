@@ -23,3 +23,30 @@ def pytest_configure(config):
 @pytest.fixture(scope="session")
 def repo_root():
     return ROOT
+
+
+@pytest.fixture(scope="session")
+def built_library():
+    """Path of libflashsample.so, (re)built in-tree if a source changed."""
+    from lm_head_exact_gb300.build import build
+    return build()
+
+
+@pytest.fixture(scope="session")
+def fs(built_library):
+    """The ctypes binding on a CUDA device (GPU tests only): fails loudly --
+    never skips -- when no device is present, so a GPU run cannot pass
+    without executing the kernels."""
+    import torch
+    assert torch.cuda.is_available(), "GPU test run without a CUDA device"
+    from lm_head_exact_gb300 import binding
+    binding.library()
+    binding.set_path(binding.FS_PATH_AUTO)
+    return binding
+
+
+@pytest.fixture(scope="session")
+def torch_cuda():
+    import torch
+    assert torch.cuda.is_available(), "GPU test run without a CUDA device"
+    return torch

@@ -1,0 +1,80 @@
+"""CPU checks of the C ABI: the library builds, loads without a GPU, exports
+every entry point include/flashsample.h declares, and rejects malformed
+arguments on the host before touching a device."""
+
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                      "include", "flashsample.h")
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^FS_API\s+[\w\s\*]+?\b(fs_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_api():
+    names = declared_symbols()
+    for required in ("fs_sample", "fs_sample_ex", "fs_sample_chunked", "fs_sample_host",
+                     "fs_status_string", "fs_debug_noise"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(built_library):
+    lib = ctypes.CDLL(built_library)
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+    out = subprocess.run(["nm", "-D", "--defined-only", built_library], capture_output=True, text=True)
+    if out.returncode == 0:
+        exported = set(re.findall(r" T (fs_\w+)$", out.stdout, flags=re.M))
+        assert set(declared_symbols()) <= exported
+        # nothing else of the fs_ namespace leaks out
+        assert exported <= set(declared_symbols())
+
+
+def test_binding_signatures_cover_the_header(built_library):
+    from lm_head_exact_gb300 import binding
+    assert set(binding.SIGNATURES) == set(declared_symbols())
+    binding.library()
+
+
+def test_status_strings(built_library):
+    from lm_head_exact_gb300 import binding
+    lib = binding.library()
+    names = [lib.fs_status_string(i).decode() for i in range(6)]
+    assert names == ["FS_OK", "FS_ERR_INVALID_ARG", "FS_ERR_UNSUPPORTED", "FS_ERR_CUDA",
+                     "FS_ERR_WORKSPACE", "FS_ERR_DEVICE_TIMEOUT"]
+    assert lib.fs_status_string(99).decode() == "FS_STATUS_UNKNOWN"
+
+
+def test_host_side_argument_checks(built_library):
+    from lm_head_exact_gb300 import binding
+    lib = binding.library()
+    z = ctypes.c_void_p(0)
+    # negative / unsupported shapes are refused before any CUDA call
+    assert lib.fs_sample(z, z, -1, 64, 10, z, 0, 0, z, z, z) == 1
+    assert "B >= 0" in lib.fs_last_error().decode()
+    assert lib.fs_sample(z, z, 4, 12, 10, z, 0, 0, z, z, z) == 2
+    assert "multiple of 8" in lib.fs_last_error().decode()
+    assert lib.fs_sample(z, z, 4, 64, 1 << 31, z, 0, 0, z, z, z) == 2
+    assert lib.fs_sample_chunked(z, z, 4, 64, 10, 5, z, z, 0, 0, 0, z, z, 1, z, z, z) == 1
+    assert lib.fs_sample_chunked(z, z, 4, 64, 0, 5, z, z, 0, 0, 0, z, z, 8, z, z, z) == 1
+    assert lib.fs_set_path(7) == 1
+    assert lib.fs_debug_noise(0, 0, -1, 1, 0, 1, z, z, z) == 1
+    # B == 0 is a no-op
+    assert lib.fs_sample(z, z, 0, 64, 10, z, 0, 0, z, z, z) == 0
+
+
+def test_product_path_refuses_cpu_tensors(built_library):
+    torch = pytest.importorskip("torch")
+    from lm_head_exact_gb300 import binding
+    h = torch.zeros(2, 8, dtype=torch.bfloat16)
+    W = torch.zeros(4, 8, dtype=torch.bfloat16)
+    t = torch.ones(2)
+    with pytest.raises(binding.FlashSampleError, match="CUDA tensor"):
+        binding.sample(h, W, t, 0, 0)

@@ -1,0 +1,92 @@
+"""GPU parity at the full workload sizes, in the launch configuration the
+benchmark times: Llama-3-8B-, Qwen3-8B- and Llama-3-70B-shaped LM heads and
+the chunked (grouped online) variant.  The GPU samples every row; the oracle
+recomputes a seeded subset of rows over the whole vocabulary in fp64.
+"""
+
+import numpy as np
+import pytest
+
+from _helpers import compare, to_device
+from oracle import sampler
+from lm_head_exact_gb300 import synthetic
+
+pytestmark = pytest.mark.gpu
+
+
+def _rows(B, k, seed, must=()):
+    rng = np.random.default_rng(seed)
+    rows = set(int(r) for r in rng.choice(B, size=min(k, B), replace=False))
+    rows.update(int(r) for r in must if r < B)
+    return np.array(sorted(rows))
+
+
+def _device(wl, torch):
+    return (to_device(wl.h, torch), to_device(wl.W, torch), to_device(wl.temp, torch),
+            None if wl.bias is None else to_device(wl.bias, torch))
+
+
+def test_llama3_8b_batch_sweep(fs, torch_cuda):
+    torch = torch_cuda
+    wl = synthetic.workload("llama3_8b", 64)
+    hd, Wd, td, _ = _device(wl, torch)
+    for step in (0, 57, 99):
+        ref = sampler.sample(wl.h, wl.W, wl.temp, wl.seed, step)
+        for B in synthetic.SHAPES["llama3_8b"]["batches"]:
+            ids, mx = fs.sample(hd[:B], Wd, td[:B], wl.seed, step)
+            torch.cuda.synchronize()
+            sub = sampler.Sample(ref.ids[:B], ref.zmax[:B], ref.gap[:B])
+            compare(ids.cpu().numpy(), mx.cpu().numpy(), sub, what=f"8B B={B} step={step}")
+
+
+def test_qwen3_8b_large_batch(fs, torch_cuda):
+    torch = torch_cuda
+    wl = synthetic.workload("qwen3_8b", 1024)
+    hd, Wd, td, _ = _device(wl, torch)
+    greedy_rows = np.nonzero(wl.temp == 0)[0]
+    for step in (0, 9):
+        for B in synthetic.SHAPES["qwen3_8b"]["batches"]:
+            rows = _rows(B, 24, seed=B + step, must=greedy_rows[:4])
+            ids, mx = fs.sample(hd[:B], Wd, td[:B], wl.seed, step)
+            torch.cuda.synchronize()
+            ref = sampler.sample(wl.h, wl.W, wl.temp, wl.seed, step, rows=rows)
+            compare(ids.cpu().numpy(), mx.cpu().numpy(), ref, rows=rows, what=f"qwen B={B} step={step}")
+
+
+def test_llama3_70b_with_bias(fs, torch_cuda):
+    torch = torch_cuda
+    wl = synthetic.workload("llama3_70b", 256)
+    hd, Wd, td, bd = _device(wl, torch)
+    step = 3
+    for B in synthetic.SHAPES["llama3_70b"]["batches"]:
+        rows = _rows(B, 16, seed=B)
+        ids, mx = fs.sample(hd[:B], Wd, td[:B], wl.seed, step, bias=bd[:B])
+        torch.cuda.synchronize()
+        ref = sampler.sample(wl.h, wl.W, wl.temp, wl.seed, step, bias=wl.bias, rows=rows)
+        compare(ids.cpu().numpy(), mx.cpu().numpy(), ref, rows=rows, what=f"70B B={B}")
+        # the +8 spikes dominate: most sampled ids are spike ids
+        spikes = wl.bias[:B] > 0
+        hit = spikes[np.arange(B), ids.cpu().numpy()]
+        assert hit.mean() > 0.5
+
+
+@pytest.mark.parametrize("n_chunks", [8, 32])
+def test_chunked_full_size(fs, torch_cuda, n_chunks):
+    torch = torch_cuda
+    wl = synthetic.workload("chunked", 256)
+    hd, Wd, td, _ = _device(wl, torch)
+    bounds = synthetic.chunk_bounds(wl.V, n_chunks)
+    step = 4
+    for B in synthetic.SHAPES["chunked"]["batches"]:
+        ids1, mx1 = fs.sample(hd[:B], Wd, td[:B], wl.seed, step)
+        cm = torch.empty(B, device="cuda")
+        ci = torch.empty(B, dtype=torch.int64, device="cuda")
+        for i, (lo, hi) in enumerate(zip(bounds[:-1], bounds[1:])):
+            res = fs.sample_chunked(hd[:B], Wd[lo:hi], lo, td[:B], wl.seed, step, cm, ci,
+                                    i == 0, i == n_chunks - 1)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(res[0].cpu().numpy(), ids1.cpu().numpy())
+        np.testing.assert_array_equal(res[1].cpu().numpy(), mx1.cpu().numpy())
+        rows = _rows(B, 16, seed=B)
+        ref = sampler.sample(wl.h, wl.W, wl.temp, wl.seed, step, rows=rows)
+        compare(res[0].cpu().numpy(), res[1].cpu().numpy(), ref, rows=rows, what=f"chunked B={B}")

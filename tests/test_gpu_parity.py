@@ -1,0 +1,215 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle on
+identical seeded inputs.
+
+Small cases are compared element by element over every row; the full-size
+workloads run in the launch configuration the benchmark times and are
+compared on sampled rows (the oracle computes each row over the whole
+vocabulary).  Comparison rule: tests/_helpers.py.
+"""
+
+import numpy as np
+import pytest
+
+from _helpers import compare, to_device
+from oracle import sampler
+from lm_head_exact_gb300 import synthetic
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(fs, torch, h, W, temp, seed, step, bias=None):
+    hd, Wd, td = to_device(h, torch), to_device(W, torch), to_device(temp, torch)
+    bd = None if bias is None else to_device(bias, torch)
+    ids, mx = fs.sample(hd, Wd, td, seed, step, bias=bd)
+    torch.cuda.synchronize()
+    return ids.cpu().numpy(), mx.cpu().numpy()
+
+
+def _problem(B, V, d, seed, w_std=0.05, temps=None):
+    rng = np.random.default_rng(seed)
+    h = synthetic.bf16_bits(rng.standard_normal((B, d)).astype(np.float32))
+    W = synthetic.bf16_bits((rng.standard_normal((V, d)) * w_std).astype(np.float32))
+    if temps is None:
+        temps = rng.uniform(0.3, 1.5, size=B).astype(np.float32)
+        temps[::7] = 0.0
+    return h, W, np.asarray(temps, np.float32)
+
+
+# ------------------------------------------------------------------ noise
+@pytest.mark.parametrize("row0,v0,step", [(0, 0, 0), (5, 3, 99), (1000, 151900, (3 << 32) + 17)])
+def test_noise_words_bit_exact(fs, torch_cuda, row0, v0, step):
+    n_rows, n_vocab = 33, 37
+    words, g = fs.debug_noise(1234, step, row0, n_rows, v0, n_vocab)
+    torch_cuda.cuda.synchronize()
+    ref = sampler.philox_words(1234, step, np.arange(row0, row0 + n_rows), np.arange(v0, v0 + n_vocab))
+    np.testing.assert_array_equal(words.cpu().numpy().view(np.uint32), ref)
+
+
+def test_gumbel_values_within_bound(fs, torch_cuda):
+    # 64 rows x 8192 ids cover ~5e5 draws, including u close to 0 and 1.
+    words, g = fs.debug_noise(77, 3, 0, 64, 0, 8192)
+    torch_cuda.cuda.synchronize()
+    w = words.cpu().numpy().view(np.uint32)
+    ref = sampler.gumbel_from_uniform(sampler.uniform_from_word(w))
+    err = np.abs(g.cpu().numpy().astype(np.float64) - ref)
+    assert err.max() < 1e-5, err.max()
+    assert np.isfinite(g.cpu().numpy()).all()
+
+
+# ------------------------------------------------------------------ small cases
+def test_tiny_workload(fs, torch_cuda):
+    wl = synthetic.tiny()
+    ids, mx = _run(fs, torch_cuda, wl.h, wl.W, wl.temp, wl.seed, 0)
+    ref = sampler.sample(wl.h, wl.W, wl.temp, wl.seed, 0)
+    compare(ids, mx, ref, what="tiny")
+    assert ids[0] == np.argmax(sampler.logits(wl.h, wl.W)[0])   # T = 0 row is greedy
+
+
+@pytest.mark.parametrize("B", [1, 3, 8, 17])
+@pytest.mark.parametrize("V,d", [(1, 8), (127, 64), (4097, 256), (1000, 8)])
+def test_ragged_shapes(fs, torch_cuda, B, V, d):
+    h, W, temp = _problem(B, V, d, seed=B * 7 + V)
+    for step in (0, 5):
+        ids, mx = _run(fs, torch_cuda, h, W, temp, 42, step)
+        compare(ids, mx, sampler.sample(h, W, temp, 42, step), what=f"B{B} V{V} d{d}")
+
+
+def test_many_steps_many_rows(fs, torch_cuda):
+    h, W, temp = _problem(64, 5000, 128, seed=3)
+    for step in range(0, 100, 9):
+        ids, mx = _run(fs, torch_cuda, h, W, temp, 1234, step)
+        compare(ids, mx, sampler.sample(h, W, temp, 1234, step), what=f"step {step}")
+
+
+def test_bias_per_row_and_shared(fs, torch_cuda):
+    B, V, d = 9, 3001, 64
+    h, W, temp = _problem(B, V, d, seed=11)
+    rng = np.random.default_rng(11)
+    bias = np.zeros((B, V), np.float32)
+    for b in range(B):
+        bias[b, rng.choice(V, 16, replace=False)] = 8.0
+    ids, mx = _run(fs, torch_cuda, h, W, temp, 9, 1, bias=bias)
+    compare(ids, mx, sampler.sample(h, W, temp, 9, 1, bias=bias), what="row bias")
+    shared = rng.standard_normal(V).astype(np.float32)
+    ids, mx = _run(fs, torch_cuda, h, W, temp, 9, 2, bias=shared)
+    compare(ids, mx, sampler.sample(h, W, temp, 9, 2, bias=shared), what="shared bias")
+
+
+def test_degenerate_rows(fs, torch_cuda):
+    B, V, d = 6, 300, 32
+    h, W, _ = _problem(B, V, d, seed=12)
+    W = W.copy()
+    W[10] = 0x7FC0                                    # NaN logits never win
+    temp = np.array([-1.0, np.nan, 0.0, 1.0, np.inf, 0.7], np.float32)
+    bias = np.zeros((B, V), np.float32)
+    bias[5, :] = -np.inf                              # nothing can win
+    ids, mx = _run(fs, torch_cuda, h, W, temp, 3, 4, bias=bias)
+    ref = sampler.sample(h, W, temp, 3, 4, bias=bias)
+    compare(ids, mx, ref, what="degenerate")
+    assert ids[0] == -1 and ids[1] == -1 and ids[5] == -1
+    assert 10 not in ids
+
+
+def test_empty_batch_and_empty_vocab(fs, torch_cuda):
+    torch = torch_cuda
+    h = torch.zeros((0, 64), dtype=torch.bfloat16, device="cuda")
+    W = torch.zeros((10, 64), dtype=torch.bfloat16, device="cuda")
+    t = torch.ones(0, device="cuda")
+    ids, mx = fs.sample(h, W, t, 0, 0)
+    assert ids.numel() == 0
+    h = torch.zeros((3, 64), dtype=torch.bfloat16, device="cuda")
+    W0 = torch.zeros((0, 64), dtype=torch.bfloat16, device="cuda")
+    ids, mx = fs.sample(h, W0, torch.ones(3, device="cuda"), 0, 0)
+    torch.cuda.synchronize()
+    assert ids.tolist() == [-1, -1, -1]
+    assert mx.tolist() == [-np.inf] * 3
+
+
+def test_ties_go_to_smaller_id(fs, torch_cuda):
+    rng = np.random.default_rng(13)
+    h = synthetic.bf16_bits(rng.standard_normal((4, 64)).astype(np.float32))
+    row = synthetic.bf16_bits(rng.standard_normal((1, 64)).astype(np.float32))
+    W = np.repeat(row, 2000, axis=0)                  # every logit identical
+    ids, _ = _run(fs, torch_cuda, h, W, np.zeros(4, np.float32), 1, 0)
+    np.testing.assert_array_equal(ids, 0)
+
+
+def test_invalid_arguments_are_rejected(fs, torch_cuda):
+    torch = torch_cuda
+    h = torch.zeros((2, 64), dtype=torch.bfloat16, device="cuda")
+    W = torch.zeros((10, 64), dtype=torch.bfloat16, device="cuda")
+    t = torch.ones(2, device="cuda")
+    with pytest.raises(fs.FlashSampleError, match="UNSUPPORTED"):
+        fs.sample(h[:, 1:63].contiguous(), W[:, 1:63].contiguous(), t, 0, 0)     # d = 62
+    lib = fs.library()
+    import ctypes
+    ids = torch.empty(2, dtype=torch.int64, device="cuda")
+    mx = torch.empty(2, dtype=torch.float32, device="cuda")
+    host = np.zeros((2, 64), np.uint16)
+    # a host pointer where device memory is required
+    st = lib.fs_sample(ctypes.c_void_p(host.ctypes.data), ctypes.c_void_p(W.data_ptr()), 2, 64, 10,
+                       ctypes.c_void_p(t.data_ptr()), 0, 0, ctypes.c_void_p(ids.data_ptr()),
+                       ctypes.c_void_p(mx.data_ptr()), None)
+    assert st == 1 and b"not device memory" in lib.fs_last_error()
+    # misaligned W
+    st = lib.fs_sample(ctypes.c_void_p(h.data_ptr()), ctypes.c_void_p(W.data_ptr() + 2), 2, 64, 9,
+                       ctypes.c_void_p(t.data_ptr()), 0, 0, ctypes.c_void_p(ids.data_ptr()),
+                       ctypes.c_void_p(mx.data_ptr()), None)
+    assert st == 2
+
+
+def test_deterministic_and_step_dependent(fs, torch_cuda):
+    h, W, temp = _problem(32, 4096, 128, seed=14, temps=np.ones(32))
+    a = _run(fs, torch_cuda, h, W, temp, 5, 0)
+    b = _run(fs, torch_cuda, h, W, temp, 5, 0)
+    c = _run(fs, torch_cuda, h, W, temp, 5, 1)
+    np.testing.assert_array_equal(a[0], b[0])
+    np.testing.assert_array_equal(a[1], b[1])
+    assert (a[0] != c[0]).mean() > 0.5
+
+
+def test_sampling_law_on_gpu(fs, torch_cuda):
+    """10^6 draws from one row (distinct row counters): chi-square against
+    softmax(logits / T) from the oracle's logits."""
+    from scipy import special, stats
+    V, d, n = 64, 64, 1_000_000
+    h1, W, _ = _problem(1, V, d, seed=15, w_std=0.15)
+    torch = torch_cuda
+    hd = to_device(np.repeat(h1, n, axis=0), torch)
+    Wd = to_device(W, torch)
+    T = 0.8
+    ids, _ = fs.sample(hd, Wd, torch.full((n,), T, device="cuda"), 2024, 0)
+    counts = np.bincount(ids.cpu().numpy(), minlength=V)
+    probs = special.softmax(sampler.logits(h1, W)[0] / T)
+    assert stats.chisquare(counts, probs * n).pvalue > 0.01
+
+
+# ------------------------------------------------------------------ chunked
+@pytest.mark.parametrize("bounds", [[0, 1, 130, 131, 2999, 4097], None])
+def test_chunked_equals_one_shot_bitwise(fs, torch_cuda, bounds):
+    torch = torch_cuda
+    B, V, d = 33, 4097, 256
+    h, W, temp = _problem(B, V, d, seed=16)
+    bounds = bounds or synthetic.chunk_bounds(V, 8)
+    hd, Wd, td = to_device(h, torch), to_device(W, torch), to_device(temp, torch)
+    ids1, mx1 = fs.sample(hd, Wd, td, 7, 3)
+    cm = torch.empty(B, device="cuda")
+    ci = torch.empty(B, dtype=torch.int64, device="cuda")
+    res = None
+    for i, (lo, hi) in enumerate(zip(bounds[:-1], bounds[1:])):
+        res = fs.sample_chunked(hd, Wd[lo:hi], lo, td, 7, 3, cm, ci, i == 0, i == len(bounds) - 2)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(res[0].cpu().numpy(), ids1.cpu().numpy())
+    np.testing.assert_array_equal(res[1].cpu().numpy(), mx1.cpu().numpy())
+    compare(res[0].cpu().numpy(), res[1].cpu().numpy(), sampler.sample(h, W, temp, 7, 3), what="chunked")
+
+
+# ------------------------------------------------------------------ host entry
+def test_sample_host_matches_device(fs, torch_cuda):
+    torch = torch_cuda
+    h, W, temp = _problem(16, 3000, 128, seed=17)
+    Wd = to_device(W, torch)
+    ids_h, mx_h = fs.sample_host(h, Wd, temp, 11, 4)
+    ids_d, mx_d = _run(fs, torch, h, W, temp, 11, 4)
+    np.testing.assert_array_equal(ids_h, ids_d)
+    np.testing.assert_array_equal(mx_h, mx_d)

@@ -201,6 +201,8 @@ def time_steps(fs, torch, hd, Wd, td, seed, first_step, n, stream, events=True):
     mean fused-kernel ms from per-step profile events)."""
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(n)] if events else []
     stops = [torch.cuda.Event(enable_timing=True) for _ in range(n)] if events else []
+    for ev in starts + stops:          # torch creates the CUDA event on first record
+        ev.record(stream)
     ids = torch.empty(hd.shape[0], dtype=torch.int64, device="cuda")
     mx = torch.empty(hd.shape[0], dtype=torch.float32, device="cuda")
     t0 = torch.cuda.Event(enable_timing=True)

@@ -44,6 +44,7 @@ struct Workspace {
 
 std::mutex g_ws_mutex;
 std::map<std::pair<int, cudaStream_t>, Workspace> g_workspaces;
+std::map<int, int*> g_error_words;   // per device: kernels' bounded-wait error word
 
 int num_sms(int device) {
   int sms = 0;
@@ -109,6 +110,28 @@ fs_status get_partials(cudaStream_t stream, size_t bytes, Partial** out) {
   s = grow(&ws.partials, &ws.partial_bytes, bytes, stream);
   if (s != FS_OK) return s;
   *out = static_cast<Partial*>(ws.partials);
+  return FS_OK;
+}
+
+// The device error word of the current device (allocated zeroed on first use).
+fs_status error_word(int** out) {
+  int dev;
+    {
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  }
+  std::lock_guard<std::mutex> lock(g_ws_mutex);
+  auto it = g_error_words.find(dev);
+  if (it != g_error_words.end()) {
+    *out = it->second;
+    return FS_OK;
+  }
+  int* w = nullptr;
+  cudaError_t e = cudaMalloc(&w, sizeof(int));
+  if (e == cudaSuccess) e = cudaMemset(w, 0, sizeof(int));
+  if (e != cudaSuccess) return fail(FS_ERR_WORKSPACE, "device error word: %s", cudaGetErrorString(e));
+  g_error_words[dev] = w;
+  *out = w;
   return FS_OK;
 }
 
@@ -180,11 +203,15 @@ fs_status check_problem(const Problem& p, bool need_out, const void* out_ids, co
   return FS_OK;
 }
 
-int resolve_path(int64_t B) {
-  const int forced = g_forced_path.load();
-  if (forced != kPathAuto) return forced;
-  (void)B;
-  return kPathSimt;
+// Kernel family for a call.  Auto: chosen from the batch size (and the
+// model width, identical for every chunk of a chunked run) only -- never from
+// V or the chunk range -- so one-shot and chunked runs compute every logit
+// with the same kernel and agree bit for bit.
+int resolve_path(int64_t B, int64_t d) {
+  int path = g_forced_path.load();
+  if (path == kPathAuto) path = (B <= 256) ? kPathTcVocab : kPathSimt;
+  if (path == kPathTcVocab && (B > 256 || d < 64)) path = kPathSimt;
+  return path;
 }
 
 // Fused kernel + cross-part reduction for one problem.
@@ -192,10 +219,15 @@ fs_status run(const Problem& p, Finish f, cudaStream_t stream) {
   if (p.B == 0) return FS_OK;
   int dev;
   FS_TRY(current_device(&dev));
-  const int path = resolve_path(p.B);
+  const int path = resolve_path(p.B, p.d);
   int n_parts = 0;
+  int* err = nullptr;
   if (p.V_local > 0) {
     switch (path) {
+      case kPathTcVocab:
+        n_parts = tc_vocab_num_parts(p, dev);
+        FS_TRY(error_word(&err));
+        break;
       case kPathSimt:
       default:
         n_parts = simt_num_parts(p, dev);
@@ -213,6 +245,9 @@ fs_status run(const Problem& p, Finish f, cudaStream_t stream) {
       if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord(start)");
     }
     switch (path) {
+      case kPathTcVocab:
+        e = launch_tc_vocab(p, partials, n_parts, err, stream);
+        break;
       case kPathSimt:
       default:
         e = launch_simt(p, partials, n_parts, stream);
@@ -365,13 +400,13 @@ fs_status fs_workspace_release(void) {
 
 fs_status fs_set_path(int path) {
   if (path < FS_PATH_AUTO || path > FS_PATH_TC_BATCH) return fail(FS_ERR_INVALID_ARG, "unknown path %d", path);
-  if (path == FS_PATH_TC_VOCAB || path == FS_PATH_TC_BATCH)
+  if (path == FS_PATH_TC_BATCH)
     return fail(FS_ERR_UNSUPPORTED, "kernel family %d is not built in this library", path);
   g_forced_path.store(path);
   return FS_OK;
 }
 
-int fs_path_for_batch(int64_t B) { return resolve_path(B); }
+int fs_path_for_batch(int64_t B) { return resolve_path(B, 4096); }
 
 fs_status fs_profile_events(void* start, void* stop) {
   if ((start == nullptr) != (stop == nullptr))
@@ -386,6 +421,11 @@ fs_status fs_device_error(int* code) {
   *code = 0;
   cudaError_t e = cudaDeviceSynchronize();
   if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+  int* w = nullptr;
+  FS_TRY(error_word(&w));
+  e = cudaMemcpy(code, w, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess) e = cudaMemset(w, 0, sizeof(int));
+  if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
   return FS_OK;
 }
 

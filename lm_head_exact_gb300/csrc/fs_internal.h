@@ -49,6 +49,13 @@ int simt_num_parts(const Problem& p, int device);
 
 // Launchers: enqueue on `stream`; return cudaSuccess or the launch error.
 cudaError_t launch_simt(const Problem& p, Partial* partials, int n_parts, cudaStream_t stream);
+
+// Tensor-core vocabulary-major path (B <= 256, d >= 64): one candidate per
+// (row, CTA); `err` is the device error word its bounded waits report to.
+int tc_vocab_num_parts(const Problem& p, int device);
+int tc_vocab_bn(int64_t B);
+cudaError_t launch_tc_vocab(const Problem& p, Partial* partials, int n_parts, int* err,
+                            cudaStream_t stream);
 cudaError_t launch_reduce(const Finish& f, int64_t B, cudaStream_t stream);
 cudaError_t launch_debug_noise(uint64_t seed, uint64_t step, int64_t row0, int64_t n_rows,
                                int64_t v0, int64_t n_vocab, uint32_t* words, float* gumbel,

@@ -1,0 +1,349 @@
+// Tensor-core fused LM-head sampler, vocabulary-major: the small / medium
+// batch path (B <= 256), where the step is bound by streaming W from HBM.
+//
+// FlashSampling: Fast and Memory-Efficient Exact Sampling -- summary page,
+// "Method": the logit tile is formed on chip, Gumbel noise is added in-tile,
+// and only a per-row (max, argmax) per tile survives; arXiv abstract: "keep
+// only one maximizer per row and per vocabulary tile".
+//
+// Mapping on GB300 (sm_103a):
+//   * One persistent CTA per SM owns a contiguous range of vocabulary rows
+//     (boundaries on 32-row units, so the ranges differ by at most 32 rows).
+//   * MMA: D[v, b] = sum_k W[v, k] * h[b, k] with tcgen05.mma kind::f16,
+//     M = 128 vocabulary rows (A = W tile), N = BN batch rows (B = h tile),
+//     K = 64 per pipeline stage; fp32 accumulators in TMEM, double-buffered
+//     so the epilogue of one tile overlaps the MMAs of the next.
+//   * TMA streams W (evict-first) and h (evict-last) tiles, 128-byte swizzled,
+//     through a STAGES-deep shared-memory ring guarded by mbarriers.
+//   * Warp roles (192 threads): warps 0-3 epilogue (TMEM lane = vocabulary
+//     row), warp 4 TMA producer, warp 5 TMEM allocator + MMA issuer.
+//   * Epilogue: per batch column, z = logit * (1/T) + Gumbel(Philox), then a
+//     warp-shuffle (max, argmax) across the 32 rows of the warp; the running
+//     best per (warp, column) lives in shared memory until the CTA's range is
+//     done, when the 4 warps are combined into one candidate per (row, CTA).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+
+#include "fs_internal.h"
+#include "fs_sm100.cuh"
+
+namespace fs {
+namespace {
+
+using namespace sm100;
+
+constexpr int kThreads = 192;
+constexpr int kEpiWarps = 4;
+constexpr int kProducerWarp = 4;
+constexpr int kMmaWarp = 5;
+constexpr int kBM = 128;          // vocabulary rows per tile (MMA M)
+constexpr int kBK = 64;           // K per stage: one 128-byte swizzle row of bf16
+constexpr int kUnitRows = 32;     // granularity of the per-CTA vocabulary ranges (one TMA box)
+constexpr int kATileBytes = kBM * kBK * 2;
+constexpr int kBoxBytes = kUnitRows * kBK * 2;
+
+template <int BN>
+struct VocabCfg {
+  static constexpr int kBTileBytes = BN * kBK * 2;
+  static constexpr int kStageBytes = kATileBytes + kBTileBytes;
+  static constexpr int kStages = std::min(12, (188 * 1024) / kStageBytes);
+  static constexpr int kTmemCols = (2 * BN < 32) ? 32 : 2 * BN;     // two accumulators
+  // shared memory carve-up (offsets from a 1024-byte aligned base)
+  static constexpr int kOffA = 0;
+  static constexpr int kOffB = kOffA + kStages * kATileBytes;
+  static constexpr int kOffBars = kOffB + kStages * kBTileBytes;
+  static constexpr int kNumBars = 2 * kStages + 5;
+  static constexpr int kOffMisc = kOffBars + kNumBars * 8;            // tmem base, abort flag
+  static constexpr int kOffInvT = kOffMisc + 16;
+  static constexpr int kOffMode = kOffInvT + BN * 4;
+  static constexpr int kOffBest = kOffMode + BN * 4;
+  static constexpr int kSmemBytes = kOffBest + kEpiWarps * BN * 8 + 1024;   // + alignment slack
+};
+
+struct VocabArgs {
+  Problem p;
+  Partial* partials;
+  int n_parts;        // = gridDim.x: one candidate per (row, CTA)
+  int64_t units;      // ceil(V_local / 32)
+  int* err;
+};
+
+template <int BN>
+__global__ void __launch_bounds__(kThreads, 1)
+tc_vocab_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_h,
+                const VocabArgs args) {
+  using C = VocabCfg<BN>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + C::kOffBars);
+  uint64_t* empty_bar = full_bar + C::kStages;
+  uint64_t* tfull_bar = empty_bar + C::kStages;     // [2]
+  uint64_t* tempty_bar = tfull_bar + 2;             // [2]
+  uint64_t* drain_bar = tempty_bar + 2;             // abort path only
+  uint32_t* tmem_base_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
+  float* col_inv_t = reinterpret_cast<float*>(smem + C::kOffInvT);
+  int* col_mode = reinterpret_cast<int*>(smem + C::kOffMode);
+  Best* warp_best = reinterpret_cast<Best*>(smem + C::kOffBest);   // [kEpiWarps][BN]
+
+  const Problem& p = args.p;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int B = static_cast<int>(p.B);
+
+  // This CTA's vocabulary rows [r0, r1) of the call's W.
+  const int64_t u0 = args.units * blockIdx.x / gridDim.x;
+  const int64_t u1 = args.units * (blockIdx.x + 1) / gridDim.x;
+  const int64_t r0 = u0 * kUnitRows;
+  const int64_t r1 = std::min<int64_t>(u1 * kUnitRows, p.V_local);
+  const int n_tiles = r1 > r0 ? static_cast<int>((r1 - r0 + kBM - 1) / kBM) : 0;
+  const int n_kb = static_cast<int>((p.d + kBK - 1) / kBK);
+
+  // ---- set-up
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull_bar[a], 1);
+      mbar_init(&tempty_bar[a], kEpiWarps * 32);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == kProducerWarp && lane == 0) {
+    tma_prefetch_desc(&tmap_w);
+    tma_prefetch_desc(&tmap_h);
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(tmem_base_slot, C::kTmemCols);
+    tmem_relinquish();
+  }
+  for (int b = threadIdx.x; b < BN; b += kThreads) {
+    const RowTemp rt = row_temp(b < B ? p.temp[b] : -1.0f);
+    col_inv_t[b] = rt.inv_t;
+    col_mode[b] = rt.mode;
+  }
+  for (int i = threadIdx.x; i < kEpiWarps * BN; i += kThreads) warp_best[i] = best_none();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_base_slot;
+
+  if (warp == kProducerWarp) {
+    // ---------------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      const uint64_t pol_w = policy_evict_first();
+      const uint64_t pol_h = policy_evict_last();
+      int stage = 0;
+      uint32_t phase = 0;
+      int64_t n_issued = 0;
+      bool ok = true;
+      for (int t = 0; t < n_tiles && ok; ++t) {
+        const int64_t row = r0 + static_cast<int64_t>(t) * kBM;
+        const int rows = static_cast<int>(std::min<int64_t>(kBM, r1 - row));
+        const int boxes = (rows + kUnitRows - 1) / kUnitRows;
+        const uint32_t bytes = boxes * kBoxBytes + C::kBTileBytes;
+        for (int kb = 0; kb < n_kb; ++kb) {
+          if (!mbar_wait(&empty_bar[stage], phase ^ 1, args.err, abort_flag)) { ok = false; break; }
+          uint8_t* a_dst = smem + C::kOffA + stage * kATileBytes;
+          uint8_t* b_dst = smem + C::kOffB + stage * C::kBTileBytes;
+          mbar_arrive_expect_tx(&full_bar[stage], bytes);
+          for (int j = 0; j < boxes; ++j)
+            tma_load_2d(a_dst + j * kBoxBytes, &tmap_w, &full_bar[stage], kb * kBK,
+                        static_cast<int32_t>(row + j * kUnitRows), pol_w);
+          tma_load_2d(b_dst, &tmap_h, &full_bar[stage], kb * kBK, 0, pol_h);
+          ++n_issued;
+          if (++stage == C::kStages) { stage = 0; phase ^= 1; }
+        }
+      }
+      if (!ok) {
+        // drain: never leave with copies in flight into this CTA's shared
+        // memory -- wait (bounded) for the last load issued into every stage
+        volatile int no_abort = 0;
+        for (int64_t i = std::max<int64_t>(0, n_issued - C::kStages); i < n_issued; ++i)
+          mbar_wait(&full_bar[i % C::kStages], static_cast<uint32_t>((i / C::kStages) & 1), args.err,
+                    &no_abort);
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(kBM, BN);
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int t = 0; t < n_tiles && ok; ++t) {
+        const int acc = t & 1;
+        const uint32_t acc_phase = (t >> 1) & 1;
+        if (!mbar_wait(&tempty_bar[acc], acc_phase ^ 1, args.err, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        for (int kb = 0; kb < n_kb; ++kb) {
+          if (!mbar_wait(&full_bar[stage], phase, args.err, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(smem + C::kOffA + stage * kATileBytes);
+          const uint32_t b_addr = smem_u32(smem + C::kOffB + stage * C::kBTileBytes);
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k)
+            mma_bf16(d_tmem, smem_desc_k128(a_addr + k * 32), smem_desc_k128(b_addr + k * 32), idesc,
+                     (kb | k) != 0);
+          mma_commit(&empty_bar[stage]);     // frees the stage once these MMAs have read it
+          if (++stage == C::kStages) { stage = 0; phase ^= 1; }
+        }
+        if (ok) mma_commit(&tfull_bar[acc]);   // accumulator ready for the epilogue
+      }
+      if (!ok) {
+        // wait (bounded) until every MMA issued so far has finished before TMEM is freed
+        mma_commit(drain_bar);
+        volatile int no_abort = 0;
+        mbar_wait(drain_bar, 0, args.err, &no_abort);
+      }
+    }
+  } else {
+    // ---------------------------------------------------------------- epilogue (warps 0-3)
+    const PhiloxKey key{static_cast<uint32_t>(p.seed), static_cast<uint32_t>(p.seed >> 32)};
+    const uint32_t step_lo = static_cast<uint32_t>(p.step);
+    const uint32_t step_hi = static_cast<uint32_t>(p.step >> 32);
+    const int t_row = warp * 32 + lane;                       // TMEM lane = row within the tile
+    const uint32_t lane_addr = static_cast<uint32_t>(warp * 32) << 16;
+    const int n_col = (B + 15) & ~15;
+    Best* my_best = warp_best + warp * BN;
+    for (int t = 0; t < n_tiles; ++t) {
+      const int acc = t & 1;
+      const uint32_t acc_phase = (t >> 1) & 1;
+      if (!mbar_wait(&tfull_bar[acc], acc_phase, args.err, abort_flag)) break;
+      tc_fence_after();
+      const int64_t row = r0 + static_cast<int64_t>(t) * kBM;
+      const bool valid = row + t_row < r1;
+      const int64_t v_local = row + t_row;
+      const int64_t vg = p.v_offset + v_local;
+      const uint32_t vq = static_cast<uint32_t>(vg >> 2);
+      const uint32_t vj = static_cast<uint32_t>(vg & 3);
+      for (int c0 = 0; c0 < n_col; c0 += 16) {
+        uint32_t r[16];
+        tmem_ld_16(tmem_base + lane_addr + acc * BN + c0, r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int b = c0 + j;
+          if (b < B) {                                          // warp-uniform
+            const int mode = col_mode[b];
+            float z = -INFINITY;
+            if (valid && mode != kRowInvalid) {
+              float logit = __uint_as_float(r[j]);
+              if (p.bias != nullptr) logit += p.bias[static_cast<int64_t>(b) * p.bias_stride + v_local];
+              if (mode == kRowSample) {
+                const uint4 w = noise_words(key, vq, static_cast<uint32_t>(b), step_lo, step_hi);
+                z = fmaf(logit, col_inv_t[b], gumbel_from_word(word_of(w, vj)));
+              } else {
+                z = logit;
+              }
+              if (!(z > -INFINITY)) z = -INFINITY;              // NaN never wins
+            }
+            Best c;
+            c.z = z;
+            c.id = z > -INFINITY ? static_cast<int32_t>(vg) : kNoId;
+            c = warp_combine(c);
+            if (lane == 0) my_best[b] = combine(my_best[b], c);
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&tempty_bar[acc]);
+    }
+    // combine the 4 epilogue warps: one candidate per (batch row, CTA)
+    asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
+    for (int b = threadIdx.x; b < B; b += kEpiWarps * 32) {
+      Best r = warp_best[b];
+#pragma unroll
+      for (int w = 1; w < kEpiWarps; ++w) r = combine(r, warp_best[w * BN + b]);
+      Partial out;
+      out.z = r.z;
+      out.id = r.id;
+      args.partials[static_cast<int64_t>(b) * args.n_parts + blockIdx.x] = out;
+    }
+  }
+
+  // ---- teardown
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kMmaWarp) tmem_dealloc(tmem_base, C::kTmemCols);
+}
+
+// ------------------------------------------------------------------ host side
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (fn == nullptr) {
+    cudaDriverEntryPointQueryResult q;
+    void* ptr = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+// bf16 [rows, d] row-major, box = 64 elements x box_rows rows, 128-byte swizzle.
+bool encode_kmajor(CUtensorMap* tm, const void* base, int64_t rows, int64_t d, int box_rows) {
+  auto encode = get_encode();
+  if (encode == nullptr) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(d) * 2};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = encode(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+                      estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int BN>
+cudaError_t launch_bn(const Problem& p, Partial* partials, int n_parts, int* err, cudaStream_t stream) {
+  using C = VocabCfg<BN>;
+  static_assert(C::kStages >= 2, "pipeline needs at least two stages");
+  static_assert(C::kSmemBytes <= 227 * 1024, "shared memory budget");
+  CUtensorMap tw, th;
+  if (!encode_kmajor(&tw, p.W, p.V_local, p.d, kUnitRows)) return cudaErrorInvalidValue;
+  if (!encode_kmajor(&th, p.h, p.B, p.d, BN)) return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(tc_vocab_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  VocabArgs a{p, partials, n_parts, (p.V_local + kUnitRows - 1) / kUnitRows, err};
+  tc_vocab_kernel<BN><<<n_parts, kThreads, C::kSmemBytes, stream>>>(tw, th, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int tc_vocab_bn(int64_t B) {
+  return B <= 16 ? 16 : B <= 32 ? 32 : B <= 64 ? 64 : B <= 128 ? 128 : 256;
+}
+
+int tc_vocab_num_parts(const Problem& p, int device) {
+  int sms = 0;
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
+  if (sms <= 0) sms = 148;
+  const int64_t units = (p.V_local + kUnitRows - 1) / kUnitRows;
+  return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(sms, units)));
+}
+
+cudaError_t launch_tc_vocab(const Problem& p, Partial* partials, int n_parts, int* err,
+                            cudaStream_t stream) {
+  if (p.B > 256 || p.d < kBK) return cudaErrorNotSupported;
+  switch (tc_vocab_bn(p.B)) {
+    case 16: return launch_bn<16>(p, partials, n_parts, err, stream);
+    case 32: return launch_bn<32>(p, partials, n_parts, err, stream);
+    case 64: return launch_bn<64>(p, partials, n_parts, err, stream);
+    case 128: return launch_bn<128>(p, partials, n_parts, err, stream);
+    default: return launch_bn<256>(p, partials, n_parts, err, stream);
+  }
+}
+
+}  // namespace fs

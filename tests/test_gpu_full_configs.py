@@ -64,10 +64,12 @@ def test_llama3_70b_with_bias(fs, torch_cuda):
         torch.cuda.synchronize()
         ref = sampler.sample(wl.h, wl.W, wl.temp, wl.seed, step, bias=wl.bias, rows=rows)
         compare(ids.cpu().numpy(), mx.cpu().numpy(), ref, rows=rows, what=f"70B B={B}")
-        # the +8 spikes dominate: most sampled ids are spike ids
-        spikes = wl.bias[:B] > 0
-        hit = spikes[np.arange(B), ids.cpu().numpy()]
-        assert hit.mean() > 0.5
+        if B == 256:
+            # The 16 spikes of +8 carry about 16 e^8 / (16 e^8 + V) ~ 27% of the
+            # softmax mass (the logit spread is the same on and off the spikes).
+            spikes = wl.bias[:B] > 0
+            hit = spikes[np.arange(B), ids.cpu().numpy()].mean()
+            assert 0.15 < hit < 0.40, hit
 
 
 @pytest.mark.parametrize("n_chunks", [8, 32])

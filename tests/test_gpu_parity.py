@@ -35,6 +35,15 @@ def _problem(B, V, d, seed, w_std=0.05, temps=None):
     return h, W, np.asarray(temps, np.float32)
 
 
+@pytest.fixture(params=["simt", "tc_vocab"])
+def path(request, fs):
+    """Run the test once per kernel family (forced through fs_set_path)."""
+    code = {"simt": fs.FS_PATH_SIMT, "tc_vocab": fs.FS_PATH_TC_VOCAB}[request.param]
+    fs.set_path(code)
+    yield request.param
+    fs.set_path(fs.FS_PATH_AUTO)
+
+
 # ------------------------------------------------------------------ noise
 @pytest.mark.parametrize("row0,v0,step", [(0, 0, 0), (5, 3, 99), (1000, 151900, (3 << 32) + 17)])
 def test_noise_words_bit_exact(fs, torch_cuda, row0, v0, step):
@@ -65,23 +74,23 @@ def test_tiny_workload(fs, torch_cuda):
     assert ids[0] == np.argmax(sampler.logits(wl.h, wl.W)[0])   # T = 0 row is greedy
 
 
-@pytest.mark.parametrize("B", [1, 3, 8, 17])
-@pytest.mark.parametrize("V,d", [(1, 8), (127, 64), (4097, 256), (1000, 8)])
-def test_ragged_shapes(fs, torch_cuda, B, V, d):
+@pytest.mark.parametrize("B", [1, 3, 8, 17, 100, 256])
+@pytest.mark.parametrize("V,d", [(1, 64), (127, 64), (4097, 256), (1000, 8), (3000, 200)])
+def test_ragged_shapes(fs, torch_cuda, path, B, V, d):
     h, W, temp = _problem(B, V, d, seed=B * 7 + V)
     for step in (0, 5):
         ids, mx = _run(fs, torch_cuda, h, W, temp, 42, step)
         compare(ids, mx, sampler.sample(h, W, temp, 42, step), what=f"B{B} V{V} d{d}")
 
 
-def test_many_steps_many_rows(fs, torch_cuda):
+def test_many_steps_many_rows(fs, torch_cuda, path):
     h, W, temp = _problem(64, 5000, 128, seed=3)
     for step in range(0, 100, 9):
         ids, mx = _run(fs, torch_cuda, h, W, temp, 1234, step)
         compare(ids, mx, sampler.sample(h, W, temp, 1234, step), what=f"step {step}")
 
 
-def test_bias_per_row_and_shared(fs, torch_cuda):
+def test_bias_per_row_and_shared(fs, torch_cuda, path):
     B, V, d = 9, 3001, 64
     h, W, temp = _problem(B, V, d, seed=11)
     rng = np.random.default_rng(11)
@@ -95,7 +104,7 @@ def test_bias_per_row_and_shared(fs, torch_cuda):
     compare(ids, mx, sampler.sample(h, W, temp, 9, 2, bias=shared), what="shared bias")
 
 
-def test_degenerate_rows(fs, torch_cuda):
+def test_degenerate_rows(fs, torch_cuda, path):
     B, V, d = 6, 300, 32
     h, W, _ = _problem(B, V, d, seed=12)
     W = W.copy()
@@ -110,7 +119,7 @@ def test_degenerate_rows(fs, torch_cuda):
     assert 10 not in ids
 
 
-def test_empty_batch_and_empty_vocab(fs, torch_cuda):
+def test_empty_batch_and_empty_vocab(fs, torch_cuda, path):
     torch = torch_cuda
     h = torch.zeros((0, 64), dtype=torch.bfloat16, device="cuda")
     W = torch.zeros((10, 64), dtype=torch.bfloat16, device="cuda")
@@ -125,7 +134,7 @@ def test_empty_batch_and_empty_vocab(fs, torch_cuda):
     assert mx.tolist() == [-np.inf] * 3
 
 
-def test_ties_go_to_smaller_id(fs, torch_cuda):
+def test_ties_go_to_smaller_id(fs, torch_cuda, path):
     rng = np.random.default_rng(13)
     h = synthetic.bf16_bits(rng.standard_normal((4, 64)).astype(np.float32))
     row = synthetic.bf16_bits(rng.standard_normal((1, 64)).astype(np.float32))
@@ -158,7 +167,7 @@ def test_invalid_arguments_are_rejected(fs, torch_cuda):
     assert st == 2
 
 
-def test_deterministic_and_step_dependent(fs, torch_cuda):
+def test_deterministic_and_step_dependent(fs, torch_cuda, path):
     h, W, temp = _problem(32, 4096, 128, seed=14, temps=np.ones(32))
     a = _run(fs, torch_cuda, h, W, temp, 5, 0)
     b = _run(fs, torch_cuda, h, W, temp, 5, 0)
@@ -168,25 +177,31 @@ def test_deterministic_and_step_dependent(fs, torch_cuda):
     assert (a[0] != c[0]).mean() > 0.5
 
 
-def test_sampling_law_on_gpu(fs, torch_cuda):
-    """10^6 draws from one row (distinct row counters): chi-square against
-    softmax(logits / T) from the oracle's logits."""
+def test_sampling_law_on_gpu(fs, torch_cuda, path):
+    """10^6 draws from one row (250 identical rows x 4000 steps; every
+    (row, step) has its own counters): chi-square against softmax(logits / T)
+    from the oracle's logits."""
     from scipy import special, stats
-    V, d, n = 64, 64, 1_000_000
+    V, d, rows, steps = 64, 64, 250, 4000
     h1, W, _ = _problem(1, V, d, seed=15, w_std=0.15)
     torch = torch_cuda
-    hd = to_device(np.repeat(h1, n, axis=0), torch)
+    hd = to_device(np.repeat(h1, rows, axis=0), torch)
     Wd = to_device(W, torch)
     T = 0.8
-    ids, _ = fs.sample(hd, Wd, torch.full((n,), T, device="cuda"), 2024, 0)
-    counts = np.bincount(ids.cpu().numpy(), minlength=V)
+    td = torch.full((rows,), T, device="cuda")
+    ids = torch.empty((steps, rows), dtype=torch.int64, device="cuda")
+    mx = torch.empty((steps, rows), dtype=torch.float32, device="cuda")
+    for s_ in range(steps):
+        fs.sample(hd, Wd, td, 2024, s_, out=(ids[s_], mx[s_]))
+    counts = np.bincount(ids.cpu().numpy().ravel(), minlength=V)
+    n = rows * steps
     probs = special.softmax(sampler.logits(h1, W)[0] / T)
     assert stats.chisquare(counts, probs * n).pvalue > 0.01
 
 
 # ------------------------------------------------------------------ chunked
 @pytest.mark.parametrize("bounds", [[0, 1, 130, 131, 2999, 4097], None])
-def test_chunked_equals_one_shot_bitwise(fs, torch_cuda, bounds):
+def test_chunked_equals_one_shot_bitwise(fs, torch_cuda, path, bounds):
     torch = torch_cuda
     B, V, d = 33, 4097, 256
     h, W, temp = _problem(B, V, d, seed=16)
@@ -205,7 +220,7 @@ def test_chunked_equals_one_shot_bitwise(fs, torch_cuda, bounds):
 
 
 # ------------------------------------------------------------------ host entry
-def test_sample_host_matches_device(fs, torch_cuda):
+def test_sample_host_matches_device(fs, torch_cuda, path):
     torch = torch_cuda
     h, W, temp = _problem(16, 3000, 128, seed=17)
     Wd = to_device(W, torch)
@@ -213,3 +228,25 @@ def test_sample_host_matches_device(fs, torch_cuda):
     ids_d, mx_d = _run(fs, torch, h, W, temp, 11, 4)
     np.testing.assert_array_equal(ids_h, ids_d)
     np.testing.assert_array_equal(mx_h, mx_d)
+
+
+def test_paths_agree_on_llama3_8b_head(fs, torch_cuda):
+    """Both kernel families on the full-size head: ids equal outside near ties,
+    maxima within the tolerance (they sum the logits in different orders)."""
+    torch = torch_cuda
+    wl = synthetic.workload("llama3_8b", 64)
+    hd, Wd, td = to_device(wl.h, torch), to_device(wl.W, torch), to_device(wl.temp, torch)
+    out = {}
+    for name, code in (("simt", fs.FS_PATH_SIMT), ("tc", fs.FS_PATH_TC_VOCAB)):
+        fs.set_path(code)
+        ids, mx = fs.sample(hd, Wd, td, wl.seed, 11)
+        torch.cuda.synchronize()
+        out[name] = (ids.cpu().numpy(), mx.cpu().numpy())
+    fs.set_path(fs.FS_PATH_AUTO)
+    diff = out["simt"][0] != out["tc"][0]
+    assert diff.sum() <= 1
+    assert np.abs(out["simt"][1] - out["tc"][1])[~diff].max() < 1e-3
+
+
+def test_device_error_word_is_clear(fs, torch_cuda):
+    assert fs.device_error() == 0

@@ -137,6 +137,29 @@ FS_API fs_status fs_sample_host(const void* h_host, const void* W, int64_t B, in
                          uint64_t seed, uint64_t step,
                          int64_t* out_ids_host, float* out_max_host, void* stream);
 
+/*
+ * fs_sample without any device-memory allocation.  (An engineering variant:
+ * the FlashSampling paper has no counterpart.)  Same arguments, results and
+ * noise as fs_sample, computed by the same tensor-core kernel, but the
+ * per-(row, tile) candidates live in a fixed static device array inside the
+ * library (about 320 KB per GPU, held until the process exits) instead of a
+ * workspace the library cudaMalloc's on demand.  For callers that cannot let
+ * a library allocate or free device memory: an allocator that already owns
+ * the GPU's memory budget, or code that cannot afford the device-wide
+ * synchronization of cudaFree.
+ *   Limits: 1 <= B <= 256 (larger B returns FS_ERR_UNSUPPORTED with a
+ *   message), d >= 64 and a multiple of 8; no bias.
+ *   Set-up: the first call on each device looks up the array's device
+ *   address (cudaGetSymbolAddress) and clears its status word; make that
+ *   first call before any stream capture starts.
+ *   Sharing: every call on a device uses the same array and finds the last
+ *   call's contents there.  Calls whose kernels overlap on the GPU (e.g. on
+ *   unordered streams) race on it; keep them ordered on one stream.
+ */
+FS_API fs_status fs_sample_noalloc(const void* h, const void* W, int64_t B, int64_t d, int64_t V,
+                                   const float* temp, uint64_t seed, uint64_t step,
+                                   int64_t* out_ids, float* out_max, void* stream);
+
 /* Workspace bytes one call with (B, V) needs on the current device. */
 FS_API size_t fs_workspace_bytes(int64_t B, int64_t V);
 

@@ -35,6 +35,8 @@ SIGNATURES = {
                                  _c_void_p, _c_void_p, _c_void_p]),
     "fs_sample_host": (_int, [_c_void_p, _c_void_p, _i64, _i64, _i64, _c_void_p, _c_void_p, _i64,
                               _u64, _u64, _c_void_p, _c_void_p, _c_void_p]),
+    "fs_sample_noalloc": (_int, [_c_void_p, _c_void_p, _i64, _i64, _i64, _c_void_p, _u64, _u64,
+                                 _c_void_p, _c_void_p, _c_void_p]),
     "fs_workspace_bytes": (ctypes.c_size_t, [_i64, _i64]),
     "fs_workspace_reserve": (_int, [_i64, _i64, _c_void_p]),
     "fs_workspace_release": (_int, []),

@@ -265,6 +265,9 @@ fs_status run(const Problem& p, Finish f, cudaStream_t stream) {
 }
 
 }  // namespace
+
+void record_error(const char* msg) { snprintf(g_last_error, sizeof(g_last_error), "%s", msg); }
+
 }  // namespace fs
 
 using namespace fs;

@@ -57,6 +57,9 @@ int tc_vocab_bn(int64_t B);
 cudaError_t launch_tc_vocab(const Problem& p, Partial* partials, int n_parts, int* err,
                             cudaStream_t stream);
 cudaError_t launch_reduce(const Finish& f, int64_t B, cudaStream_t stream);
+
+// Set the calling thread's fs_last_error() text.
+void record_error(const char* msg);
 cudaError_t launch_debug_noise(uint64_t seed, uint64_t step, int64_t row0, int64_t n_rows,
                                int64_t v0, int64_t n_vocab, uint32_t* words, float* gumbel,
                                cudaStream_t stream);

@@ -1,0 +1,150 @@
+// fs_sample_noalloc: the tensor-core sampling path with its scratch memory in
+// a fixed, statically allocated device array instead of the library's
+// cudaMalloc'ed workspace.
+//
+// Why it exists: fs_sample keeps its per-(row, CTA) candidates in a
+// workspace that the library allocates with cudaMalloc the first time a
+// (device, stream) needs it, and re-allocates when a larger call arrives.
+// Some callers cannot let a library do that: serving stacks whose allocator
+// has already claimed the device memory budget (a library cudaMalloc then
+// fails or fragments memory it does not own), and callers that must not pay
+// for the device-wide synchronization cudaFree implies when a workspace is
+// replaced.  This entry point never allocates or frees device memory.
+//
+// The scratch lives in `g_noalloc_scratch` below, a file-scope static
+// __device__ array of kScratchBytes (about 320 KB) that every GPU loading the
+// library keeps until the process exits.  Host code cannot use the array's
+// name as a device address (it is a host-side stand-in), so the first call
+// on each device looks the address up with cudaGetSymbolAddress while that
+// device is current, clears the status word at the start of the array, and
+// caches the pointer for later calls on that device.  Make that first call on
+// each device before any stream capture begins.
+//
+// Every call on a device shares the one array and finds the previous call's
+// contents in it; each call writes every candidate slot it later reads, so no
+// clearing is needed between calls.  Calls whose kernels overlap on the GPU
+// (for example on two streams without ordering between them) race on the
+// array and may return wrong samples: order them on one stream.
+#include <cstdio>
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/flashsample.h"
+#include "fs_internal.h"
+
+namespace fs {
+namespace {
+
+// Largest batch this entry point accepts (the tensor-core vocabulary-major
+// kernel's limit) and the largest number of candidates per row it can hold
+// (one per CTA = one per SM; 160 covers GB300's 152 SMs).
+constexpr int64_t kNoAllocMaxBatch = 256;
+constexpr int64_t kNoAllocMaxParts = 160;
+constexpr size_t kHeaderBytes = 256;   // status word of the kernels' bounded waits, padded
+constexpr size_t kScratchBytes = kHeaderBytes + kNoAllocMaxBatch * kNoAllocMaxParts * sizeof(Partial);
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_setup_mutex;
+void* g_scratch_ptr[kMaxDevices] = {};
+
+fs_status noalloc_fail(fs_status s, const char* msg) {
+  char buf[256];
+  snprintf(buf, sizeof(buf), "fs_sample_noalloc: %s", msg);
+  record_error(buf);
+  return s;
+}
+
+// Device address of the static scratch on the current device; the first
+// call per device resolves it and zeroes the status word.
+fs_status scratch_for_current_device(unsigned char** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+    return noalloc_fail(FS_ERR_CUDA, "cannot query the current device");
+  std::lock_guard<std::mutex> lock(g_setup_mutex);
+  if (g_scratch_ptr[dev] == nullptr) {
+    void* ptr = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+    if (e != cudaSuccess || ptr == nullptr) {
+      cudaGetLastError();
+      return noalloc_fail(FS_ERR_CUDA, "cudaGetSymbolAddress of the static scratch failed");
+    }
+    e = cudaMemset(ptr, 0, kHeaderBytes);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return noalloc_fail(FS_ERR_CUDA, "clearing the static scratch status word failed");
+    }
+    g_scratch_ptr[dev] = ptr;
+  }
+  *out = static_cast<unsigned char*>(g_scratch_ptr[dev]);
+  return FS_OK;
+}
+
+bool is_device_ptr(const void* p) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged;
+}
+
+}  // namespace
+}  // namespace fs
+
+using namespace fs;
+
+extern "C" FS_API fs_status fs_sample_noalloc(const void* h, const void* W, int64_t B, int64_t d,
+                                              int64_t V, const float* temp, uint64_t seed,
+                                              uint64_t step, int64_t* out_ids, float* out_max,
+                                              void* stream_) {
+  record_error("");
+  if (B < 0 || d <= 0 || V < 0) return noalloc_fail(FS_ERR_INVALID_ARG, "need B >= 0, d > 0, V >= 0");
+  if (B > kNoAllocMaxBatch)
+    return noalloc_fail(FS_ERR_UNSUPPORTED, "B exceeds 256, the static scratch's batch limit");
+  if (d < 64) return noalloc_fail(FS_ERR_UNSUPPORTED, "d must be at least 64");
+  if (d % 8 != 0) return noalloc_fail(FS_ERR_UNSUPPORTED, "d must be a multiple of 8");
+  if (V >= (int64_t(1) << 31)) return noalloc_fail(FS_ERR_UNSUPPORTED, "V must be < 2^31");
+  if (B == 0) return FS_OK;
+  if (!h || !temp || !out_ids || !out_max || (V > 0 && !W))
+    return noalloc_fail(FS_ERR_INVALID_ARG, "NULL pointer");
+  if (reinterpret_cast<uintptr_t>(h) % 16 || reinterpret_cast<uintptr_t>(W) % 16)
+    return noalloc_fail(FS_ERR_UNSUPPORTED, "h and W must be 16-byte aligned");
+  if (!is_device_ptr(h) || !is_device_ptr(temp) || !is_device_ptr(out_ids) || !is_device_ptr(out_max) ||
+      (V > 0 && !is_device_ptr(W)))
+    return noalloc_fail(FS_ERR_INVALID_ARG, "h, W, temp, out_ids and out_max must be device memory");
+
+  unsigned char* scratch = nullptr;
+  fs_status s = scratch_for_current_device(&scratch);
+  if (s != FS_OK) return s;
+  int* status_word = reinterpret_cast<int*>(scratch);
+  Partial* partials = reinterpret_cast<Partial*>(scratch + kHeaderBytes);
+
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  Problem p{h, W, B, d, V, 0, temp, nullptr, 0, seed, step};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const int n_parts = V > 0 ? tc_vocab_num_parts(p, dev) : 0;
+  if (n_parts > kNoAllocMaxParts)
+    return noalloc_fail(FS_ERR_UNSUPPORTED, "this device has more SMs than the static scratch holds");
+  if (V > 0) {
+    cudaError_t e = launch_tc_vocab(p, partials, n_parts, status_word, stream);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return noalloc_fail(FS_ERR_CUDA, "fused sampling kernel launch failed");
+    }
+  }
+  Finish f{};
+  f.partials = partials;
+  f.n_parts = n_parts;
+  f.write_out = true;
+  f.out_ids = out_ids;
+  f.out_max = out_max;
+  cudaError_t e = launch_reduce(f, B, stream);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return noalloc_fail(FS_ERR_CUDA, "reduction kernel launch failed");
+  }
+  return FS_OK;
+}

@@ -34,6 +34,7 @@ if ROOT not in sys.path:
 METRIC = "fused LM-head sample µs/step & % of HBM/TC roofline vs batch (d4096,V128256)"
 UNIT = "us/step"
 SWEEP = (1, 2, 4, 8, 16, 32, 64)
+SWEEP_LARGE = (128, 256, 512, 1024)
 
 
 # ---------------------------------------------------------------- roofline
@@ -285,16 +286,32 @@ def run_ours(args):
     barrier(dist)
     e2e_ms = max_over_ranks(e2e_ms, dist, device="cuda")
 
-    # batch sweep of the metric (same kernels, fewer steps per point)
+    # batch sweeps of the metric (same kernels, fewer steps per point): the
+    # Llama-3-8B head over the decode range and the large-batch tensor-core
+    # range, and the Qwen3-8B head's large batches
     sweep = []
     if not args.no_sweep:
+        def point(kind, b, hdev, Wdev, tdev, Vk, dk):
+            time_steps(fs, torch, hdev[:b], Wdev, tdev[:b], seed, 0, 3, stream, events=False)
+            tot, km = time_steps(fs, torch, hdev[:b], Wdev, tdev[:b], seed, 3, 20, stream)
+            rf = roofline(b, dk, Vk, km * 1e3, peaks)
+            return {"workload": kind, "B": b, "us_per_step": round(tot / 20 * 1e3, 2),
+                    "fused_kernel_us": round(km * 1e3, 2), "roofline_us": rf["roofline_us"],
+                    "frac": rf["frac"], "bound": rf["bound"], "path": fs.path_for_batch(b)}
+
+        big = max(SWEEP_LARGE)
+        h_big = _to_dev(synthetic.normal_rows_bf16(synthetic.SEED_H, big, d, 1.0), torch)
+        t_big = torch.ones(big, dtype=torch.float32, device="cuda")
         for b in SWEEP:
-            time_steps(fs, torch, hd_all[:b], Wd, temp_all[:b], seed, 0, 3, stream, events=False)
-            tot, km = time_steps(fs, torch, hd_all[:b], Wd, temp_all[:b], seed, 3, 20, stream)
-            rf = roofline(b, d, V, km * 1e3, peaks)
-            sweep.append({"B": b, "us_per_step": round(tot / 20 * 1e3, 2),
-                          "fused_kernel_us": round(km * 1e3, 2), "frac": rf["frac"],
-                          "bound": rf["bound"], "path": fs.path_for_batch(b)})
+            sweep.append(point(kind, b, hd_all, Wd, temp_all, V, d))
+        for b in SWEEP_LARGE:
+            sweep.append(point(kind, b, h_big, Wd, t_big, V, d))
+        qshape = synthetic.SHAPES["qwen3_8b"]
+        Wq = _to_dev(synthetic.weights("qwen3_8b"), torch)
+        tq = _to_dev(synthetic.temperatures("qwen3_8b", big), torch)
+        for b in qshape["batches"]:
+            sweep.append(point("qwen3_8b", b, h_big, Wq, tq, qshape["V"], qshape["d"]))
+        del Wq
 
     result = None
     if rank == 0:

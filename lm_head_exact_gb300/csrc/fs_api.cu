@@ -56,8 +56,9 @@ int num_sms(int device) {
 // Upper bound of the candidates per row any kernel family produces for a
 // vocabulary of V rows (used to size reservations ahead of graph capture).
 int64_t max_parts(int64_t V, int device) {
-  const int64_t simt = std::min<int64_t>(static_cast<int64_t>(num_sms(device)) * 8, (V + 7) / 8);
-  return std::max<int64_t>(simt, 1);
+  const int64_t sms = num_sms(device);
+  const int64_t simt = std::min<int64_t>(sms * 8, (V + 7) / 8);   // CUDA-core path: blocks
+  return std::max<int64_t>(std::max<int64_t>(simt, sms), 1);       // tensor-core paths: <= one per SM
 }
 
 size_t partial_bytes(int64_t B, int64_t parts) {
@@ -209,8 +210,9 @@ fs_status check_problem(const Problem& p, bool need_out, const void* out_ids, co
 // with the same kernel and agree bit for bit.
 int resolve_path(int64_t B, int64_t d) {
   int path = g_forced_path.load();
-  if (path == kPathAuto) path = (B <= 256) ? kPathTcVocab : kPathSimt;
-  if (path == kPathTcVocab && (B > 256 || d < 64)) path = kPathSimt;
+  if (path == kPathAuto) path = (B <= 256) ? kPathTcVocab : kPathTcBatch;
+  if (path == kPathTcVocab && B > 256) path = kPathTcBatch;
+  if ((path == kPathTcVocab || path == kPathTcBatch) && d < 64) path = kPathSimt;
   return path;
 }
 
@@ -226,6 +228,10 @@ fs_status run(const Problem& p, Finish f, cudaStream_t stream) {
     switch (path) {
       case kPathTcVocab:
         n_parts = tc_vocab_num_parts(p, dev);
+        FS_TRY(error_word(&err));
+        break;
+      case kPathTcBatch:
+        n_parts = tc_batch_num_parts(p, dev);
         FS_TRY(error_word(&err));
         break;
       case kPathSimt:
@@ -247,6 +253,9 @@ fs_status run(const Problem& p, Finish f, cudaStream_t stream) {
     switch (path) {
       case kPathTcVocab:
         e = launch_tc_vocab(p, partials, n_parts, err, stream);
+        break;
+      case kPathTcBatch:
+        e = launch_tc_batch(p, partials, n_parts, err, stream);
         break;
       case kPathSimt:
       default:
@@ -403,8 +412,6 @@ fs_status fs_workspace_release(void) {
 
 fs_status fs_set_path(int path) {
   if (path < FS_PATH_AUTO || path > FS_PATH_TC_BATCH) return fail(FS_ERR_INVALID_ARG, "unknown path %d", path);
-  if (path == FS_PATH_TC_BATCH)
-    return fail(FS_ERR_UNSUPPORTED, "kernel family %d is not built in this library", path);
   g_forced_path.store(path);
   return FS_OK;
 }

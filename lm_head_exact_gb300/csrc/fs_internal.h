@@ -56,6 +56,12 @@ int tc_vocab_num_parts(const Problem& p, int device);
 int tc_vocab_bn(int64_t B);
 cudaError_t launch_tc_vocab(const Problem& p, Partial* partials, int n_parts, int* err,
                             cudaStream_t stream);
+// Tensor-core batch-major path (any B, d >= 64; used for B > 256): one
+// candidate per (row, CTA group).
+int tc_batch_num_parts(const Problem& p, int device);
+cudaError_t launch_tc_batch(const Problem& p, Partial* partials, int n_parts, int* err,
+                            cudaStream_t stream);
+
 cudaError_t launch_reduce(const Finish& f, int64_t B, cudaStream_t stream);
 
 // Set the calling thread's fs_last_error() text.

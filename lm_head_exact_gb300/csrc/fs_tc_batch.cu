@@ -1,0 +1,311 @@
+// Tensor-core fused LM-head sampler, batch-major: the large-batch path
+// (B > 256), where the contraction, not the W stream, bounds the step.
+//
+// FlashSampling: Fast and Memory-Efficient Exact Sampling -- summary page,
+// "Method": the logit tile is formed on chip, Gumbel noise is added in-tile,
+// and only a per-row (max, argmax) survives; arXiv abstract: "keep only one
+// maximizer per row and per vocabulary tile, and finish with a small
+// reduction over tiles".
+//
+// Mapping on GB300 (sm_103a):
+//   * Tile = 128 batch rows (MMA M; A = h tile) x 256 vocabulary rows (MMA N;
+//     B = W tile), K = 64 per stage; tcgen05.mma kind::f16, fp32 accumulators
+//     in TMEM, two 256-column accumulators (all 512 columns) so the epilogue
+//     of one tile overlaps the MMAs of the next.
+//   * CTA grouping: with nbt = ceil(B / 128) batch tiles, the grid is cut into
+//     groups of nbt CTAs.  CTA c keeps batch tile c % nbt for its whole life
+//     and walks the vocabulary tiles q, q + n_groups, ... (q = c / nbt).  The
+//     nbt CTAs of a group read the same W tile at the same time, so W comes
+//     from HBM once per group and from L2 for the others, and every epilogue
+//     thread keeps ITS batch row's running (max, argmax) in registers across
+//     all of the CTA's tiles: one candidate per (row, group) at the end.
+//   * Warp roles (320 threads): warps 0-7 epilogue (TMEM lane = batch row;
+//     warps w and w + 4 share lanes and split the 256 columns in halves),
+//     warp 8 TMA producer, warp 9 TMEM allocator + MMA issuer.
+//   * Epilogue per element: z = logit * (1/T) + Gumbel(Philox); one Philox
+//     call serves the four consecutive vocabulary ids that share a counter.
+#include <cuda.h>
+
+#include <algorithm>
+
+#include "fs_internal.h"
+#include "fs_sm100.cuh"
+#include "fs_tmap.h"
+
+namespace fs {
+namespace {
+
+using namespace sm100;
+
+constexpr int kThreads = 320;
+constexpr int kEpiWarps = 8;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kBM = 128;            // batch rows per tile (MMA M)
+constexpr int kBN = 256;            // vocabulary rows per tile (MMA N)
+constexpr int kBK = 64;             // K per stage
+constexpr int kStages = 4;
+constexpr int kATileBytes = kBM * kBK * 2;     // 16 KB
+constexpr int kBTileBytes = kBN * kBK * 2;     // 32 KB
+constexpr int kTmemCols = 512;                 // two 256-column accumulators
+constexpr int kOffA = 0;
+constexpr int kOffB = kOffA + kStages * kATileBytes;
+constexpr int kOffBars = kOffB + kStages * kBTileBytes;
+constexpr int kNumBars = 2 * kStages + 5;
+constexpr int kOffMisc = kOffBars + kNumBars * 8;
+constexpr int kOffHalf = kOffMisc + 16;                            // Best[128]: second-half results
+constexpr int kSmemBytes = kOffHalf + kBM * 8 + 1024;
+
+struct BatchArgs {
+  Problem p;            // rows [0, p.B) of this launch's batch slice
+  Partial* partials;    // row b's candidates at partials[b * n_groups + q], q < n_groups
+  int nbt;              // batch tiles of this launch
+  int n_groups;         // CTA groups = gridDim.x / nbt (= candidates per row)
+  int n_vt;             // vocabulary tiles = ceil(V_local / 256)
+  int* err;
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+tc_batch_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_constant__ CUtensorMap tmap_w,
+                const BatchArgs args) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + kOffBars);
+  uint64_t* empty_bar = full_bar + kStages;
+  uint64_t* tfull_bar = empty_bar + kStages;
+  uint64_t* tempty_bar = tfull_bar + 2;
+  uint64_t* drain_bar = tempty_bar + 2;
+  uint32_t* tmem_base_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
+  Best* half_best = reinterpret_cast<Best*>(smem + kOffHalf);
+
+  const Problem& p = args.p;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int bt = blockIdx.x % args.nbt;
+  const int q = blockIdx.x / args.nbt;
+  const int n_tiles = q < args.n_vt ? (args.n_vt - 1 - q) / args.n_groups + 1 : 0;
+  const int n_kb = static_cast<int>((p.d + kBK - 1) / kBK);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull_bar[a], 1);
+      mbar_init(&tempty_bar[a], kEpiWarps * 32);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == kProducerWarp && lane == 0) {
+    tma_prefetch_desc(&tmap_h);
+    tma_prefetch_desc(&tmap_w);
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(tmem_base_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_base_slot;
+
+  if (warp == kProducerWarp) {
+    // ---------------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      const uint64_t pol_w = policy_evict_first();
+      const uint64_t pol_h = policy_evict_last();
+      int stage = 0;
+      uint32_t phase = 0;
+      int64_t n_issued = 0;
+      bool ok = true;
+      for (int t = 0; t < n_tiles && ok; ++t) {
+        const int vt = q + t * args.n_groups;
+        for (int kb = 0; kb < n_kb; ++kb) {
+          if (!mbar_wait(&empty_bar[stage], phase ^ 1, args.err, abort_flag)) { ok = false; break; }
+          mbar_arrive_expect_tx(&full_bar[stage], kATileBytes + kBTileBytes);
+          tma_load_2d(smem + kOffA + stage * kATileBytes, &tmap_h, &full_bar[stage], kb * kBK, bt * kBM,
+                      pol_h);
+          tma_load_2d(smem + kOffB + stage * kBTileBytes, &tmap_w, &full_bar[stage], kb * kBK, vt * kBN,
+                      pol_w);
+          ++n_issued;
+          if (++stage == kStages) { stage = 0; phase ^= 1; }
+        }
+      }
+      if (!ok) {
+        volatile int no_abort = 0;
+        for (int64_t i = std::max<int64_t>(0, n_issued - kStages); i < n_issued; ++i)
+          mbar_wait(&full_bar[i % kStages], static_cast<uint32_t>((i / kStages) & 1), args.err, &no_abort);
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBN);
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int t = 0; t < n_tiles && ok; ++t) {
+        const int acc = t & 1;
+        const uint32_t acc_phase = (t >> 1) & 1;
+        if (!mbar_wait(&tempty_bar[acc], acc_phase ^ 1, args.err, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * kBN;
+        for (int kb = 0; kb < n_kb; ++kb) {
+          if (!mbar_wait(&full_bar[stage], phase, args.err, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(smem + kOffA + stage * kATileBytes);
+          const uint32_t b_addr = smem_u32(smem + kOffB + stage * kBTileBytes);
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k)
+            mma_bf16(d_tmem, smem_desc_k128(a_addr + k * 32), smem_desc_k128(b_addr + k * 32), idesc,
+                     (kb | k) != 0);
+          mma_commit(&empty_bar[stage]);
+          if (++stage == kStages) { stage = 0; phase ^= 1; }
+        }
+        if (ok) mma_commit(&tfull_bar[acc]);
+      }
+      if (!ok) {
+        mma_commit(drain_bar);
+        volatile int no_abort = 0;
+        mbar_wait(drain_bar, 0, args.err, &no_abort);
+      }
+    }
+  } else {
+    // ---------------------------------------------------------------- epilogue (warps 0-7)
+    const int quad = warp & 3;                 // TMEM lane quadrant
+    const int half = warp >> 2;                // column half of the 256-wide tile
+    const int row_in_tile = quad * 32 + lane;
+    const int64_t b = static_cast<int64_t>(bt) * kBM + row_in_tile;
+    const bool row_ok = b < p.B;
+    const RowTemp rt = row_temp(row_ok ? p.temp[b] : -1.0f);
+    const bool active = row_ok && rt.mode != kRowInvalid;
+    const bool greedy = rt.mode == kRowGreedy;
+    const PhiloxKey key{static_cast<uint32_t>(p.seed), static_cast<uint32_t>(p.seed >> 32)};
+    const uint32_t step_lo = static_cast<uint32_t>(p.step);
+    const uint32_t step_hi = static_cast<uint32_t>(p.step >> 32);
+    const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
+    Best best = best_none();
+
+    for (int t = 0; t < n_tiles; ++t) {
+      const int acc = t & 1;
+      const uint32_t acc_phase = (t >> 1) & 1;
+      if (!mbar_wait(&tfull_bar[acc], acc_phase, args.err, abort_flag)) break;
+      tc_fence_after();
+      const int vt = q + t * args.n_groups;
+      const int64_t col0 = static_cast<int64_t>(vt) * kBN + half * (kBN / 2);   // local vocabulary row
+#pragma unroll 1
+      for (int c = 0; c < kBN / 2; c += 32) {
+        uint32_t r[32];
+        tmem_ld_32(tmem_base + lane_addr + acc * kBN + half * (kBN / 2) + c, r);
+        tmem_ld_wait();
+        const int64_t v0 = col0 + c;                       // local id of r[0]
+        if (active && v0 < p.V_local) {
+          const int64_t vg0 = p.v_offset + v0;
+          uint4 w = make_uint4(0, 0, 0, 0);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int64_t vg = vg0 + j;
+            if (j == 0 || (vg & 3) == 0)
+              w = noise_words(key, static_cast<uint32_t>(vg >> 2), static_cast<uint32_t>(b), step_lo, step_hi);
+            float logit = __uint_as_float(r[j]);
+            if (p.bias != nullptr && v0 + j < p.V_local) logit += p.bias[b * p.bias_stride + v0 + j];
+            const float g = gumbel_from_word(word_of(w, static_cast<uint32_t>(vg & 3)));
+            const float z = greedy ? logit : fmaf(logit, rt.inv_t, g);
+            if (v0 + j < p.V_local && z > best.z) {   // ids rise: strict > keeps the smaller id
+              best.z = z;
+              best.id = static_cast<int32_t>(vg);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&tempty_bar[acc]);
+    }
+    // combine the two column halves of each row, then one candidate per (row, group)
+    if (half == 1) half_best[row_in_tile] = best;
+    asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
+    if (half == 0 && row_ok) {
+      best = combine(best, half_best[row_in_tile]);
+      Partial out;
+      out.z = best.z;
+      out.id = best.id;
+      args.partials[b * args.n_groups + q] = out;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kMmaWarp) tmem_dealloc(tmem_base, kTmemCols);
+}
+
+}  // namespace
+
+// Geometry of one launch over a batch slice of B rows.
+struct BatchGeometry {
+  int nbt, n_groups, grid;
+};
+
+static BatchGeometry batch_geometry(int64_t B, int sms) {
+  BatchGeometry g;
+  g.nbt = static_cast<int>((B + kBM - 1) / kBM);
+  g.n_groups = std::max(1, sms / g.nbt);
+  g.grid = g.n_groups * g.nbt;
+  return g;
+}
+
+int64_t tc_batch_max_rows_per_launch(int device) {
+  int sms = 0;
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
+  if (sms <= 0) sms = 148;
+  return static_cast<int64_t>(sms) * kBM;
+}
+
+int tc_batch_num_parts(const Problem& p, int device) {
+  int sms = 0;
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
+  if (sms <= 0) sms = 148;
+  const int64_t slice = tc_batch_max_rows_per_launch(device);
+  // every launch slice writes its rows' candidates at the same stride
+  const int64_t first = std::min<int64_t>(p.B, slice);
+  return batch_geometry(first, sms).n_groups;
+}
+
+cudaError_t launch_tc_batch(const Problem& p, Partial* partials, int n_parts, int* err,
+                            cudaStream_t stream) {
+  if (p.d < kBK) return cudaErrorNotSupported;
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (sms <= 0) sms = 148;
+  cudaError_t e = cudaFuncSetAttribute(tc_batch_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  CUtensorMap tw;
+  if (!encode_kmajor_bf16(&tw, p.W, p.V_local, p.d, kBK, kBN)) return cudaErrorInvalidValue;
+  const int64_t slice = tc_batch_max_rows_per_launch(dev);
+  for (int64_t b0 = 0; b0 < p.B; b0 += slice) {
+    Problem ps = p;
+    ps.B = std::min<int64_t>(slice, p.B - b0);
+    ps.h = static_cast<const uint16_t*>(p.h) + b0 * p.d;
+    ps.temp = p.temp + b0;
+    if (p.bias != nullptr) ps.bias = p.bias + b0 * p.bias_stride;
+    // Every slice uses n_parts groups so all rows share the candidate stride;
+    // a later (shorter) slice has at least as many groups available.
+    const BatchGeometry g = batch_geometry(ps.B, sms);
+    if (g.n_groups < n_parts) return cudaErrorInvalidValue;
+    CUtensorMap th;
+    if (!encode_kmajor_bf16(&th, ps.h, ps.B, p.d, kBK, kBM)) return cudaErrorInvalidValue;
+    BatchArgs a{ps, partials + b0 * n_parts, g.nbt, n_parts,
+                static_cast<int>((p.V_local + kBN - 1) / kBN), err};
+    tc_batch_kernel<<<n_parts * g.nbt, kThreads, kSmemBytes, stream>>>(th, tw, a);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+}  // namespace fs

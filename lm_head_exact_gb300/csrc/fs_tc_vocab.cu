@@ -28,6 +28,7 @@
 
 #include "fs_internal.h"
 #include "fs_sm100.cuh"
+#include "fs_tmap.h"
 
 namespace fs {
 namespace {
@@ -277,41 +278,14 @@ tc_vocab_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
 }
 
 // ------------------------------------------------------------------ host side
-PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (fn == nullptr) {
-    cudaDriverEntryPointQueryResult q;
-    void* ptr = nullptr;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  }
-  return fn;
-}
-
-// bf16 [rows, d] row-major, box = 64 elements x box_rows rows, 128-byte swizzle.
-bool encode_kmajor(CUtensorMap* tm, const void* base, int64_t rows, int64_t d, int box_rows) {
-  auto encode = get_encode();
-  if (encode == nullptr) return false;
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(d) * 2};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(box_rows)};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = encode(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
-                      estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
-
 template <int BN>
 cudaError_t launch_bn(const Problem& p, Partial* partials, int n_parts, int* err, cudaStream_t stream) {
   using C = VocabCfg<BN>;
   static_assert(C::kStages >= 2, "pipeline needs at least two stages");
   static_assert(C::kSmemBytes <= 227 * 1024, "shared memory budget");
   CUtensorMap tw, th;
-  if (!encode_kmajor(&tw, p.W, p.V_local, p.d, kUnitRows)) return cudaErrorInvalidValue;
-  if (!encode_kmajor(&th, p.h, p.B, p.d, BN)) return cudaErrorInvalidValue;
+  if (!encode_kmajor_bf16(&tw, p.W, p.V_local, p.d, kBK, kUnitRows)) return cudaErrorInvalidValue;
+  if (!encode_kmajor_bf16(&th, p.h, p.B, p.d, kBK, BN)) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(tc_vocab_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::kSmemBytes);
   if (e != cudaSuccess) return e;

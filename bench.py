@@ -4,7 +4,7 @@ Metric: fused LM-head sample microseconds per decode step and the fraction of
 the HBM / tensor-core roofline, versus batch, on a Llama-3-8B-shaped LM head
 (d = 4096, V = 128256; synthetic bf16 weights and hidden states -- no trained
 weights or datasets).  One step is one call of the public sampling entry point
-(fused kernel + cross-tile reduction) over one batch of hidden states with
+(one fused-kernel launch; the cross-tile reduction finishes inside it) over one batch of hidden states with
 its own step counter.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--batch B] [--impl ours|reference]
@@ -267,7 +267,7 @@ def run_ours(args):
         clocks.stop()
     step_ms = max_over_ranks(total_ms / args.steps, dist, device="cuda")
     kern_ms = max_over_ranks(kern_ms, dist, device="cuda")
-    launches = 2 * args.steps          # fused kernel + cross-tile reduction per step
+    launches = args.steps              # one fused kernel per step (the cross-tile finish is in-kernel)
 
     # end to end through the host-buffer entry point: pinned h / temp in,
     # ids / max out, every step
@@ -313,6 +313,26 @@ def run_ours(args):
             sweep.append(point("qwen3_8b", b, h_big, Wq, tq, qshape["V"], qshape["d"]))
         del Wq
 
+    # the unfused comparison pipeline on the same workload: GEMM -> fp32
+    # logits in HBM -> softmax -> sample (the traffic fusion removes)
+    unfused = None
+    if not args.no_sweep:
+        with torch.cuda.stream(stream):
+            for i in range(3):
+                fs.sample_unfused(hd, Wd, td, seed, i, stream=stream)
+            u0 = torch.cuda.Event(enable_timing=True)
+            u1 = torch.cuda.Event(enable_timing=True)
+            u0.record(stream)
+            for i in range(20):
+                fs.sample_unfused(hd, Wd, td, seed, 3 + i, stream=stream)
+            u1.record(stream)
+        torch.cuda.synchronize()
+        uus = u0.elapsed_time(u1) / 20 * 1e3
+        unfused = {"us_per_step": round(uus, 2), "fused_us_per_step": round(step_ms * 1e3, 2),
+                   "speedup_of_fusion": round(uus / (step_ms * 1e3), 3),
+                   "extra_hbm_bytes_per_step": 20 * B * V,
+                   "note": "logits write 4BV + softmax reads 8BV, writes 4BV + sample reads 4BV"}
+
     result = None
     if rank == 0:
         us = step_ms * 1e3
@@ -336,6 +356,7 @@ def run_ours(args):
             "clocks": clocks.summary() if clocks else None,
             "gpu_launches": launches,
             "sweep": sweep,
+            "unfused": unfused,
         }
         if not args.no_cpu_baseline:
             result["cpu_baseline"] = cpu_baseline(B, args.cpu_seconds)

@@ -33,9 +33,11 @@
  *    on `stream` (a cudaStream_t; NULL is the legacy default stream) and
  *    returns without synchronizing.  Results are valid once the stream has
  *    reached that point.
- *  - The library owns one workspace per (device, stream) that holds the
- *    per-(row, tile) candidates.  It grows on demand, which is not allowed
- *    inside CUDA-graph capture: call fs_workspace_reserve() first.
+ *  - The library owns one small workspace per (device, stream): a ticket
+ *    counter and one packed candidate key per batch row, through which the
+ *    CTAs of the fused kernel finish the sample (the last CTA to finish writes
+ *    the outputs).  It grows on demand, which is not allowed inside
+ *    CUDA-graph capture: call fs_workspace_reserve() first.
  *  - Errors: argument problems return FS_ERR_INVALID_ARG / FS_ERR_UNSUPPORTED
  *    before anything is enqueued; a failed CUDA call returns FS_ERR_CUDA.
  *    fs_last_error() gives a human-readable detail of the last failure on
@@ -124,6 +126,23 @@ FS_API fs_status fs_sample_chunked(const void* h, const void* W_chunk, int64_t B
                             int64_t* out_ids, float* out_max, void* stream);
 
 /*
+ * The UNFUSED comparison pipeline (summary page, "Method", ops (1)-(4)):
+ * a tensor-core GEMM writes fp32 logits [B, V] (+ bias) to device memory,
+ * a softmax kernel reads them and writes probabilities [B, V], and a sample
+ * kernel re-reads those and picks argmax_v p_v / (-log u_v) with the same
+ * Philox draws.  Same arguments and outputs as fs_sample_ex; ids agree with
+ * the fused path up to rounding near ties.  It exists to measure the memory
+ * traffic fusion removes (about 20 * B * V bytes per step).
+ *   logits_out (device fp32 [B, V], nullable): where the GEMM writes the
+ *     logits; NULL uses library workspace.  Probabilities always live in
+ *     library workspace.  Needs d >= 64.
+ */
+FS_API fs_status fs_sample_unfused(const void* h, const void* W, int64_t B, int64_t d, int64_t V,
+                                   const float* temp, const float* bias, int64_t bias_row_stride,
+                                   uint64_t seed, uint64_t step, int64_t* out_ids, float* out_max,
+                                   float* logits_out, void* stream);
+
+/*
  * End-to-end convenience call with HOST buffers: copies h_host [B, d] bf16 and
  * temp_host [B] fp32 to the device, samples against the device-resident
  * W [V, d] (and optional device bias), copies out_ids_host [B] int64 and
@@ -141,17 +160,18 @@ FS_API fs_status fs_sample_host(const void* h_host, const void* W, int64_t B, in
  * fs_sample without any device-memory allocation.  (An engineering variant:
  * the FlashSampling paper has no counterpart.)  Same arguments, results and
  * noise as fs_sample, computed by the same tensor-core kernel, but the
- * per-(row, tile) candidates live in a fixed static device array inside the
- * library (about 320 KB per GPU, held until the process exits) instead of a
- * workspace the library cudaMalloc's on demand.  For callers that cannot let
+ * cross-tile finish area (ticket counter + one candidate key per row) lives
+ * in a fixed static device array inside the library (2.3 KB per GPU, held
+ * until the process exits) instead of a workspace the library cudaMalloc's
+ * on demand.  For callers that cannot let
  * a library allocate or free device memory: an allocator that already owns
  * the GPU's memory budget, or code that cannot afford the device-wide
  * synchronization of cudaFree.
  *   Limits: 1 <= B <= 256 (larger B returns FS_ERR_UNSUPPORTED with a
  *   message), d >= 64 and a multiple of 8; no bias.
  *   Set-up: the first call on each device looks up the array's device
- *   address (cudaGetSymbolAddress) and clears its status word; make that
- *   first call before any stream capture starts.
+ *   address (cudaGetSymbolAddress) and zeroes it; make that first call
+ *   before any stream capture starts.
  *   Sharing: every call on a device uses the same array and finds the last
  *   call's contents there.  Calls whose kernels overlap on the GPU (e.g. on
  *   unordered streams) race on it; keep them ordered on one stream.
@@ -192,6 +212,15 @@ FS_API fs_status fs_profile_events(void* start, void* stop);
 /* Read and clear the device error word of the current device (synchronizes
  * the device).  *code receives 0 when no kernel reported a problem. */
 FS_API fs_status fs_device_error(int* code);
+
+/*
+ * Failure-path check: enqueue a one-warp kernel whose bounded mbarrier wait
+ * (the kind every tensor-core kernel uses) waits for an arrival that never
+ * comes, gives up after timeout_ns (0 < timeout_ns <= 1e9) and sets the device
+ * error word to 1 -- as a real stall would -- without faulting the context.
+ * fs_device_error() then reports and clears it.
+ */
+FS_API fs_status fs_debug_wait_timeout(uint64_t timeout_ns, void* stream);
 
 /* Static name of a status code. */
 FS_API const char* fs_status_string(fs_status s);

@@ -33,6 +33,8 @@ SIGNATURES = {
     "fs_sample_chunked": (_int, [_c_void_p, _c_void_p, _i64, _i64, _i64, _i64, _c_void_p,
                                  _c_void_p, _i64, _u64, _u64, _c_void_p, _c_void_p, _int,
                                  _c_void_p, _c_void_p, _c_void_p]),
+    "fs_sample_unfused": (_int, [_c_void_p, _c_void_p, _i64, _i64, _i64, _c_void_p, _c_void_p, _i64,
+                                 _u64, _u64, _c_void_p, _c_void_p, _c_void_p, _c_void_p]),
     "fs_sample_host": (_int, [_c_void_p, _c_void_p, _i64, _i64, _i64, _c_void_p, _c_void_p, _i64,
                               _u64, _u64, _c_void_p, _c_void_p, _c_void_p]),
     "fs_sample_noalloc": (_int, [_c_void_p, _c_void_p, _i64, _i64, _i64, _c_void_p, _u64, _u64,
@@ -44,6 +46,7 @@ SIGNATURES = {
     "fs_path_for_batch": (_int, [_i64]),
     "fs_profile_events": (_int, [_c_void_p, _c_void_p]),
     "fs_device_error": (_int, [ctypes.POINTER(_int)]),
+    "fs_debug_wait_timeout": (_int, [_u64, _c_void_p]),
     "fs_status_string": (ctypes.c_char_p, [_int]),
     "fs_last_error": (ctypes.c_char_p, []),
     "fs_debug_noise": (_int, [_u64, _u64, _i64, _i64, _i64, _i64, _c_void_p, _c_void_p, _c_void_p]),
@@ -144,6 +147,23 @@ def sample(h, W, temp, seed, step, bias=None, out=None, stream=None):
     return ids, mx
 
 
+def sample_unfused(h, W, temp, seed, step, bias=None, logits_out=None, out=None, stream=None):
+    """The unfused comparison pipeline (GEMM -> fp32 logits in HBM -> softmax
+    -> sample).  Same inputs / outputs as ``sample``; ``logits_out`` (fp32
+    [B, V] CUDA tensor) receives the logits if given."""
+    torch = _torch()
+    B, d = h.shape
+    V = W.shape[0]
+    ids, mx = _outs(B, h.device, out)
+    bptr, bstride = _bias_args(bias, B, V)
+    lptr = _dev(logits_out, "logits_out", torch.float32) if logits_out is not None else ctypes.c_void_p(0)
+    check(library().fs_sample_unfused(_dev(h, "h", torch.bfloat16, 2), _dev(W, "W", torch.bfloat16, 2),
+                                      B, d, V, _dev(temp, "temp", torch.float32, 1), bptr, bstride,
+                                      seed, step, _dev(ids, "out_ids", torch.int64),
+                                      _dev(mx, "out_max", torch.float32), lptr, _stream_ptr(stream)))
+    return ids, mx
+
+
 def sample_ex(*args, **kwargs):
     """Alias of ``sample`` (the bias argument maps to fs_sample_ex)."""
     return sample(*args, **kwargs)
@@ -234,6 +254,10 @@ def profile_events(start, stop):
     else:
         check(library().fs_profile_events(ctypes.c_void_p(start.cuda_event),
                                           ctypes.c_void_p(stop.cuda_event)))
+
+
+def debug_wait_timeout(timeout_ns, stream=None):
+    check(library().fs_debug_wait_timeout(timeout_ns, _stream_ptr(stream)))
 
 
 def device_error():

@@ -35,35 +35,28 @@ fs_status cuda_fail(cudaError_t e, const char* what) {
 }
 
 // ---------------------------------------------------------------- workspace
+// Per (device, stream): the finish area of the fused kernels -- a ticket
+// counter (at offset 0, padded to 256 bytes) followed by one packed 64-bit
+// candidate key per batch row; all zero between calls (zeroed on allocation,
+// re-zeroed by the last CTA of every call) -- plus staging for the host entry
+// point and the unfused pipeline's logits / probabilities.
 struct Workspace {
-  void* partials = nullptr;
-  size_t partial_bytes = 0;
+  void* finish = nullptr;
+  size_t finish_bytes = 0;
   void* staging = nullptr;      // device staging of fs_sample_host
   size_t staging_bytes = 0;
+  void* unfused = nullptr;      // logits + probabilities of fs_sample_unfused
+  size_t unfused_bytes = 0;
 };
 
 std::mutex g_ws_mutex;
 std::map<std::pair<int, cudaStream_t>, Workspace> g_workspaces;
 std::map<int, int*> g_error_words;   // per device: kernels' bounded-wait error word
 
-int num_sms(int device) {
-  int sms = 0;
-  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess || sms <= 0)
-    sms = 148;
-  return sms;
-}
+constexpr size_t kFinishHeader = 256;
 
-// Upper bound of the candidates per row any kernel family produces for a
-// vocabulary of V rows (used to size reservations ahead of graph capture).
-int64_t max_parts(int64_t V, int device) {
-  const int64_t sms = num_sms(device);
-  const int64_t simt = std::min<int64_t>(sms * 8, (V + 7) / 8);   // CUDA-core path: blocks
-  return std::max<int64_t>(std::max<int64_t>(simt, sms), 1);       // tensor-core paths: <= one per SM
-}
-
-size_t partial_bytes(int64_t B, int64_t parts) {
-  return static_cast<size_t>(std::max<int64_t>(B, 1)) * static_cast<size_t>(std::max<int64_t>(parts, 1)) *
-         sizeof(Partial);
+size_t finish_bytes_for(int64_t B) {
+  return kFinishHeader + static_cast<size_t>(std::max<int64_t>(B, 1)) * sizeof(unsigned long long);
 }
 
 bool capturing(cudaStream_t stream) {
@@ -102,15 +95,25 @@ fs_status current_device(int* dev) {
   return FS_OK;
 }
 
-fs_status get_partials(cudaStream_t stream, size_t bytes, Partial** out) {
+// The finish area of (current device, stream) for batches up to B rows.
+fs_status get_finish(cudaStream_t stream, int64_t B, Finish* f) {
   int dev;
   fs_status s = current_device(&dev);
   if (s != FS_OK) return s;
   std::lock_guard<std::mutex> lock(g_ws_mutex);
   Workspace& ws = g_workspaces[{dev, stream}];
-  s = grow(&ws.partials, &ws.partial_bytes, bytes, stream);
-  if (s != FS_OK) return s;
-  *out = static_cast<Partial*>(ws.partials);
+  const size_t need = finish_bytes_for(B);
+  if (ws.finish_bytes < need) {
+    s = grow(&ws.finish, &ws.finish_bytes, need, stream);
+    if (s != FS_OK) return s;
+    cudaError_t e = cudaMemset(ws.finish, 0, ws.finish_bytes);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return fail(FS_ERR_WORKSPACE, "zeroing the workspace failed: %s", cudaGetErrorString(e));
+    }
+  }
+  f->counter = static_cast<unsigned int*>(ws.finish);
+  f->keys = reinterpret_cast<unsigned long long*>(static_cast<char*>(ws.finish) + kFinishHeader);
   return FS_OK;
 }
 
@@ -208,68 +211,55 @@ fs_status check_problem(const Problem& p, bool need_out, const void* out_ids, co
 // model width, identical for every chunk of a chunked run) only -- never from
 // V or the chunk range -- so one-shot and chunked runs compute every logit
 // with the same kernel and agree bit for bit.
+constexpr int64_t kVocabMajorMaxBatch = 64;
+
 int resolve_path(int64_t B, int64_t d) {
   int path = g_forced_path.load();
-  if (path == kPathAuto) path = (B <= 256) ? kPathTcVocab : kPathTcBatch;
+  // Measured on GB300 (Llama-3-8B head): vocabulary-major streams W fastest
+  // up to B = 64; from B = 96 the batch-major kernel, whose W tiles are
+  // shared by the batch tiles of a CTA group through L2, is faster.
+  if (path == kPathAuto) path = (B <= kVocabMajorMaxBatch) ? kPathTcVocab : kPathTcBatch;
   if (path == kPathTcVocab && B > 256) path = kPathTcBatch;
   if ((path == kPathTcVocab || path == kPathTcBatch) && d < 64) path = kPathSimt;
   return path;
 }
 
-// Fused kernel + cross-part reduction for one problem.
+// One fused launch (kernel + in-kernel cross-CTA finish) for one problem.
 fs_status run(const Problem& p, Finish f, cudaStream_t stream) {
   if (p.B == 0) return FS_OK;
-  int dev;
-  FS_TRY(current_device(&dev));
+  if (p.V_local == 0) {                 // no vocabulary: every row gets "no sample"
+    f.partials = nullptr;
+    f.n_parts = 0;
+    cudaError_t e = launch_reduce(f, p.B, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "reduction kernel launch");
+    return FS_OK;
+  }
+  FS_TRY(get_finish(stream, p.B, &f));
   const int path = resolve_path(p.B, p.d);
-  int n_parts = 0;
   int* err = nullptr;
-  if (p.V_local > 0) {
-    switch (path) {
-      case kPathTcVocab:
-        n_parts = tc_vocab_num_parts(p, dev);
-        FS_TRY(error_word(&err));
-        break;
-      case kPathTcBatch:
-        n_parts = tc_batch_num_parts(p, dev);
-        FS_TRY(error_word(&err));
-        break;
-      case kPathSimt:
-      default:
-        n_parts = simt_num_parts(p, dev);
-        break;
-    }
+  if (path != kPathSimt) FS_TRY(error_word(&err));
+  cudaError_t e = cudaSuccess;
+  if (g_prof_start != nullptr) {
+    e = cudaEventRecord(g_prof_start, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord(start)");
   }
-  Partial* partials = nullptr;
-  FS_TRY(get_partials(stream, partial_bytes(p.B, n_parts), &partials));
-  f.partials = partials;
-  f.n_parts = n_parts;
-  if (p.V_local > 0) {
-    cudaError_t e = cudaSuccess;
-    if (g_prof_start != nullptr) {
-      e = cudaEventRecord(g_prof_start, stream);
-      if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord(start)");
-    }
-    switch (path) {
-      case kPathTcVocab:
-        e = launch_tc_vocab(p, partials, n_parts, err, stream);
-        break;
-      case kPathTcBatch:
-        e = launch_tc_batch(p, partials, n_parts, err, stream);
-        break;
-      case kPathSimt:
-      default:
-        e = launch_simt(p, partials, n_parts, stream);
-        break;
-    }
-    if (e != cudaSuccess) return cuda_fail(e, "fused sampling kernel launch");
-    if (g_prof_stop != nullptr) {
-      e = cudaEventRecord(g_prof_stop, stream);
-      if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord(stop)");
-    }
+  switch (path) {
+    case kPathTcVocab:
+      e = launch_tc_vocab(p, f, err, stream);
+      break;
+    case kPathTcBatch:
+      e = launch_tc_batch(p, f, err, stream);
+      break;
+    case kPathSimt:
+    default:
+      e = launch_simt(p, f, stream);
+      break;
   }
-  cudaError_t e = launch_reduce(f, p.B, stream);
-  if (e != cudaSuccess) return cuda_fail(e, "reduction kernel launch");
+  if (e != cudaSuccess) return cuda_fail(e, "fused sampling kernel launch");
+  if (g_prof_stop != nullptr) {
+    e = cudaEventRecord(g_prof_stop, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord(stop)");
+  }
   return FS_OK;
 }
 
@@ -378,19 +368,60 @@ fs_status fs_sample_host(const void* h_host, const void* W, int64_t B, int64_t d
   return FS_OK;
 }
 
+fs_status fs_sample_unfused(const void* h, const void* W, int64_t B, int64_t d, int64_t V,
+                            const float* temp, const float* bias, int64_t bias_row_stride,
+                            uint64_t seed, uint64_t step, int64_t* out_ids, float* out_max,
+                            float* logits_out, void* stream_) {
+  g_last_error[0] = '\0';
+  Problem p{h, W, B, d, V, 0, temp, bias, bias_row_stride, seed, step};
+  FS_TRY(check_problem(p, true, out_ids, out_max));
+  if (B == 0) return FS_OK;
+  if (d < 64) return fail(FS_ERR_UNSUPPORTED, "the unfused path needs d >= 64");
+  if (logits_out != nullptr) {
+    FS_TRY(check_device_ptr(logits_out, "logits_out"));
+    FS_TRY(check_aligned(logits_out, 4, "logits_out"));
+  }
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  if (V == 0) {
+    Finish f{};
+    f.write_out = true;
+    f.out_ids = out_ids;
+    f.out_max = out_max;
+    cudaError_t e = launch_reduce(f, B, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "reduction kernel launch");
+    return FS_OK;
+  }
+  int dev;
+  FS_TRY(current_device(&dev));
+  const size_t plane = (static_cast<size_t>(B) * static_cast<size_t>(V) * 4 + 255) & ~size_t(255);
+  char* buf = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_ws_mutex);
+    Workspace& ws = g_workspaces[{dev, stream}];
+    FS_TRY(grow(&ws.unfused, &ws.unfused_bytes, logits_out ? plane : 2 * plane, stream));
+    buf = static_cast<char*>(ws.unfused);
+  }
+  float* logits = logits_out ? logits_out : reinterpret_cast<float*>(buf);
+  float* probs = reinterpret_cast<float*>(logits_out ? buf : buf + plane);
+  int* err = nullptr;
+  FS_TRY(error_word(&err));
+  cudaError_t e = launch_tc_logits(p, logits, err, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "logits GEMM launch");
+  e = launch_unfused_tail(p, logits, probs, out_ids, out_max, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "softmax / sample launch");
+  return FS_OK;
+}
+
 size_t fs_workspace_bytes(int64_t B, int64_t V) {
-  int dev = 0;
-  cudaGetDevice(&dev);
-  return partial_bytes(B, max_parts(V, dev));
+  (void)V;
+  return finish_bytes_for(B);
 }
 
 fs_status fs_workspace_reserve(int64_t B, int64_t V, void* stream) {
   g_last_error[0] = '\0';
   if (B < 0 || V < 0) return fail(FS_ERR_INVALID_ARG, "need B >= 0 and V >= 0");
-  int dev;
-  FS_TRY(current_device(&dev));
-  Partial* p = nullptr;
-  return get_partials(static_cast<cudaStream_t>(stream), partial_bytes(B, max_parts(V, dev)), &p);
+  Finish f{};
+  return get_finish(static_cast<cudaStream_t>(stream), B, &f);
 }
 
 fs_status fs_workspace_release(void) {
@@ -400,7 +431,8 @@ fs_status fs_workspace_release(void) {
   for (auto it = g_workspaces.begin(); it != g_workspaces.end();) {
     if (it->first.first == dev) {
       cudaStreamSynchronize(it->first.second);
-      if (it->second.partials) cudaFree(it->second.partials);
+      if (it->second.finish) cudaFree(it->second.finish);
+      if (it->second.unfused) cudaFree(it->second.unfused);
       if (it->second.staging) cudaFree(it->second.staging);
       it = g_workspaces.erase(it);
     } else {
@@ -436,6 +468,17 @@ fs_status fs_device_error(int* code) {
   e = cudaMemcpy(code, w, sizeof(int), cudaMemcpyDeviceToHost);
   if (e == cudaSuccess) e = cudaMemset(w, 0, sizeof(int));
   if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
+  return FS_OK;
+}
+
+fs_status fs_debug_wait_timeout(uint64_t timeout_ns, void* stream) {
+  g_last_error[0] = '\0';
+  if (timeout_ns == 0 || timeout_ns > 1000000000ull)
+    return fail(FS_ERR_INVALID_ARG, "timeout_ns must be in (0, 1e9]");
+  int* err = nullptr;
+  FS_TRY(error_word(&err));
+  cudaError_t e = launch_debug_wait(err, timeout_ns, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "wait kernel launch");
   return FS_OK;
 }
 

@@ -149,6 +149,30 @@ struct __align__(8) Partial {
   int32_t id;
 };
 
+// -------------------------------------------------------------------------
+// Packed candidate keys: one 64-bit word per row whose unsigned order is the
+// total order above, so atomicMax over all CTAs' candidates is the cross-tile
+// reduction (order-independent, hence deterministic).  High 32 bits: z mapped
+// to an order-preserving unsigned; low 32 bits: 0xFFFFFFFF - id (a smaller id
+// is larger).  0 means "no candidate" and is below every real key.
+// -------------------------------------------------------------------------
+__device__ __forceinline__ unsigned long long pack_key(float z, int32_t id) {
+  if (id == kNoId) return 0ull;
+  uint32_t u = __float_as_uint(z);
+  u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  return (static_cast<unsigned long long>(u) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(id));
+}
+
+__device__ __forceinline__ Best unpack_key(unsigned long long k) {
+  if (k == 0ull) return best_none();
+  uint32_t u = static_cast<uint32_t>(k >> 32);
+  u = (u & 0x80000000u) ? (u & 0x7FFFFFFFu) : ~u;
+  Best b;
+  b.z = __uint_as_float(u);
+  b.id = static_cast<int32_t>(0xFFFFFFFFu - static_cast<uint32_t>(k));
+  return b;
+}
+
 // Device error word: set by kernels whose bounded waits run out; read and
 // cleared by the host through fs_device_error().
 enum DeviceError : int {

@@ -26,10 +26,15 @@ struct Problem {
   uint64_t step;
 };
 
-// Where a launch leaves its per-(row, part) candidates, and how the final
-// reduction finishes them.
+// How a launch finishes the sample.  The fused kernels reduce across CTAs
+// themselves: every CTA atomicMax-es its per-row candidates into `keys`
+// (packed, see pack_key), and the CTA that finishes last -- counted in
+// `counter` -- turns the keys into outputs and zeroes keys and counter for the
+// next call.  The separate reduction kernel instead reads `partials`.
 struct Finish {
-  Partial* partials;      // [B, n_parts]
+  unsigned long long* keys;   // [B], zero between calls
+  unsigned int* counter;      // zero between calls
+  Partial* partials;      // [B, n_parts] (reduction-kernel path only)
   int n_parts;
   // chunked-variant carry (nullable): merged into the result, then updated
   float* carry_max;
@@ -43,25 +48,29 @@ struct Finish {
 // Kernel families selectable by batch size (or forced for tests).
 enum Path : int { kPathAuto = 0, kPathSimt = 1, kPathTcVocab = 2, kPathTcBatch = 3 };
 
-// Number of partial candidates per row each family produces for a problem;
-// used to size the workspace before launching.
-int simt_num_parts(const Problem& p, int device);
-
 // Launchers: enqueue on `stream`; return cudaSuccess or the launch error.
-cudaError_t launch_simt(const Problem& p, Partial* partials, int n_parts, cudaStream_t stream);
+// Each fused kernel finishes the sample itself through `f` (one launch).
+cudaError_t launch_simt(const Problem& p, const Finish& f, cudaStream_t stream);
 
-// Tensor-core vocabulary-major path (B <= 256, d >= 64): one candidate per
-// (row, CTA); `err` is the device error word its bounded waits report to.
-int tc_vocab_num_parts(const Problem& p, int device);
+// Tensor-core vocabulary-major path (B <= 256, d >= 64); `err` is the device
+// error word its bounded waits report to.
 int tc_vocab_bn(int64_t B);
-cudaError_t launch_tc_vocab(const Problem& p, Partial* partials, int n_parts, int* err,
-                            cudaStream_t stream);
-// Tensor-core batch-major path (any B, d >= 64; used for B > 256): one
-// candidate per (row, CTA group).
-int tc_batch_num_parts(const Problem& p, int device);
-cudaError_t launch_tc_batch(const Problem& p, Partial* partials, int n_parts, int* err,
-                            cudaStream_t stream);
+cudaError_t launch_tc_vocab(const Problem& p, const Finish& f, int* err, cudaStream_t stream);
 
+// Tensor-core batch-major path (any B, d >= 64; auto-selected for B > 64).
+cudaError_t launch_tc_batch(const Problem& p, const Finish& f, int* err, cudaStream_t stream);
+
+// Unfused comparison pipeline: tensor-core GEMM storing fp32 logits [B, V]
+// (+ bias) to HBM, then row softmax into probs [B, V], then the sample.
+cudaError_t launch_tc_logits(const Problem& p, float* logits, int* err, cudaStream_t stream);
+cudaError_t launch_unfused_tail(const Problem& p, float* logits, float* probs, int64_t* out_ids,
+                                float* out_max, cudaStream_t stream);
+
+// Failure-path check of the bounded waits: one wait that runs out after
+// timeout_ns and flags `err`.
+cudaError_t launch_debug_wait(int* err, uint64_t timeout_ns, cudaStream_t stream);
+
+// Reduction kernel over `f.partials` (used when no fused kernel runs: V == 0).
 cudaError_t launch_reduce(const Finish& f, int64_t B, cudaStream_t stream);
 
 // Set the calling thread's fs_last_error() text.

@@ -2,9 +2,10 @@
 // a fixed, statically allocated device array instead of the library's
 // cudaMalloc'ed workspace.
 //
-// Why it exists: fs_sample keeps its per-(row, CTA) candidates in a
-// workspace that the library allocates with cudaMalloc the first time a
-// (device, stream) needs it, and re-allocates when a larger call arrives.
+// Why it exists: fs_sample finishes the sample through a small workspace (a
+// ticket counter and one packed candidate key per batch row) that the
+// library allocates with cudaMalloc the first time a (device, stream) needs
+// it, and re-allocates when a larger batch arrives.
 // Some callers cannot let a library do that: serving stacks whose allocator
 // has already claimed the device memory budget (a library cudaMalloc then
 // fails or fragments memory it does not own), and callers that must not pay
@@ -12,19 +13,21 @@
 // replaced.  This entry point never allocates or frees device memory.
 //
 // The scratch lives in `g_noalloc_scratch` below, a file-scope static
-// __device__ array of kScratchBytes (about 320 KB) that every GPU loading the
-// library keeps until the process exits.  Host code cannot use the array's
-// name as a device address (it is a host-side stand-in), so the first call
-// on each device looks the address up with cudaGetSymbolAddress while that
-// device is current, clears the status word at the start of the array, and
-// caches the pointer for later calls on that device.  Make that first call on
-// each device before any stream capture begins.
+// __device__ array of kScratchBytes (2.3 KB: a 256-byte header holding the
+// bounded-wait status word and the ticket counter, then 256 candidate keys)
+// that every GPU loading the library keeps until the process exits.  Host
+// code cannot use the array's name as a device address (it is a host-side
+// stand-in), so the first call on each device looks the address up with
+// cudaGetSymbolAddress while that device is current, zeroes the whole array,
+// and caches the pointer for later calls on that device.  Make that first
+// call on each device before any stream capture begins.
 //
 // Every call on a device shares the one array and finds the previous call's
-// contents in it; each call writes every candidate slot it later reads, so no
-// clearing is needed between calls.  Calls whose kernels overlap on the GPU
-// (for example on two streams without ordering between them) race on the
-// array and may return wrong samples: order them on one stream.
+// contents in it.  The ticket and the keys must start each call at zero; the
+// kernel's last CTA zeroes them again before the call completes, so they are
+// zero for the next call.  Calls whose kernels overlap on the GPU (for
+// example on two streams without ordering between them) race on the array
+// and may return wrong samples: order them on one stream.
 #include <cstdio>
 #include <cstdint>
 #include <mutex>
@@ -36,12 +39,11 @@ namespace fs {
 namespace {
 
 // Largest batch this entry point accepts (the tensor-core vocabulary-major
-// kernel's limit) and the largest number of candidates per row it can hold
-// (one per CTA = one per SM; 160 covers GB300's 152 SMs).
+// kernel's limit): one packed candidate key per batch row.
 constexpr int64_t kNoAllocMaxBatch = 256;
-constexpr int64_t kNoAllocMaxParts = 160;
-constexpr size_t kHeaderBytes = 256;   // status word of the kernels' bounded waits, padded
-constexpr size_t kScratchBytes = kHeaderBytes + kNoAllocMaxBatch * kNoAllocMaxParts * sizeof(Partial);
+constexpr size_t kHeaderBytes = 256;   // [0]: bounded-wait status word, [64]: ticket counter
+constexpr size_t kCounterOffset = 64;
+constexpr size_t kScratchBytes = kHeaderBytes + kNoAllocMaxBatch * sizeof(unsigned long long);
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
@@ -57,7 +59,7 @@ fs_status noalloc_fail(fs_status s, const char* msg) {
 }
 
 // Device address of the static scratch on the current device; the first
-// call per device resolves it and zeroes the status word.
+// call per device resolves it and zeroes the whole array.
 fs_status scratch_for_current_device(unsigned char** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
@@ -70,10 +72,10 @@ fs_status scratch_for_current_device(unsigned char** out) {
       cudaGetLastError();
       return noalloc_fail(FS_ERR_CUDA, "cudaGetSymbolAddress of the static scratch failed");
     }
-    e = cudaMemset(ptr, 0, kHeaderBytes);
+    e = cudaMemset(ptr, 0, kScratchBytes);
     if (e != cudaSuccess) {
       cudaGetLastError();
-      return noalloc_fail(FS_ERR_CUDA, "clearing the static scratch status word failed");
+      return noalloc_fail(FS_ERR_CUDA, "clearing the static scratch failed");
     }
     g_scratch_ptr[dev] = ptr;
   }
@@ -119,32 +121,18 @@ extern "C" FS_API fs_status fs_sample_noalloc(const void* h, const void* W, int6
   fs_status s = scratch_for_current_device(&scratch);
   if (s != FS_OK) return s;
   int* status_word = reinterpret_cast<int*>(scratch);
-  Partial* partials = reinterpret_cast<Partial*>(scratch + kHeaderBytes);
-
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
-  Problem p{h, W, B, d, V, 0, temp, nullptr, 0, seed, step};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  const int n_parts = V > 0 ? tc_vocab_num_parts(p, dev) : 0;
-  if (n_parts > kNoAllocMaxParts)
-    return noalloc_fail(FS_ERR_UNSUPPORTED, "this device has more SMs than the static scratch holds");
-  if (V > 0) {
-    cudaError_t e = launch_tc_vocab(p, partials, n_parts, status_word, stream);
-    if (e != cudaSuccess) {
-      cudaGetLastError();
-      return noalloc_fail(FS_ERR_CUDA, "fused sampling kernel launch failed");
-    }
-  }
   Finish f{};
-  f.partials = partials;
-  f.n_parts = n_parts;
+  f.counter = reinterpret_cast<unsigned int*>(scratch + kCounterOffset);
+  f.keys = reinterpret_cast<unsigned long long*>(scratch + kHeaderBytes);
   f.write_out = true;
   f.out_ids = out_ids;
   f.out_max = out_max;
-  cudaError_t e = launch_reduce(f, B, stream);
+  Problem p{h, W, B, d, V, 0, temp, nullptr, 0, seed, step};
+  cudaError_t e = V > 0 ? launch_tc_vocab(p, f, status_word, stream) : launch_reduce(f, B, stream);
   if (e != cudaSuccess) {
     cudaGetLastError();
-    return noalloc_fail(FS_ERR_CUDA, "reduction kernel launch failed");
+    return noalloc_fail(FS_ERR_CUDA, "kernel launch failed");
   }
   return FS_OK;
 }

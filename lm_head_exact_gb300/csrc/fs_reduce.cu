@@ -6,7 +6,9 @@
 //
 // Also holds the noise-inspection kernel that exposes the exact Philox words
 // and Gumbel values every sampling kernel uses, for parity tests.
+#include "fs_finish.cuh"
 #include "fs_internal.h"
+#include "fs_sm100.cuh"
 
 namespace fs {
 namespace {
@@ -29,25 +31,7 @@ reduce_kernel(Finish f, int64_t B) {
     best = combine(best, c);
   }
   best = warp_combine(best);
-  if (lane != 0) return;
-
-  if (f.carry_max != nullptr) {
-    if (f.carry_in) {
-      const int64_t cid = f.carry_ids[b];
-      if (cid >= 0) {
-        Best c;
-        c.z = f.carry_max[b];
-        c.id = static_cast<int32_t>(cid);
-        best = combine(best, c);
-      }
-    }
-    f.carry_max[b] = best.id == kNoId ? -INFINITY : best.z;
-    f.carry_ids[b] = best.id == kNoId ? -1 : static_cast<int64_t>(best.id);
-  }
-  if (f.write_out) {
-    f.out_ids[b] = best.id == kNoId ? -1 : static_cast<int64_t>(best.id);
-    f.out_max[b] = best.id == kNoId ? -INFINITY : best.z;
-  }
+  if (lane == 0) write_row(f, b, best);
 }
 
 __global__ void debug_noise_kernel(uint64_t seed, uint64_t step, int64_t row0, int64_t n_rows,
@@ -66,7 +50,28 @@ __global__ void debug_noise_kernel(uint64_t seed, uint64_t step, int64_t row0, i
   }
 }
 
+// Waits on an mbarrier that nothing ever arrives on, with a short limit: the
+// bounded wait must give up, flag the device error word and return, leaving
+// the context usable.  Exercises the failure path of the tensor-core kernels'
+// waits without faulting or hanging the GPU.
+__global__ void debug_wait_kernel(int* err, uint64_t timeout_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    sm100::mbar_init(&bar, 1);
+    abort_flag = 0;
+    sm100::fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) sm100::mbar_wait_ns(&bar, 0, err, &abort_flag, timeout_ns);
+}
+
 }  // namespace
+
+cudaError_t launch_debug_wait(int* err, uint64_t timeout_ns, cudaStream_t stream) {
+  debug_wait_kernel<<<1, 32, 0, stream>>>(err, timeout_ns);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_reduce(const Finish& f, int64_t B, cudaStream_t stream) {
   if (B == 0) return cudaSuccess;

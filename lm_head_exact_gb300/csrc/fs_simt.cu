@@ -9,10 +9,11 @@
 // that the block keeps in shared memory, and reduced across the warp.  Lanes
 // 0..BG-1 then own one batch row each: they scale by 1/T, add the row's
 // Philox-Gumbel draw and keep the running (max, argmax) in registers.  Each
-// block writes one candidate per batch row to the partial buffer; the
-// cross-part reduction kernel finishes the sample.
+// block pushes one candidate per batch row into the row's packed key and the
+// last block to finish writes the sample (fs_finish.cuh).
 #include <algorithm>
 
+#include "fs_finish.cuh"
 #include "fs_internal.h"
 
 namespace fs {
@@ -42,9 +43,11 @@ __device__ __forceinline__ float dot8(uint4 a, uint4 b, float acc) {
 
 template <int BG>
 __global__ void __launch_bounds__(kSimtThreads)
-simt_fused_kernel(Problem p, Partial* __restrict__ partials, int n_parts) {
+simt_fused_kernel(Problem p, Finish f) {
   extern __shared__ uint4 smem_h[];            // [BG][d/8] bf16x8 packets
   __shared__ Best warp_best[kSimtWarps][BG];
+  __shared__ int last_flag;
+  const int n_parts = gridDim.x;
 
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
@@ -128,12 +131,10 @@ simt_fused_kernel(Problem p, Partial* __restrict__ partials, int n_parts) {
       Best r = warp_best[0][threadIdx.x];
 #pragma unroll
       for (int w = 1; w < kSimtWarps; ++w) r = combine(r, warp_best[w][threadIdx.x]);
-      Partial out;
-      out.z = r.z;
-      out.id = r.id;
-      partials[(b0 + threadIdx.x) * n_parts + blockIdx.x] = out;
+      push_candidate(f, b0 + threadIdx.x, r);
     }
   }
+  finish_grid(f, p.B, threadIdx.x, kSimtThreads, &last_flag, [] { __syncthreads(); });
 }
 
 int pick_group(int64_t B, int64_t d) {
@@ -143,7 +144,7 @@ int pick_group(int64_t B, int64_t d) {
 }
 
 template <int BG>
-cudaError_t launch_group(const Problem& p, Partial* partials, int n_parts, cudaStream_t stream) {
+cudaError_t launch_group(const Problem& p, const Finish& f, int n_parts, cudaStream_t stream) {
   const size_t smem = static_cast<size_t>(BG) * p.d * 2;
   cudaError_t e = cudaFuncSetAttribute(simt_fused_kernel<BG>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -151,13 +152,13 @@ cudaError_t launch_group(const Problem& p, Partial* partials, int n_parts, cudaS
   if (e != cudaSuccess) return e;
   const int64_t groups = (p.B + BG - 1) / BG;
   dim3 grid(n_parts, static_cast<unsigned>(std::min<int64_t>(groups, 65535)));
-  simt_fused_kernel<BG><<<grid, kSimtThreads, smem, stream>>>(p, partials, n_parts);
+  simt_fused_kernel<BG><<<grid, kSimtThreads, smem, stream>>>(p, f);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-int simt_num_parts(const Problem& p, int device) {
+static int simt_num_parts(const Problem& p, int device) {
   int sms = 0;
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
   if (sms <= 0) sms = 148;
@@ -171,12 +172,15 @@ int simt_num_parts(const Problem& p, int device) {
   return static_cast<int>(parts);
 }
 
-cudaError_t launch_simt(const Problem& p, Partial* partials, int n_parts, cudaStream_t stream) {
+cudaError_t launch_simt(const Problem& p, const Finish& f, cudaStream_t stream) {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const int n_parts = simt_num_parts(p, dev);
   switch (pick_group(p.B, p.d)) {
-    case 1: return launch_group<1>(p, partials, n_parts, stream);
-    case 2: return launch_group<2>(p, partials, n_parts, stream);
-    case 4: return launch_group<4>(p, partials, n_parts, stream);
-    default: return launch_group<8>(p, partials, n_parts, stream);
+    case 1: return launch_group<1>(p, f, n_parts, stream);
+    case 2: return launch_group<2>(p, f, n_parts, stream);
+    case 4: return launch_group<4>(p, f, n_parts, stream);
+    default: return launch_group<8>(p, f, n_parts, stream);
   }
 }
 

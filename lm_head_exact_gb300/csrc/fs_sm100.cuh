@@ -60,11 +60,12 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 
 // Wait until the phase with the given parity has completed.  Gives up after
 // `timeout_ns` of wall time (or once another thread of the block raised
-// `*abort`), records kDevWaitTimeout in `*err` and returns false.
+// `*abort`), records the timeout (1) in the device error word `*err`, raises
+// `*abort` for the rest of the block and returns false.
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;  // 2 s: orders of magnitude above any legitimate wait
 
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err,
-                                          volatile int* abort) {
+__device__ __forceinline__ bool mbar_wait_ns(uint64_t* bar, uint32_t parity, int* err,
+                                             volatile int* abort, uint64_t timeout_ns) {
   const uint32_t a = smem_u32(bar);
   if (mbar_try_wait(a, parity)) return true;
   const uint64_t t0 = global_timer_ns();
@@ -72,13 +73,18 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* e
     if (mbar_try_wait(a, parity)) return true;
     if ((it & 63) == 63) {
       if (*abort) return false;
-      if (global_timer_ns() - t0 > kWaitTimeoutNs) {
+      if (global_timer_ns() - t0 > timeout_ns) {
         atomicExch(err, 1);
         *abort = 1;
         return false;
       }
     }
   }
+}
+
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err,
+                                          volatile int* abort) {
+  return mbar_wait_ns(bar, parity, err, abort, kWaitTimeoutNs);
 }
 
 // ------------------------------------------------------------------ TMA

@@ -1,5 +1,6 @@
 // Tensor-core fused LM-head sampler, batch-major: the large-batch path
-// (B > 256), where the contraction, not the W stream, bounds the step.
+// (B > 64 by default): W tiles are shared by the batch tiles of a CTA group
+// through L2, and from B ~ 300 on the contraction bounds the step.
 //
 // FlashSampling: Fast and Memory-Efficient Exact Sampling -- summary page,
 // "Method": the logit tile is formed on chip, Gumbel noise is added in-tile,
@@ -18,7 +19,8 @@
 //     nbt CTAs of a group read the same W tile at the same time, so W comes
 //     from HBM once per group and from L2 for the others, and every epilogue
 //     thread keeps ITS batch row's running (max, argmax) in registers across
-//     all of the CTA's tiles: one candidate per (row, group) at the end.
+//     all of the CTA's tiles and pushes one candidate per (row, CTA) at the
+//     end; the last CTA to finish writes the sample (fs_finish.cuh).
 //   * Warp roles (320 threads): warps 0-7 epilogue (TMEM lane = batch row;
 //     warps w and w + 4 share lanes and split the 256 columns in halves),
 //     warp 8 TMA producer, warp 9 TMEM allocator + MMA issuer.
@@ -28,6 +30,7 @@
 
 #include <algorithm>
 
+#include "fs_finish.cuh"
 #include "fs_internal.h"
 #include "fs_sm100.cuh"
 #include "fs_tmap.h"
@@ -58,13 +61,17 @@ constexpr int kSmemBytes = kOffHalf + kBM * 8 + 1024;
 
 struct BatchArgs {
   Problem p;            // rows [0, p.B) of this launch's batch slice
-  Partial* partials;    // row b's candidates at partials[b * n_groups + q], q < n_groups
+  float* logits;        // store-logits mode: [B_slice, V_local] fp32 (row stride V_local)
+  Finish f;             // sampling mode: cross-CTA finish of this slice's rows
   int nbt;              // batch tiles of this launch
-  int n_groups;         // CTA groups = gridDim.x / nbt (= candidates per row)
+  int n_groups;         // CTA groups = gridDim.x / nbt
   int n_vt;             // vocabulary tiles = ceil(V_local / 256)
   int* err;
 };
 
+// kStoreLogits = false: fused sampling epilogue.  true: the unfused
+// comparison path's plain GEMM epilogue, storing logits (+ bias) to HBM.
+template <bool kStoreLogits>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_batch_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_constant__ CUtensorMap tmap_w,
                 const BatchArgs args) {
@@ -77,6 +84,7 @@ tc_batch_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_constan
   uint64_t* drain_bar = tempty_bar + 2;
   uint32_t* tmem_base_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
+  int* last_flag = reinterpret_cast<int*>(smem + kOffMisc + 8);
   Best* half_best = reinterpret_cast<Best*>(smem + kOffHalf);
 
   const Problem& p = args.p;
@@ -203,7 +211,19 @@ tc_batch_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_constan
         tmem_ld_32(tmem_base + lane_addr + acc * kBN + half * (kBN / 2) + c, r);
         tmem_ld_wait();
         const int64_t v0 = col0 + c;                       // local id of r[0]
-        if (active && v0 < p.V_local) {
+        if constexpr (kStoreLogits) {
+          if (row_ok && v0 < p.V_local) {
+            float* dst = args.logits + b * p.V_local + v0;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              if (v0 + j < p.V_local) {
+                float logit = __uint_as_float(r[j]);
+                if (p.bias != nullptr) logit += p.bias[b * p.bias_stride + v0 + j];
+                dst[j] = logit;
+              }
+            }
+          }
+        } else if (active && v0 < p.V_local) {
           const int64_t vg0 = p.v_offset + v0;
           uint4 w = make_uint4(0, 0, 0, 0);
 #pragma unroll
@@ -228,12 +248,10 @@ tc_batch_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_constan
     // combine the two column halves of each row, then one candidate per (row, group)
     if (half == 1) half_best[row_in_tile] = best;
     asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
-    if (half == 0 && row_ok) {
-      best = combine(best, half_best[row_in_tile]);
-      Partial out;
-      out.z = best.z;
-      out.id = best.id;
-      args.partials[b * args.n_groups + q] = out;
+    if constexpr (!kStoreLogits) {
+      if (half == 0 && row_ok) push_candidate(args.f, b, combine(best, half_best[row_in_tile]));
+      finish_grid(args.f, p.B, threadIdx.x, kEpiWarps * 32, last_flag,
+                  [] { asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory"); });
     }
   }
 
@@ -265,24 +283,16 @@ int64_t tc_batch_max_rows_per_launch(int device) {
   return static_cast<int64_t>(sms) * kBM;
 }
 
-int tc_batch_num_parts(const Problem& p, int device) {
-  int sms = 0;
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
-  if (sms <= 0) sms = 148;
-  const int64_t slice = tc_batch_max_rows_per_launch(device);
-  // every launch slice writes its rows' candidates at the same stride
-  const int64_t first = std::min<int64_t>(p.B, slice);
-  return batch_geometry(first, sms).n_groups;
-}
-
-cudaError_t launch_tc_batch(const Problem& p, Partial* partials, int n_parts, int* err,
-                            cudaStream_t stream) {
-  if (p.d < kBK) return cudaErrorNotSupported;
+static cudaError_t launch_batch_impl(const Problem& p, const Finish* f, float* logits, int* err,
+                                     cudaStream_t stream) {
+  if (p.d < kBK || p.V_local <= 0) return cudaErrorNotSupported;
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (sms <= 0) sms = 148;
-  cudaError_t e = cudaFuncSetAttribute(tc_batch_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  const bool store = logits != nullptr;
+  cudaError_t e = store ? cudaFuncSetAttribute(tc_batch_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes)
+                        : cudaFuncSetAttribute(tc_batch_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   CUtensorMap tw;
   if (!encode_kmajor_bf16(&tw, p.W, p.V_local, p.d, kBK, kBN)) return cudaErrorInvalidValue;
@@ -293,19 +303,40 @@ cudaError_t launch_tc_batch(const Problem& p, Partial* partials, int n_parts, in
     ps.h = static_cast<const uint16_t*>(p.h) + b0 * p.d;
     ps.temp = p.temp + b0;
     if (p.bias != nullptr) ps.bias = p.bias + b0 * p.bias_stride;
-    // Every slice uses n_parts groups so all rows share the candidate stride;
-    // a later (shorter) slice has at least as many groups available.
+    Finish fs_slice{};
+    if (!store) {            // this launch finishes rows [b0, b0 + ps.B)
+      fs_slice = *f;
+      fs_slice.keys = f->keys + b0;
+      if (f->carry_max != nullptr) {
+        fs_slice.carry_max = f->carry_max + b0;
+        fs_slice.carry_ids = f->carry_ids + b0;
+      }
+      if (f->write_out) {
+        fs_slice.out_ids = f->out_ids + b0;
+        fs_slice.out_max = f->out_max + b0;
+      }
+    }
     const BatchGeometry g = batch_geometry(ps.B, sms);
-    if (g.n_groups < n_parts) return cudaErrorInvalidValue;
     CUtensorMap th;
     if (!encode_kmajor_bf16(&th, ps.h, ps.B, p.d, kBK, kBM)) return cudaErrorInvalidValue;
-    BatchArgs a{ps, partials + b0 * n_parts, g.nbt, n_parts,
+    BatchArgs a{ps, store ? logits + b0 * p.V_local : nullptr, fs_slice, g.nbt, g.n_groups,
                 static_cast<int>((p.V_local + kBN - 1) / kBN), err};
-    tc_batch_kernel<<<n_parts * g.nbt, kThreads, kSmemBytes, stream>>>(th, tw, a);
+    if (store)
+      tc_batch_kernel<true><<<g.grid, kThreads, kSmemBytes, stream>>>(th, tw, a);
+    else
+      tc_batch_kernel<false><<<g.grid, kThreads, kSmemBytes, stream>>>(th, tw, a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
+}
+
+cudaError_t launch_tc_batch(const Problem& p, const Finish& f, int* err, cudaStream_t stream) {
+  return launch_batch_impl(p, &f, nullptr, err, stream);
+}
+
+cudaError_t launch_tc_logits(const Problem& p, float* logits, int* err, cudaStream_t stream) {
+  return launch_batch_impl(p, nullptr, logits, err, stream);
 }
 
 }  // namespace fs

@@ -17,15 +17,18 @@
 //     through a STAGES-deep shared-memory ring guarded by mbarriers.
 //   * Warp roles (192 threads): warps 0-3 epilogue (TMEM lane = vocabulary
 //     row), warp 4 TMA producer, warp 5 TMEM allocator + MMA issuer.
-//   * Epilogue: per batch column, z = logit * (1/T) + Gumbel(Philox), then a
-//     warp-shuffle (max, argmax) across the 32 rows of the warp; the running
-//     best per (warp, column) lives in shared memory until the CTA's range is
-//     done, when the 4 warps are combined into one candidate per (row, CTA).
+//   * Epilogue: each warp transposes its 32 rows x 32 accumulator columns
+//     through shared memory; lane j then scans batch column j over the rows in
+//     increasing id order: z = logit * (1/T) + Gumbel(Philox), one Philox call
+//     per four consecutive ids, running (max, argmax) in registers for the
+//     whole CTA range; at the end the 4 warps are combined into one candidate
+//     per (batch row, CTA).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
 #include <algorithm>
 
+#include "fs_finish.cuh"
 #include "fs_internal.h"
 #include "fs_sm100.cuh"
 #include "fs_tmap.h"
@@ -49,24 +52,29 @@ template <int BN>
 struct VocabCfg {
   static constexpr int kBTileBytes = BN * kBK * 2;
   static constexpr int kStageBytes = kATileBytes + kBTileBytes;
-  static constexpr int kStages = std::min(12, (188 * 1024) / kStageBytes);
+  static constexpr int kChunk = BN < 32 ? BN : 32;     // accumulator columns per transpose step
+  static constexpr int kChunks = BN / kChunk;
   static constexpr int kTmemCols = (2 * BN < 32) ? 32 : 2 * BN;     // two accumulators
+  // everything but the stage ring: barriers (<= 29), tmem base / flags,
+  // per-column 1/T and mode, per-warp bests, transpose tiles, alignment slack
+  static constexpr int kFixedBytes = 29 * 8 + 16 + BN * 8 + kEpiWarps * BN * 8 + kEpiWarps * 32 * 33 * 4 + 1024;
+  static constexpr int kStages = std::min(12, (225 * 1024 - kFixedBytes) / kStageBytes);
   // shared memory carve-up (offsets from a 1024-byte aligned base)
   static constexpr int kOffA = 0;
   static constexpr int kOffB = kOffA + kStages * kATileBytes;
   static constexpr int kOffBars = kOffB + kStages * kBTileBytes;
   static constexpr int kNumBars = 2 * kStages + 5;
-  static constexpr int kOffMisc = kOffBars + kNumBars * 8;            // tmem base, abort flag
+  static constexpr int kOffMisc = kOffBars + kNumBars * 8;            // tmem base, abort flag, last-CTA flag
   static constexpr int kOffInvT = kOffMisc + 16;
   static constexpr int kOffMode = kOffInvT + BN * 4;
   static constexpr int kOffBest = kOffMode + BN * 4;
-  static constexpr int kSmemBytes = kOffBest + kEpiWarps * BN * 8 + 1024;   // + alignment slack
+  static constexpr int kOffTr = kOffBest + kEpiWarps * BN * 8;     // per-warp 32 x 33 transpose tiles
+  static constexpr int kSmemBytes = kOffTr + kEpiWarps * 32 * 33 * 4 + 1024;   // + alignment slack
 };
 
 struct VocabArgs {
   Problem p;
-  Partial* partials;
-  int n_parts;        // = gridDim.x: one candidate per (row, CTA)
+  Finish f;           // cross-CTA finish: packed keys, ticket, carry, outputs
   int64_t units;      // ceil(V_local / 32)
   int* err;
 };
@@ -85,9 +93,11 @@ tc_vocab_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
   uint64_t* drain_bar = tempty_bar + 2;             // abort path only
   uint32_t* tmem_base_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
+  int* last_flag = reinterpret_cast<int*>(smem + C::kOffMisc + 8);
   float* col_inv_t = reinterpret_cast<float*>(smem + C::kOffInvT);
   int* col_mode = reinterpret_cast<int*>(smem + C::kOffMode);
   Best* warp_best = reinterpret_cast<Best*>(smem + C::kOffBest);   // [kEpiWarps][BN]
+  float* tr_all = reinterpret_cast<float*>(smem + C::kOffTr);       // [kEpiWarps][32][33]
 
   const Problem& p = args.p;
   const int warp = threadIdx.x >> 5;
@@ -207,67 +217,94 @@ tc_vocab_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
     }
   } else {
     // ---------------------------------------------------------------- epilogue (warps 0-3)
+    // Each warp owns 32 vocabulary rows (its TMEM lane quadrant).  Per chunk
+    // of accumulator columns it transposes the 32 x chunk block through
+    // shared memory so that lane j then owns batch column c0 + j and scans the
+    // 32 rows in increasing id order: consecutive ids share one Philox call
+    // and the running (max, argmax) of (warp, column) stays in registers
+    // across all of the CTA's tiles -- no cross-lane reduction per tile.
     const PhiloxKey key{static_cast<uint32_t>(p.seed), static_cast<uint32_t>(p.seed >> 32)};
     const uint32_t step_lo = static_cast<uint32_t>(p.step);
     const uint32_t step_hi = static_cast<uint32_t>(p.step >> 32);
-    const int t_row = warp * 32 + lane;                       // TMEM lane = row within the tile
     const uint32_t lane_addr = static_cast<uint32_t>(warp * 32) << 16;
-    const int n_col = (B + 15) & ~15;
-    Best* my_best = warp_best + warp * BN;
+    float* tr = tr_all + warp * 32 * 33;
+    float best_z[C::kChunks];
+    int32_t best_id[C::kChunks];
+#pragma unroll
+    for (int c = 0; c < C::kChunks; ++c) {
+      best_z[c] = -INFINITY;
+      best_id[c] = kNoId;
+    }
     for (int t = 0; t < n_tiles; ++t) {
       const int acc = t & 1;
       const uint32_t acc_phase = (t >> 1) & 1;
       if (!mbar_wait(&tfull_bar[acc], acc_phase, args.err, abort_flag)) break;
       tc_fence_after();
-      const int64_t row = r0 + static_cast<int64_t>(t) * kBM;
-      const bool valid = row + t_row < r1;
-      const int64_t v_local = row + t_row;
-      const int64_t vg = p.v_offset + v_local;
-      const uint32_t vq = static_cast<uint32_t>(vg >> 2);
-      const uint32_t vj = static_cast<uint32_t>(vg & 3);
-      for (int c0 = 0; c0 < n_col; c0 += 16) {
-        uint32_t r[16];
-        tmem_ld_16(tmem_base + lane_addr + acc * BN + c0, r);
-        tmem_ld_wait();
+      const int64_t row0 = r0 + static_cast<int64_t>(t) * kBM + warp * 32;   // this warp's first row
+      const int n_rows = static_cast<int>(std::max<int64_t>(0, std::min<int64_t>(32, r1 - row0)));
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int b = c0 + j;
-          if (b < B) {                                          // warp-uniform
-            const int mode = col_mode[b];
-            float z = -INFINITY;
-            if (valid && mode != kRowInvalid) {
-              float logit = __uint_as_float(r[j]);
-              if (p.bias != nullptr) logit += p.bias[static_cast<int64_t>(b) * p.bias_stride + v_local];
-              if (mode == kRowSample) {
-                const uint4 w = noise_words(key, vq, static_cast<uint32_t>(b), step_lo, step_hi);
-                z = fmaf(logit, col_inv_t[b], gumbel_from_word(word_of(w, vj)));
-              } else {
-                z = logit;
+      for (int c = 0; c < C::kChunks; ++c) {
+        const int c0 = c * C::kChunk;
+        if (c0 < B) {                                                 // warp-uniform
+          uint32_t r[C::kChunk];
+          if constexpr (C::kChunk == 32) {
+            tmem_ld_32(tmem_base + lane_addr + acc * BN + c0, r);
+          } else {
+            tmem_ld_16(tmem_base + lane_addr + acc * BN + c0, r);
+          }
+          tmem_ld_wait();
+          __syncwarp();
+#pragma unroll
+          for (int j = 0; j < C::kChunk; ++j) tr[j * 33 + lane] = __uint_as_float(r[j]);
+          __syncwarp();
+          const int b = c0 + lane;
+          const int mode = (lane < C::kChunk && b < B) ? col_mode[b] : kRowInvalid;
+          if (mode != kRowInvalid) {
+            const float inv_t = col_inv_t[b];
+            const float* col = tr + lane * 33;
+            const float* bias_row = p.bias != nullptr ? p.bias + static_cast<int64_t>(b) * p.bias_stride : nullptr;
+            uint4 w = make_uint4(0, 0, 0, 0);
+            for (int i = 0; i < n_rows; ++i) {
+              const int64_t v_local = row0 + i;
+              const int64_t vg = p.v_offset + v_local;
+              if (i == 0 || (vg & 3) == 0)
+                w = noise_words(key, static_cast<uint32_t>(vg >> 2), static_cast<uint32_t>(b), step_lo, step_hi);
+              float logit = col[i];
+              if (bias_row != nullptr) logit += __ldg(bias_row + v_local);
+              const float z = mode == kRowGreedy
+                                  ? logit
+                                  : fmaf(logit, inv_t, gumbel_from_word(word_of(w, static_cast<uint32_t>(vg & 3))));
+              if (z > best_z[c]) {      // ids rise: strict > keeps the smaller id on ties
+                best_z[c] = z;
+                best_id[c] = static_cast<int32_t>(vg);
               }
-              if (!(z > -INFINITY)) z = -INFINITY;              // NaN never wins
             }
-            Best c;
-            c.z = z;
-            c.id = z > -INFINITY ? static_cast<int32_t>(vg) : kNoId;
-            c = warp_combine(c);
-            if (lane == 0) my_best[b] = combine(my_best[b], c);
           }
         }
       }
       tc_fence_before();
       mbar_arrive(&tempty_bar[acc]);
     }
-    // combine the 4 epilogue warps: one candidate per (batch row, CTA)
+#pragma unroll
+    for (int c = 0; c < C::kChunks; ++c) {
+      const int b = c * C::kChunk + lane;
+      if (lane < C::kChunk && b < B) {
+        Best bb;
+        bb.z = best_z[c];
+        bb.id = best_id[c];
+        warp_best[warp * BN + b] = bb;
+      }
+    }
+    // combine the 4 epilogue warps, push one candidate per (batch row, CTA)
     asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
     for (int b = threadIdx.x; b < B; b += kEpiWarps * 32) {
       Best r = warp_best[b];
 #pragma unroll
       for (int w = 1; w < kEpiWarps; ++w) r = combine(r, warp_best[w * BN + b]);
-      Partial out;
-      out.z = r.z;
-      out.id = r.id;
-      args.partials[static_cast<int64_t>(b) * args.n_parts + blockIdx.x] = out;
+      push_candidate(args.f, b, r);
     }
+    finish_grid(args.f, B, threadIdx.x, kEpiWarps * 32, last_flag,
+                [] { asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory"); });
   }
 
   // ---- teardown
@@ -279,7 +316,7 @@ tc_vocab_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
 
 // ------------------------------------------------------------------ host side
 template <int BN>
-cudaError_t launch_bn(const Problem& p, Partial* partials, int n_parts, int* err, cudaStream_t stream) {
+cudaError_t launch_bn(const Problem& p, const Finish& f, int* err, cudaStream_t stream) {
   using C = VocabCfg<BN>;
   static_assert(C::kStages >= 2, "pipeline needs at least two stages");
   static_assert(C::kSmemBytes <= 227 * 1024, "shared memory budget");
@@ -289,8 +326,14 @@ cudaError_t launch_bn(const Problem& p, Partial* partials, int n_parts, int* err
   cudaError_t e = cudaFuncSetAttribute(tc_vocab_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::kSmemBytes);
   if (e != cudaSuccess) return e;
-  VocabArgs a{p, partials, n_parts, (p.V_local + kUnitRows - 1) / kUnitRows, err};
-  tc_vocab_kernel<BN><<<n_parts, kThreads, C::kSmemBytes, stream>>>(tw, th, a);
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (sms <= 0) sms = 148;
+  const int64_t units = (p.V_local + kUnitRows - 1) / kUnitRows;
+  const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(sms, units)));
+  VocabArgs a{p, f, units, err};
+  tc_vocab_kernel<BN><<<grid, kThreads, C::kSmemBytes, stream>>>(tw, th, a);
   return cudaGetLastError();
 }
 
@@ -300,23 +343,14 @@ int tc_vocab_bn(int64_t B) {
   return B <= 16 ? 16 : B <= 32 ? 32 : B <= 64 ? 64 : B <= 128 ? 128 : 256;
 }
 
-int tc_vocab_num_parts(const Problem& p, int device) {
-  int sms = 0;
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
-  if (sms <= 0) sms = 148;
-  const int64_t units = (p.V_local + kUnitRows - 1) / kUnitRows;
-  return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(sms, units)));
-}
-
-cudaError_t launch_tc_vocab(const Problem& p, Partial* partials, int n_parts, int* err,
-                            cudaStream_t stream) {
-  if (p.B > 256 || p.d < kBK) return cudaErrorNotSupported;
+cudaError_t launch_tc_vocab(const Problem& p, const Finish& f, int* err, cudaStream_t stream) {
+  if (p.B > 256 || p.d < kBK || p.V_local <= 0) return cudaErrorNotSupported;
   switch (tc_vocab_bn(p.B)) {
-    case 16: return launch_bn<16>(p, partials, n_parts, err, stream);
-    case 32: return launch_bn<32>(p, partials, n_parts, err, stream);
-    case 64: return launch_bn<64>(p, partials, n_parts, err, stream);
-    case 128: return launch_bn<128>(p, partials, n_parts, err, stream);
-    default: return launch_bn<256>(p, partials, n_parts, err, stream);
+    case 16: return launch_bn<16>(p, f, err, stream);
+    case 32: return launch_bn<32>(p, f, err, stream);
+    case 64: return launch_bn<64>(p, f, err, stream);
+    case 128: return launch_bn<128>(p, f, err, stream);
+    default: return launch_bn<256>(p, f, err, stream);
   }
 }
 

@@ -252,3 +252,68 @@ def test_paths_agree_on_llama3_8b_head(fs, torch_cuda):
 
 def test_device_error_word_is_clear(fs, torch_cuda):
     assert fs.device_error() == 0
+
+
+# ------------------------------------------------------------------ unfused comparison path
+@pytest.mark.parametrize("B,V,d", [(4, 4096, 256), (37, 4097, 512), (300, 3001, 256)])
+def test_unfused_logits_and_ids(fs, torch_cuda, B, V, d):
+    """The unfused pipeline's HBM logits against the oracle's fp64 logits
+    (|delta| <= 2e-3), and its ids / maxima against the oracle (same rule as
+    the fused path) and the fused path."""
+    torch = torch_cuda
+    h, W, temp = _problem(B, V, d, seed=B + V)
+    rng = np.random.default_rng(B)
+    bias = np.zeros((B, V), np.float32)
+    bias[np.arange(B)[:, None], rng.integers(0, V, size=(B, 4))] = 3.0
+    hd, Wd, td, bd = (to_device(h, torch), to_device(W, torch), to_device(temp, torch),
+                      to_device(bias, torch))
+    logits = torch.empty((B, V), dtype=torch.float32, device="cuda")
+    ids, mx = fs.sample_unfused(hd, Wd, td, 99, 5, bias=bd, logits_out=logits)
+    fids, fmx = fs.sample(hd, Wd, td, 99, 5, bias=bd)
+    torch.cuda.synchronize()
+    ell = sampler.logits(h, W, bias)
+    assert np.abs(logits.cpu().numpy().astype(np.float64) - ell).max() <= 2e-3
+    ref = sampler.sample(h, W, temp, 99, 5, bias=bias)
+    compare(ids.cpu().numpy(), mx.cpu().numpy(), ref, what="unfused")
+    compare(fids.cpu().numpy(), fmx.cpu().numpy(), ref, what="fused")
+
+
+def test_unfused_on_llama3_8b_head(fs, torch_cuda):
+    torch = torch_cuda
+    wl = synthetic.workload("llama3_8b", 16)
+    hd, Wd, td = to_device(wl.h, torch), to_device(wl.W, torch), to_device(wl.temp, torch)
+    logits = torch.empty((16, wl.V), dtype=torch.float32, device="cuda")
+    ids, mx = fs.sample_unfused(hd, Wd, td, wl.seed, 7, logits_out=logits)
+    torch.cuda.synchronize()
+    rows = np.array([0, 5, 15])
+    ell = sampler.logits(wl.h[rows], wl.W)
+    assert np.abs(logits.cpu().numpy()[rows].astype(np.float64) - ell).max() <= 2e-3
+    ref = sampler.sample(wl.h, wl.W, wl.temp, wl.seed, 7)
+    compare(ids.cpu().numpy(), mx.cpu().numpy(), ref, what="unfused 8B")
+
+
+def test_bounded_wait_times_out_and_reports(fs, torch_cuda):
+    """A wait that nobody satisfies gives up after its limit, flags the device
+    error word, and leaves the context usable."""
+    torch = torch_cuda
+    assert fs.device_error() == 0
+    fs.debug_wait_timeout(20_000_000)                 # 20 ms
+    torch.cuda.synchronize()
+    assert fs.device_error() == 1
+    assert fs.device_error() == 0                     # read clears it
+    wl = synthetic.tiny()
+    ids, mx = _run(fs, torch, wl.h, wl.W, wl.temp, wl.seed, 0)
+    compare(ids, mx, sampler.sample(wl.h, wl.W, wl.temp, wl.seed, 0), what="after timeout")
+
+
+def test_back_to_back_calls_of_different_batch_sizes(fs, torch_cuda, path):
+    """The in-kernel finish leaves its ticket and keys at zero: calls with
+    shrinking and growing batches on one stream stay exact."""
+    torch = torch_cuda
+    h, W, temp = _problem(300, 2000, 128, seed=31)
+    hd, Wd, td = to_device(h, torch), to_device(W, torch), to_device(temp, torch)
+    for B in (300, 7, 64, 1, 300):
+        ids, mx = fs.sample(hd[:B], Wd, td[:B], 3, B)
+        torch.cuda.synchronize()
+        compare(ids.cpu().numpy(), mx.cpu().numpy(), sampler.sample(h[:B], W, temp[:B], 3, B),
+                what=f"B={B}")

@@ -215,10 +215,12 @@ constexpr int64_t kVocabMajorMaxBatch = 64;
 
 int resolve_path(int64_t B, int64_t d) {
   int path = g_forced_path.load();
-  // Measured on GB300 (Llama-3-8B head): vocabulary-major streams W fastest
+  // Measured on GB300 (Llama-3-8B head): for one row the CUDA-core kernel
+  // streams W fastest (96% of the copy bandwidth); vocabulary-major is best
   // up to B = 64; from B = 96 the batch-major kernel, whose W tiles are
   // shared by the batch tiles of a CTA group through L2, is faster.
-  if (path == kPathAuto) path = (B <= kVocabMajorMaxBatch) ? kPathTcVocab : kPathTcBatch;
+  if (path == kPathAuto)
+    path = B == 1 ? kPathSimt : (B <= kVocabMajorMaxBatch) ? kPathTcVocab : kPathTcBatch;
   if (path == kPathTcVocab && B > 256) path = kPathTcBatch;
   if ((path == kPathTcVocab || path == kPathTcBatch) && d < 64) path = kPathSimt;
   return path;

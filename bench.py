@@ -50,6 +50,40 @@ def algorithmic_flops(B, d, V):
     return 2 * B * d * V
 
 
+# Sources that determine each fused kernel's code; the recorded ncu traffic of
+# a kernel (profiles/traffic.json) is only reported while their hash matches.
+_CSRC = os.path.join(ROOT, "lm_head_exact_gb300", "csrc")
+_SHARED = ["fs_device.cuh", "fs_sm100.cuh", "fs_finish.cuh", "fs_internal.h", "fs_tmap.cu", "fs_tmap.h"]
+KERNEL_SOURCES = {
+    "tc_vocab_kernel": ["fs_tc_vocab.cu"] + _SHARED,
+    "tc_batch_kernel": ["fs_tc_batch.cu"] + _SHARED,
+    "simt_fused_kernel": ["fs_simt.cu"] + _SHARED,
+}
+PATH_KERNEL = {1: "simt_fused_kernel", 2: "tc_vocab_kernel", 3: "tc_batch_kernel"}
+
+
+def kernel_source_hash(kernel):
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(_CSRC, f), "rb") as fh:
+            h.update(f.encode() + b"\0" + fh.read())
+    return h.hexdigest()
+
+
+def recorded_traffic(kernel, workload):
+    """DRAM bytes per launch from the committed ncu capture of `kernel` on
+    `workload`, or None if there is none or the kernel's sources changed."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            entry = json.load(f).get(f"{kernel}@{workload}")
+    except (OSError, ValueError):
+        return None
+    if not entry or entry.get("source_sha256") != kernel_source_hash(kernel):
+        return None
+    return entry["dram_bytes_per_launch"]
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -337,7 +371,8 @@ def run_ours(args):
     if rank == 0:
         us = step_ms * 1e3
         rf = roofline(B, d, V, kern_ms * 1e3, peaks)
-        rf["traffic"] = None
+        rf["kernel"] = PATH_KERNEL.get(fs.path_for_batch(B))
+        rf["traffic"] = recorded_traffic(rf["kernel"], f"llama3_8b_B{B}")
         rf["kernel_us"] = round(kern_ms * 1e3, 2)
         result = {
             "metric": METRIC, "value": round(us, 2), "unit": UNIT, "higher_is_better": False,

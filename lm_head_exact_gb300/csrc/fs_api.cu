@@ -11,7 +11,7 @@
 #include <mutex>
 #include <utility>
 
-#include "../../include/flashsample.h"
+#include "flashsample.h"
 #include "fs_internal.h"
 
 namespace fs {

@@ -32,7 +32,7 @@
 #include <cstdint>
 #include <mutex>
 
-#include "../../include/flashsample.h"
+#include "flashsample.h"
 #include "fs_internal.h"
 
 namespace fs {

@@ -7,8 +7,10 @@
 // only one maximizer per row and per vocabulary tile".
 //
 // Mapping on GB300 (sm_103a):
-//   * One persistent CTA per SM owns a contiguous range of vocabulary rows
-//     (boundaries on 32-row units, so the ranges differ by at most 32 rows).
+//   * One persistent CTA per SM takes the 128-row vocabulary tiles c, c + G,
+//     c + 2G, ... (G = grid size): every tile is one 128-row TMA box of W per
+//     K step (measured faster on GB300 than contiguous per-CTA ranges loaded
+//     as 32-row boxes: 173 vs 178 us for the Llama-3-8B head at B = 16).
 //   * MMA: D[v, b] = sum_k W[v, k] * h[b, k] with tcgen05.mma kind::f16,
 //     M = 128 vocabulary rows (A = W tile), N = BN batch rows (B = h tile),
 //     K = 64 per pipeline stage; fp32 accumulators in TMEM, double-buffered
@@ -44,9 +46,7 @@ constexpr int kProducerWarp = 4;
 constexpr int kMmaWarp = 5;
 constexpr int kBM = 128;          // vocabulary rows per tile (MMA M)
 constexpr int kBK = 64;           // K per stage: one 128-byte swizzle row of bf16
-constexpr int kUnitRows = 32;     // granularity of the per-CTA vocabulary ranges (one TMA box)
 constexpr int kATileBytes = kBM * kBK * 2;
-constexpr int kBoxBytes = kUnitRows * kBK * 2;
 
 template <int BN>
 struct VocabCfg {
@@ -75,7 +75,7 @@ struct VocabCfg {
 struct VocabArgs {
   Problem p;
   Finish f;           // cross-CTA finish: packed keys, ticket, carry, outputs
-  int64_t units;      // ceil(V_local / 32)
+  int64_t n_vt;       // vocabulary tiles: ceil(V_local / 128)
   int* err;
 };
 
@@ -104,12 +104,9 @@ tc_vocab_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
   const int lane = threadIdx.x & 31;
   const int B = static_cast<int>(p.B);
 
-  // This CTA's vocabulary rows [r0, r1) of the call's W.
-  const int64_t u0 = args.units * blockIdx.x / gridDim.x;
-  const int64_t u1 = args.units * (blockIdx.x + 1) / gridDim.x;
-  const int64_t r0 = u0 * kUnitRows;
-  const int64_t r1 = std::min<int64_t>(u1 * kUnitRows, p.V_local);
-  const int n_tiles = r1 > r0 ? static_cast<int>((r1 - r0 + kBM - 1) / kBM) : 0;
+  // This CTA's tiles: global tile blockIdx.x + t * gridDim.x, rows [128 g, 128 g + 128) of W.
+  const int n_tiles = blockIdx.x < args.n_vt ? static_cast<int>((args.n_vt - 1 - blockIdx.x) / gridDim.x + 1) : 0;
+  auto tile_row = [&](int t) { return (static_cast<int64_t>(blockIdx.x) + static_cast<int64_t>(t) * gridDim.x) * kBM; };
   const int n_kb = static_cast<int>((p.d + kBK - 1) / kBK);
 
   // ---- set-up
@@ -155,18 +152,15 @@ tc_vocab_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
       int64_t n_issued = 0;
       bool ok = true;
       for (int t = 0; t < n_tiles && ok; ++t) {
-        const int64_t row = r0 + static_cast<int64_t>(t) * kBM;
-        const int rows = static_cast<int>(std::min<int64_t>(kBM, r1 - row));
-        const int boxes = (rows + kUnitRows - 1) / kUnitRows;
-        const uint32_t bytes = boxes * kBoxBytes + C::kBTileBytes;
+        const int64_t row = tile_row(t);
+        // rows past V (last tile) are zero-filled and still count as transferred bytes
+        const uint32_t bytes = kATileBytes + C::kBTileBytes;
         for (int kb = 0; kb < n_kb; ++kb) {
           if (!mbar_wait(&empty_bar[stage], phase ^ 1, args.err, abort_flag)) { ok = false; break; }
           uint8_t* a_dst = smem + C::kOffA + stage * kATileBytes;
           uint8_t* b_dst = smem + C::kOffB + stage * C::kBTileBytes;
           mbar_arrive_expect_tx(&full_bar[stage], bytes);
-          for (int j = 0; j < boxes; ++j)
-            tma_load_2d(a_dst + j * kBoxBytes, &tmap_w, &full_bar[stage], kb * kBK,
-                        static_cast<int32_t>(row + j * kUnitRows), pol_w);
+          tma_load_2d(a_dst, &tmap_w, &full_bar[stage], kb * kBK, static_cast<int32_t>(row), pol_w);
           tma_load_2d(b_dst, &tmap_h, &full_bar[stage], kb * kBK, 0, pol_h);
           ++n_issued;
           if (++stage == C::kStages) { stage = 0; phase ^= 1; }
@@ -240,8 +234,8 @@ tc_vocab_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
       const uint32_t acc_phase = (t >> 1) & 1;
       if (!mbar_wait(&tfull_bar[acc], acc_phase, args.err, abort_flag)) break;
       tc_fence_after();
-      const int64_t row0 = r0 + static_cast<int64_t>(t) * kBM + warp * 32;   // this warp's first row
-      const int n_rows = static_cast<int>(std::max<int64_t>(0, std::min<int64_t>(32, r1 - row0)));
+      const int64_t row0 = tile_row(t) + warp * 32;                     // this warp's first row
+      const int n_rows = static_cast<int>(std::max<int64_t>(0, std::min<int64_t>(32, p.V_local - row0)));
 #pragma unroll
       for (int c = 0; c < C::kChunks; ++c) {
         const int c0 = c * C::kChunk;
@@ -321,7 +315,7 @@ cudaError_t launch_bn(const Problem& p, const Finish& f, int* err, cudaStream_t 
   static_assert(C::kStages >= 2, "pipeline needs at least two stages");
   static_assert(C::kSmemBytes <= 227 * 1024, "shared memory budget");
   CUtensorMap tw, th;
-  if (!encode_kmajor_bf16(&tw, p.W, p.V_local, p.d, kBK, kUnitRows)) return cudaErrorInvalidValue;
+  if (!encode_kmajor_bf16(&tw, p.W, p.V_local, p.d, kBK, kBM)) return cudaErrorInvalidValue;
   if (!encode_kmajor_bf16(&th, p.h, p.B, p.d, kBK, BN)) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(tc_vocab_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::kSmemBytes);
@@ -330,9 +324,9 @@ cudaError_t launch_bn(const Problem& p, const Finish& f, int* err, cudaStream_t 
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (sms <= 0) sms = 148;
-  const int64_t units = (p.V_local + kUnitRows - 1) / kUnitRows;
-  const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(sms, units)));
-  VocabArgs a{p, f, units, err};
+  const int64_t n_vt = (p.V_local + kBM - 1) / kBM;
+  const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(sms, n_vt)));
+  VocabArgs a{p, f, n_vt, err};
   tc_vocab_kernel<BN><<<grid, kThreads, C::kSmemBytes, stream>>>(tw, th, a);
   return cudaGetLastError();
 }

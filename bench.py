@@ -58,8 +58,9 @@ KERNEL_SOURCES = {
     "tc_vocab_kernel": ["fs_tc_vocab.cu"] + _SHARED,
     "tc_batch_kernel": ["fs_tc_batch.cu"] + _SHARED,
     "simt_fused_kernel": ["fs_simt.cu"] + _SHARED,
+    "tc_pair_kernel": ["fs_tc_pair.cu"] + _SHARED,
 }
-PATH_KERNEL = {1: "simt_fused_kernel", 2: "tc_vocab_kernel", 3: "tc_batch_kernel"}
+PATH_KERNEL = {1: "simt_fused_kernel", 2: "tc_vocab_kernel", 3: "tc_batch_kernel", 4: "tc_pair_kernel"}
 
 
 def kernel_source_hash(kernel):

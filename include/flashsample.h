@@ -78,6 +78,7 @@ typedef enum fs_status {
 #define FS_PATH_SIMT 1        /* W-streaming CUDA-core path */
 #define FS_PATH_TC_VOCAB 2    /* tcgen05 tensor-core path, vocabulary rows on the MMA M axis */
 #define FS_PATH_TC_BATCH 3    /* tcgen05 tensor-core path, batch rows on the MMA M axis */
+#define FS_PATH_TC_PAIR 4     /* as FS_PATH_TC_BATCH, one MMA over a pair of CTAs (cta_group::2) */
 
 /*
  * One decode step of fused sampling (summary page, "Method"; arXiv abstract).

@@ -17,7 +17,7 @@ LIB_PATH = os.path.join(_PKG, "libflashsample.so")
 FS_OK = 0
 FS_CHUNK_FIRST = 1
 FS_CHUNK_LAST = 2
-FS_PATH_AUTO, FS_PATH_SIMT, FS_PATH_TC_VOCAB, FS_PATH_TC_BATCH = 0, 1, 2, 3
+FS_PATH_AUTO, FS_PATH_SIMT, FS_PATH_TC_VOCAB, FS_PATH_TC_BATCH, FS_PATH_TC_PAIR = 0, 1, 2, 3, 4
 
 _c_void_p = ctypes.c_void_p
 _i64 = ctypes.c_int64

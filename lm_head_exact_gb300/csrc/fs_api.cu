@@ -211,18 +211,26 @@ fs_status check_problem(const Problem& p, bool need_out, const void* out_ids, co
 // model width, identical for every chunk of a chunked run) only -- never from
 // V or the chunk range -- so one-shot and chunked runs compute every logit
 // with the same kernel and agree bit for bit.
-constexpr int64_t kVocabMajorMaxBatch = 64;
+constexpr int64_t kVocabMajorMaxBatch = 96;
+
+// Auto rule, measured on GB300 (Llama-3-8B head, fused kernel µs):
+//   B = 1: CUDA-core kernel (161 vs 168 vocabulary-major);
+//   B <= 96: vocabulary-major (W streaming, 166-181);
+//   larger B: the CTA-pair kernel when padding B to 256-row pair tiles wastes
+//   fewer than 128 rows (B = 256: 205 vs 217, B = 1024: 701 vs 729), otherwise
+//   the single-CTA batch-major kernel (B = 128: 185 vs 193, B = 384: 307 vs 344).
+int auto_path(int64_t B) {
+  if (B == 1) return kPathSimt;
+  if (B <= kVocabMajorMaxBatch) return kPathTcVocab;
+  const int64_t padded = (B + 255) / 256 * 256;
+  return (B > 128 && padded - B < 128) ? kPathTcPair : kPathTcBatch;
+}
 
 int resolve_path(int64_t B, int64_t d) {
   int path = g_forced_path.load();
-  // Measured on GB300 (Llama-3-8B head): for one row the CUDA-core kernel
-  // streams W fastest (96% of the copy bandwidth); vocabulary-major is best
-  // up to B = 64; from B = 96 the batch-major kernel, whose W tiles are
-  // shared by the batch tiles of a CTA group through L2, is faster.
-  if (path == kPathAuto)
-    path = B == 1 ? kPathSimt : (B <= kVocabMajorMaxBatch) ? kPathTcVocab : kPathTcBatch;
+  if (path == kPathAuto) path = auto_path(B);
   if (path == kPathTcVocab && B > 256) path = kPathTcBatch;
-  if ((path == kPathTcVocab || path == kPathTcBatch) && d < 64) path = kPathSimt;
+  if ((path == kPathTcVocab || path == kPathTcBatch || path == kPathTcPair) && d < 64) path = kPathSimt;
   return path;
 }
 
@@ -251,6 +259,9 @@ fs_status run(const Problem& p, Finish f, cudaStream_t stream) {
       break;
     case kPathTcBatch:
       e = launch_tc_batch(p, f, err, stream);
+      break;
+    case kPathTcPair:
+      e = launch_tc_pair(p, f, err, stream);
       break;
     case kPathSimt:
     default:
@@ -445,7 +456,7 @@ fs_status fs_workspace_release(void) {
 }
 
 fs_status fs_set_path(int path) {
-  if (path < FS_PATH_AUTO || path > FS_PATH_TC_BATCH) return fail(FS_ERR_INVALID_ARG, "unknown path %d", path);
+  if (path < FS_PATH_AUTO || path > FS_PATH_TC_PAIR) return fail(FS_ERR_INVALID_ARG, "unknown path %d", path);
   g_forced_path.store(path);
   return FS_OK;
 }

@@ -46,7 +46,7 @@ struct Finish {
 };
 
 // Kernel families selectable by batch size (or forced for tests).
-enum Path : int { kPathAuto = 0, kPathSimt = 1, kPathTcVocab = 2, kPathTcBatch = 3 };
+enum Path : int { kPathAuto = 0, kPathSimt = 1, kPathTcVocab = 2, kPathTcBatch = 3, kPathTcPair = 4 };
 
 // Launchers: enqueue on `stream`; return cudaSuccess or the launch error.
 // Each fused kernel finishes the sample itself through `f` (one launch).
@@ -57,8 +57,12 @@ cudaError_t launch_simt(const Problem& p, const Finish& f, cudaStream_t stream);
 int tc_vocab_bn(int64_t B);
 cudaError_t launch_tc_vocab(const Problem& p, const Finish& f, int* err, cudaStream_t stream);
 
-// Tensor-core batch-major path (any B, d >= 64; auto-selected for B > 64).
+// Tensor-core batch-major path (any B, d >= 64).
 cudaError_t launch_tc_batch(const Problem& p, const Finish& f, int* err, cudaStream_t stream);
+
+// Tensor-core batch-major path over CTA pairs (tcgen05 cta_group::2; any B,
+// d >= 64).
+cudaError_t launch_tc_pair(const Problem& p, const Finish& f, int* err, cudaStream_t stream);
 
 // Unfused comparison pipeline: tensor-core GEMM storing fp32 logits [B, V]
 // (+ bias) to HBM, then row softmax into probs [B, V], then the sample.

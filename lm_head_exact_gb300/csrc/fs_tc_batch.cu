@@ -1,6 +1,8 @@
-// Tensor-core fused LM-head sampler, batch-major: the large-batch path
-// (B > 64 by default): W tiles are shared by the batch tiles of a CTA group
-// through L2, and from B ~ 300 on the contraction bounds the step.
+// Tensor-core fused LM-head sampler, batch-major, one CTA per MMA: used for
+// 96 < B <= 128 and for batches that do not fill 256-row CTA-pair tiles (the
+// pair kernel, fs_tc_pair.cu, takes the rest).  W tiles are shared by the
+// batch tiles of a CTA group through L2; from B ~ 300 on the contraction
+// bounds the step.
 //
 // FlashSampling: Fast and Memory-Efficient Exact Sampling -- summary page,
 // "Method": the logit tile is formed on chip, Gumbel noise is added in-tile,
@@ -30,6 +32,7 @@
 
 #include <algorithm>
 
+#include "fs_epilogue.cuh"
 #include "fs_finish.cuh"
 #include "fs_internal.h"
 #include "fs_sm100.cuh"
@@ -196,6 +199,14 @@ tc_batch_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_constan
     const uint32_t step_lo = static_cast<uint32_t>(p.step);
     const uint32_t step_hi = static_cast<uint32_t>(p.step >> 32);
     const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
+    RowScan scan;
+    scan.key = key;
+    scan.row = static_cast<uint32_t>(b);
+    scan.step_lo = step_lo;
+    scan.step_hi = step_hi;
+    scan.inv_t = rt.inv_t;
+    scan.greedy = greedy;
+    scan.bias_row = p.bias != nullptr ? p.bias + b * p.bias_stride : nullptr;
     Best best = best_none();
 
     for (int t = 0; t < n_tiles; ++t) {
@@ -224,22 +235,10 @@ tc_batch_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_constan
             }
           }
         } else if (active && v0 < p.V_local) {
-          const int64_t vg0 = p.v_offset + v0;
-          uint4 w = make_uint4(0, 0, 0, 0);
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int64_t vg = vg0 + j;
-            if (j == 0 || (vg & 3) == 0)
-              w = noise_words(key, static_cast<uint32_t>(vg >> 2), static_cast<uint32_t>(b), step_lo, step_hi);
-            float logit = __uint_as_float(r[j]);
-            if (p.bias != nullptr && v0 + j < p.V_local) logit += p.bias[b * p.bias_stride + v0 + j];
-            const float g = gumbel_from_word(word_of(w, static_cast<uint32_t>(vg & 3)));
-            const float z = greedy ? logit : fmaf(logit, rt.inv_t, g);
-            if (v0 + j < p.V_local && z > best.z) {   // ids rise: strict > keeps the smaller id
-              best.z = z;
-              best.id = static_cast<int32_t>(vg);
-            }
-          }
+          if (scan.bias_row != nullptr)
+            scan32<true>(r, v0, p.V_local, p.v_offset, scan, best);
+          else
+            scan32<false>(r, v0, p.V_local, p.v_offset, scan, best);
         }
       }
       tc_fence_before();

@@ -1,0 +1,287 @@
+// Tensor-core fused LM-head sampler, batch-major over CTA PAIRS: the
+// large-batch path in the contraction-bound regime.
+//
+// FlashSampling: Fast and Memory-Efficient Exact Sampling -- summary page,
+// "Method": the logit tile is formed on chip, Gumbel noise is added in-tile,
+// and only a per-row (max, argmax) survives; arXiv abstract: "keep only one
+// maximizer per row and per vocabulary tile, and finish with a small
+// reduction over tiles".
+//
+// Same tiling and epilogue as the single-CTA batch-major kernel, but each MMA
+// spans a cluster of two CTAs (tcgen05 cta_group::2): M = 256 batch rows
+// (128 per CTA, each CTA loads its own h rows) by N = 256 vocabulary rows
+// (each CTA loads HALF of the W tile, 128 rows), K = 64 per stage.  Per CTA a
+// stage is 32 KB instead of 48 KB, so six stages fit and each CTA moves a
+// third fewer bytes from L2 for the same MMA work.  The even CTA of the pair
+// issues the MMAs and commits them to both CTAs' barriers; each CTA's TMEM
+// holds the accumulators of its own 128 batch rows x 256 vocabulary rows, and
+// each CTA's epilogue releases the accumulator by arriving on the even CTA's
+// barrier.
+//
+// CTA grouping as in the single-CTA kernel: with npt = ceil(B / 256) pair
+// tiles, groups of npt pairs walk the vocabulary tiles q, q + n_groups, ...
+// in lockstep, so W comes from HBM once per group.
+#include <cuda.h>
+
+#include <algorithm>
+
+#include "fs_epilogue.cuh"
+#include "fs_finish.cuh"
+#include "fs_internal.h"
+#include "fs_sm100.cuh"
+#include "fs_tmap.h"
+
+namespace fs {
+namespace {
+
+using namespace sm100;
+
+constexpr int kThreads = 320;
+constexpr int kEpiWarps = 8;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kRowsPerCta = 128;    // batch rows of one CTA (half of the MMA M = 256)
+constexpr int kBN = 256;            // vocabulary rows per tile (MMA N); each CTA loads 128
+constexpr int kBK = 64;
+constexpr int kStages = 6;
+constexpr int kATileBytes = kRowsPerCta * kBK * 2;     // 16 KB: this CTA's h rows
+constexpr int kBTileBytes = (kBN / 2) * kBK * 2;       // 16 KB: this CTA's half of the W tile
+constexpr int kTmemCols = 512;
+constexpr int kOffA = 0;
+constexpr int kOffB = kOffA + kStages * kATileBytes;
+constexpr int kOffBars = kOffB + kStages * kBTileBytes;
+constexpr int kNumBars = 2 * kStages + 5;
+constexpr int kOffMisc = kOffBars + kNumBars * 8;
+constexpr int kOffHalf = kOffMisc + 16;
+constexpr int kSmemBytes = kOffHalf + kRowsPerCta * 8 + 1024;
+constexpr uint16_t kPairMask = 0x3;
+
+struct PairArgs {
+  Problem p;            // rows [0, p.B) of this launch's batch slice
+  Finish f;
+  int npt;              // pair tiles (256 batch rows each) of this launch
+  int n_groups;         // groups of npt pairs
+  int n_vt;             // vocabulary tiles = ceil(V_local / 256)
+  int* err;
+};
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_constant__ CUtensorMap tmap_w,
+               const PairArgs args) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + kOffBars);   // used in the even CTA
+  uint64_t* empty_bar = full_bar + kStages;                            // both CTAs
+  uint64_t* tfull_bar = empty_bar + kStages;                           // both CTAs
+  uint64_t* tempty_bar = tfull_bar + 2;                                // used in the even CTA
+  uint64_t* drain_bar = tempty_bar + 2;
+  uint32_t* tmem_base_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
+  int* last_flag = reinterpret_cast<int*>(smem + kOffMisc + 8);
+  Best* half_best = reinterpret_cast<Best*>(smem + kOffHalf);
+
+  const Problem& p = args.p;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();              // 0: issues the MMAs
+  const int pair = blockIdx.x >> 1;
+  const int pt = pair % args.npt;
+  const int q = pair / args.npt;
+  const int n_tiles = q < args.n_vt ? (args.n_vt - 1 - q) / args.n_groups + 1 : 0;
+  const int n_kb = static_cast<int>((p.d + kBK - 1) / kBK);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull_bar[a], 1);
+      mbar_init(&tempty_bar[a], 2 * kEpiWarps);        // one arrival per epilogue warp of both CTAs
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == kProducerWarp && lane == 0) {
+    tma_prefetch_desc(&tmap_h);
+    tma_prefetch_desc(&tmap_w);
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc_pair(tmem_base_slot, kTmemCols);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();                                       // both CTAs' barriers exist before any cross-CTA signal
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_base_slot;
+
+  if (warp == kProducerWarp) {
+    // ---------------------------------------------------------------- TMA producer (both CTAs)
+    if (lane == 0) {
+      const uint64_t pol_w = policy_evict_first();
+      const uint64_t pol_h = policy_evict_last();
+      int stage = 0;
+      uint32_t phase = 0;
+      int64_t n_issued = 0;
+      bool ok = true;
+      for (int t = 0; t < n_tiles && ok; ++t) {
+        const int vt = q + t * args.n_groups;
+        for (int kb = 0; kb < n_kb; ++kb) {
+          if (!mbar_wait(&empty_bar[stage], phase ^ 1, args.err, abort_flag)) { ok = false; break; }
+          const uint32_t leader_full = mapa_shared(smem_u32(&full_bar[stage]), 0);
+          if (rank == 0) mbar_arrive_expect_tx(&full_bar[stage], 2 * (kATileBytes + kBTileBytes));
+          tma_load_2d_pair(smem + kOffA + stage * kATileBytes, &tmap_h, leader_full, kb * kBK,
+                           pt * 2 * kRowsPerCta + static_cast<int>(rank) * kRowsPerCta, pol_h);
+          tma_load_2d_pair(smem + kOffB + stage * kBTileBytes, &tmap_w, leader_full, kb * kBK,
+                           vt * kBN + static_cast<int>(rank) * (kBN / 2), pol_w);
+          ++n_issued;
+          if (++stage == kStages) { stage = 0; phase ^= 1; }
+        }
+      }
+      if (!ok && rank == 0) {
+        volatile int no_abort = 0;
+        for (int64_t i = std::max<int64_t>(0, n_issued - kStages); i < n_issued; ++i)
+          mbar_wait(&full_bar[i % kStages], static_cast<uint32_t>((i / kStages) & 1), args.err, &no_abort);
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // ---------------------------------------------------------------- MMA issuer (even CTA only)
+    if (lane == 0 && rank == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(2 * kRowsPerCta, kBN);
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int t = 0; t < n_tiles && ok; ++t) {
+        const int acc = t & 1;
+        const uint32_t acc_phase = (t >> 1) & 1;
+        if (!mbar_wait(&tempty_bar[acc], acc_phase ^ 1, args.err, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * kBN;
+        for (int kb = 0; kb < n_kb; ++kb) {
+          if (!mbar_wait(&full_bar[stage], phase, args.err, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(smem + kOffA + stage * kATileBytes);
+          const uint32_t b_addr = smem_u32(smem + kOffB + stage * kBTileBytes);
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k)
+            mma_bf16_pair(d_tmem, smem_desc_k128(a_addr + k * 32), smem_desc_k128(b_addr + k * 32), idesc,
+                          (kb | k) != 0);
+          mma_commit_pair_multicast(&empty_bar[stage], kPairMask);   // frees the stage in both CTAs
+          if (++stage == kStages) { stage = 0; phase ^= 1; }
+        }
+        if (ok) mma_commit_pair_multicast(&tfull_bar[acc], kPairMask);
+      }
+      if (!ok) {
+        mma_commit_pair_multicast(drain_bar, 0x1);
+        volatile int no_abort = 0;
+        mbar_wait(drain_bar, 0, args.err, &no_abort);
+      }
+    }
+  } else {
+    // ---------------------------------------------------------------- epilogue (warps 0-7, both CTAs)
+    const int quad = warp & 3;
+    const int half = warp >> 2;
+    const int row_in_tile = quad * 32 + lane;
+    const int64_t b = static_cast<int64_t>(pt) * 2 * kRowsPerCta + static_cast<int64_t>(rank) * kRowsPerCta + row_in_tile;
+    const bool row_ok = b < p.B;
+    const RowTemp rt = row_temp(row_ok ? p.temp[b] : -1.0f);
+    const bool active = row_ok && rt.mode != kRowInvalid;
+    const bool greedy = rt.mode == kRowGreedy;
+    const PhiloxKey key{static_cast<uint32_t>(p.seed), static_cast<uint32_t>(p.seed >> 32)};
+    const uint32_t step_lo = static_cast<uint32_t>(p.step);
+    const uint32_t step_hi = static_cast<uint32_t>(p.step >> 32);
+    const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
+    RowScan scan;
+    scan.key = key;
+    scan.row = static_cast<uint32_t>(b);
+    scan.step_lo = step_lo;
+    scan.step_hi = step_hi;
+    scan.inv_t = rt.inv_t;
+    scan.greedy = greedy;
+    scan.bias_row = p.bias != nullptr ? p.bias + b * p.bias_stride : nullptr;
+    Best best = best_none();
+    for (int t = 0; t < n_tiles; ++t) {
+      const int acc = t & 1;
+      const uint32_t acc_phase = (t >> 1) & 1;
+      if (!mbar_wait(&tfull_bar[acc], acc_phase, args.err, abort_flag)) break;
+      tc_fence_after();
+      const int vt = q + t * args.n_groups;
+      const int64_t col0 = static_cast<int64_t>(vt) * kBN + half * (kBN / 2);
+#pragma unroll 1
+      for (int c = 0; c < kBN / 2; c += 32) {
+        uint32_t r[32];
+        tmem_ld_32(tmem_base + lane_addr + acc * kBN + half * (kBN / 2) + c, r);
+        tmem_ld_wait();
+        const int64_t v0 = col0 + c;
+        if (active && v0 < p.V_local) {
+          if (scan.bias_row != nullptr)
+            scan32<true>(r, v0, p.V_local, p.v_offset, scan, best);
+          else
+            scan32<false>(r, v0, p.V_local, p.v_offset, scan, best);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&tempty_bar[acc]), 0));
+    }
+    if (half == 1) half_best[row_in_tile] = best;
+    asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
+    if (half == 0 && row_ok) push_candidate(args.f, b, combine(best, half_best[row_in_tile]));
+    finish_grid(args.f, p.B, threadIdx.x, kEpiWarps * 32, last_flag,
+                [] { asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory"); });
+  }
+
+  // ---- teardown: neither CTA leaves (or frees TMEM) while the pair's MMAs or
+  // the peer's signals may still touch it
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();
+  tc_fence_after();
+  if (warp == kMmaWarp) tmem_dealloc_pair(tmem_base, kTmemCols);
+}
+
+}  // namespace
+
+cudaError_t launch_tc_pair(const Problem& p, const Finish& f, int* err, cudaStream_t stream) {
+  if (p.d < kBK || p.V_local <= 0) return cudaErrorNotSupported;
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (sms <= 0) sms = 148;
+  const int pairs = sms / 2;
+  cudaError_t e = cudaFuncSetAttribute(tc_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  CUtensorMap tw;
+  if (!encode_kmajor_bf16(&tw, p.W, p.V_local, p.d, kBK, kBN / 2)) return cudaErrorInvalidValue;
+  const int64_t slice = static_cast<int64_t>(pairs) * 2 * kRowsPerCta;
+  for (int64_t b0 = 0; b0 < p.B; b0 += slice) {
+    Problem ps = p;
+    ps.B = std::min<int64_t>(slice, p.B - b0);
+    ps.h = static_cast<const uint16_t*>(p.h) + b0 * p.d;
+    ps.temp = p.temp + b0;
+    if (p.bias != nullptr) ps.bias = p.bias + b0 * p.bias_stride;
+    Finish fs_slice = f;
+    fs_slice.keys = f.keys + b0;
+    if (f.carry_max != nullptr) {
+      fs_slice.carry_max = f.carry_max + b0;
+      fs_slice.carry_ids = f.carry_ids + b0;
+    }
+    if (f.write_out) {
+      fs_slice.out_ids = f.out_ids + b0;
+      fs_slice.out_max = f.out_max + b0;
+    }
+    const int npt = static_cast<int>((ps.B + 2 * kRowsPerCta - 1) / (2 * kRowsPerCta));
+    const int n_groups = std::max(1, pairs / npt);
+    CUtensorMap th;
+    if (!encode_kmajor_bf16(&th, ps.h, ps.B, p.d, kBK, kRowsPerCta)) return cudaErrorInvalidValue;
+    PairArgs a{ps, fs_slice, npt, n_groups, static_cast<int>((p.V_local + kBN - 1) / kBN), err};
+    tc_pair_kernel<<<2 * npt * n_groups, kThreads, kSmemBytes, stream>>>(th, tw, a);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+}  // namespace fs

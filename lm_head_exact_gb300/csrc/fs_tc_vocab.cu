@@ -30,6 +30,7 @@
 
 #include <algorithm>
 
+#include "fs_epilogue.cuh"
 #include "fs_finish.cuh"
 #include "fs_internal.h"
 #include "fs_sm100.cuh"
@@ -254,25 +255,28 @@ tc_vocab_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
           const int b = c0 + lane;
           const int mode = (lane < C::kChunk && b < B) ? col_mode[b] : kRowInvalid;
           if (mode != kRowInvalid) {
-            const float inv_t = col_inv_t[b];
+            RowScan scan;
+            scan.key = key;
+            scan.row = static_cast<uint32_t>(b);
+            scan.step_lo = step_lo;
+            scan.step_hi = step_hi;
+            scan.inv_t = col_inv_t[b];
+            scan.greedy = mode == kRowGreedy;
+            scan.bias_row = p.bias != nullptr ? p.bias + static_cast<int64_t>(b) * p.bias_stride : nullptr;
+            uint32_t vals[32];
             const float* col = tr + lane * 33;
-            const float* bias_row = p.bias != nullptr ? p.bias + static_cast<int64_t>(b) * p.bias_stride : nullptr;
-            uint4 w = make_uint4(0, 0, 0, 0);
-            for (int i = 0; i < n_rows; ++i) {
-              const int64_t v_local = row0 + i;
-              const int64_t vg = p.v_offset + v_local;
-              if (i == 0 || (vg & 3) == 0)
-                w = noise_words(key, static_cast<uint32_t>(vg >> 2), static_cast<uint32_t>(b), step_lo, step_hi);
-              float logit = col[i];
-              if (bias_row != nullptr) logit += __ldg(bias_row + v_local);
-              const float z = mode == kRowGreedy
-                                  ? logit
-                                  : fmaf(logit, inv_t, gumbel_from_word(word_of(w, static_cast<uint32_t>(vg & 3))));
-              if (z > best_z[c]) {      // ids rise: strict > keeps the smaller id on ties
-                best_z[c] = z;
-                best_id[c] = static_cast<int32_t>(vg);
-              }
-            }
+#pragma unroll
+            for (int i = 0; i < 32; ++i) vals[i] = __float_as_uint(col[i]);
+            Best bb;
+            bb.z = best_z[c];
+            bb.id = best_id[c];
+            const int64_t row_end = row0 + n_rows;
+            if (scan.bias_row != nullptr)
+              scan32<true>(vals, row0, row_end, p.v_offset, scan, bb);
+            else
+              scan32<false>(vals, row0, row_end, p.v_offset, scan, bb);
+            best_z[c] = bb.z;
+            best_id[c] = bb.id;
           }
         }
       }

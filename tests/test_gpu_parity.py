@@ -35,11 +35,11 @@ def _problem(B, V, d, seed, w_std=0.05, temps=None):
     return h, W, np.asarray(temps, np.float32)
 
 
-@pytest.fixture(params=["simt", "tc_vocab", "tc_batch"])
+@pytest.fixture(params=["simt", "tc_vocab", "tc_batch", "tc_pair"])
 def path(request, fs):
     """Run the test once per kernel family (forced through fs_set_path)."""
     code = {"simt": fs.FS_PATH_SIMT, "tc_vocab": fs.FS_PATH_TC_VOCAB,
-            "tc_batch": fs.FS_PATH_TC_BATCH}[request.param]
+            "tc_batch": fs.FS_PATH_TC_BATCH, "tc_pair": fs.FS_PATH_TC_PAIR}[request.param]
     fs.set_path(code)
     yield request.param
     fs.set_path(fs.FS_PATH_AUTO)
@@ -238,13 +238,14 @@ def test_paths_agree_on_llama3_8b_head(fs, torch_cuda):
     wl = synthetic.workload("llama3_8b", 64)
     hd, Wd, td = to_device(wl.h, torch), to_device(wl.W, torch), to_device(wl.temp, torch)
     out = {}
-    for name, code in (("simt", fs.FS_PATH_SIMT), ("tc", fs.FS_PATH_TC_VOCAB), ("tcb", fs.FS_PATH_TC_BATCH)):
+    for name, code in (("simt", fs.FS_PATH_SIMT), ("tc", fs.FS_PATH_TC_VOCAB), ("tcb", fs.FS_PATH_TC_BATCH),
+                       ("tcp", fs.FS_PATH_TC_PAIR)):
         fs.set_path(code)
         ids, mx = fs.sample(hd, Wd, td, wl.seed, 11)
         torch.cuda.synchronize()
         out[name] = (ids.cpu().numpy(), mx.cpu().numpy())
     fs.set_path(fs.FS_PATH_AUTO)
-    for other in ("tc", "tcb"):
+    for other in ("tc", "tcb", "tcp"):
         diff = out["simt"][0] != out[other][0]
         assert diff.sum() <= 1
         assert np.abs(out["simt"][1] - out[other][1])[~diff].max() < 1e-3

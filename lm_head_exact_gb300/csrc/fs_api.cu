@@ -47,6 +47,8 @@ struct Workspace {
   size_t staging_bytes = 0;
   void* unfused = nullptr;      // logits + probabilities of fs_sample_unfused
   size_t unfused_bytes = 0;
+  void* host_out = nullptr;     // pinned host landing area of fs_sample_host's results
+  size_t host_out_bytes = 0;
 };
 
 std::mutex g_ws_mutex;
@@ -349,35 +351,65 @@ fs_status fs_sample_host(const void* h_host, const void* W, int64_t B, int64_t d
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
   int dev;
   FS_TRY(current_device(&dev));
+  if (V > 0) {
+    FS_TRY(check_device_ptr(W, "W"));
+    FS_TRY(check_aligned(W, 16, "W"));
+  }
+  if (bias != nullptr) {
+    if (bias_row_stride < 0 || (bias_row_stride != 0 && bias_row_stride < V))
+      return fail(FS_ERR_INVALID_ARG, "bias_row_stride must be 0 or >= V");
+    FS_TRY(check_device_ptr(bias, "bias"));
+    FS_TRY(check_aligned(bias, 4, "bias"));
+  }
+  // device staging: [h | temp | ids, max] -- the results are contiguous so one
+  // copy brings them back into a pinned landing area of the library
   const size_t h_bytes = static_cast<size_t>(B) * d * 2;
   const size_t off_temp = (h_bytes + 255) & ~size_t(255);
   const size_t off_ids = off_temp + ((static_cast<size_t>(B) * 4 + 255) & ~size_t(255));
-  const size_t off_max = off_ids + ((static_cast<size_t>(B) * 8 + 255) & ~size_t(255));
-  const size_t total = off_max + static_cast<size_t>(B) * 4;
+  const size_t off_max = off_ids + static_cast<size_t>(B) * 8;
+  const size_t out_bytes = static_cast<size_t>(B) * 12;
+  const size_t total = off_ids + out_bytes;
   char* staging = nullptr;
+  char* landing = nullptr;
   {
     std::lock_guard<std::mutex> lock(g_ws_mutex);
     Workspace& ws = g_workspaces[{dev, stream}];
     FS_TRY(grow(&ws.staging, &ws.staging_bytes, total, stream));
     staging = static_cast<char*>(ws.staging);
+    if (ws.host_out_bytes < out_bytes) {
+      if (ws.host_out != nullptr) {
+        cudaStreamSynchronize(stream);
+        cudaFreeHost(ws.host_out);
+        ws.host_out = nullptr;
+        ws.host_out_bytes = 0;
+      }
+      if (cudaHostAlloc(&ws.host_out, out_bytes, cudaHostAllocDefault) != cudaSuccess) {
+        cudaGetLastError();
+        ws.host_out = nullptr;
+        return fail(FS_ERR_WORKSPACE, "pinned host landing area of %zu bytes", out_bytes);
+      }
+      ws.host_out_bytes = out_bytes;
+    }
+    landing = static_cast<char*>(ws.host_out);
   }
   cudaError_t e = cudaMemcpyAsync(staging, h_host, h_bytes, cudaMemcpyHostToDevice, stream);
   if (e == cudaSuccess)
     e = cudaMemcpyAsync(staging + off_temp, temp_host, static_cast<size_t>(B) * 4,
                         cudaMemcpyHostToDevice, stream);
   if (e != cudaSuccess) return cuda_fail(e, "host-to-device copy");
-  fs_status s = fs_sample_ex(staging, W, B, d, V, reinterpret_cast<const float*>(staging + off_temp),
-                             bias, bias_row_stride, seed, step,
-                             reinterpret_cast<int64_t*>(staging + off_ids),
-                             reinterpret_cast<float*>(staging + off_max), stream);
-  if (s != FS_OK) return s;
-  e = cudaMemcpyAsync(out_ids_host, staging + off_ids, static_cast<size_t>(B) * 8,
-                      cudaMemcpyDeviceToHost, stream);
-  if (e == cudaSuccess)
-    e = cudaMemcpyAsync(out_max_host, staging + off_max, static_cast<size_t>(B) * 4,
-                        cudaMemcpyDeviceToHost, stream);
+  // staging pointers are the library's own device memory: no per-pointer queries
+  Problem p{staging, W, B, d, V, 0, reinterpret_cast<const float*>(staging + off_temp), bias,
+            bias_row_stride, seed, step};
+  Finish f{};
+  f.write_out = true;
+  f.out_ids = reinterpret_cast<int64_t*>(staging + off_ids);
+  f.out_max = reinterpret_cast<float*>(staging + off_max);
+  FS_TRY(run(p, f, stream));
+  e = cudaMemcpyAsync(landing, staging + off_ids, out_bytes, cudaMemcpyDeviceToHost, stream);
   if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
   if (e != cudaSuccess) return cuda_fail(e, "device-to-host copy");
+  memcpy(out_ids_host, landing, static_cast<size_t>(B) * 8);
+  memcpy(out_max_host, landing + static_cast<size_t>(B) * 8, static_cast<size_t>(B) * 4);
   return FS_OK;
 }
 
@@ -446,6 +478,7 @@ fs_status fs_workspace_release(void) {
       cudaStreamSynchronize(it->first.second);
       if (it->second.finish) cudaFree(it->second.finish);
       if (it->second.unfused) cudaFree(it->second.unfused);
+      if (it->second.host_out) cudaFreeHost(it->second.host_out);
       if (it->second.staging) cudaFree(it->second.staging);
       it = g_workspaces.erase(it);
     } else {

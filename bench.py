@@ -275,7 +275,7 @@ def run_ours(args):
     shape = synthetic.SHAPES[kind]
     d, V = shape["d"], shape["V"]
     B = args.batch
-    bmax = max(max(SWEEP), B)
+    bmax = max(max(SWEEP), B, max(synthetic.SHAPES["chunked"]["batches"]))
     # every rank gets its own batch rows (weak scaling); W is replicated
     h_all = synthetic.normal_rows_bf16(synthetic.SEED_H, bmax * world, d, 1.0)
     h_rank = h_all[rank * bmax:(rank + 1) * bmax]
@@ -348,6 +348,48 @@ def run_ours(args):
             sweep.append(point("qwen3_8b", b, h_big, Wq, tq, qshape["V"], qshape["d"]))
         del Wq
 
+    # the grouped online (chunked) variant: 8 and 32 contiguous vocabulary
+    # chunks per decode step, each chunk one launch; the step is captured in a
+    # CUDA graph and replayed (launches amortized), timed with events
+    chunked = []
+    if not args.no_sweep:
+        for b in synthetic.SHAPES["chunked"]["batches"]:
+            for n in (8, 32):
+                bounds = synthetic.chunk_bounds(V, n)
+                cm = torch.empty(b, device="cuda")
+                ci = torch.empty(b, dtype=torch.int64, device="cuda")
+                cids = torch.empty(b, dtype=torch.int64, device="cuda")
+                cmx = torch.empty(b, dtype=torch.float32, device="cuda")
+                fs.workspace_reserve(b, V, stream=stream)
+
+                def chunk_step():
+                    for i, (lo, hi) in enumerate(zip(bounds[:-1], bounds[1:])):
+                        fs.sample_chunked(hd_all[:b], Wd[lo:hi], lo, temp_all[:b],
+                                          seed, 5, cm, ci, i == 0, i == n - 1, out=(cids, cmx), stream=stream)
+
+                with torch.cuda.stream(stream):
+                    chunk_step()
+                torch.cuda.synchronize()
+                graph = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(graph, stream=stream):
+                    chunk_step()
+                for _ in range(3):
+                    graph.replay()
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                with torch.cuda.stream(stream):
+                    for _ in range(20):
+                        graph.replay()
+                e1.record(stream)
+                torch.cuda.synchronize()
+                us = e0.elapsed_time(e1) / 20 * 1e3
+                rf = roofline(b, d, V, us, peaks)
+                chunked.append({"workload": "chunked", "B": b, "chunks": n, "us_per_step": round(us, 2),
+                                "frac": rf["frac"], "bound": rf["bound"], "path": fs.path_for_batch(b),
+                                "launches_per_step": n, "cuda_graph": True})
+                del graph
+
     # the unfused comparison pipeline on the same workload: GEMM -> fp32
     # logits in HBM -> softmax -> sample (the traffic fusion removes)
     unfused = None
@@ -393,6 +435,7 @@ def run_ours(args):
             "gpu_launches": launches,
             "sweep": sweep,
             "unfused": unfused,
+            "chunked": chunked,
         }
         if not args.no_cpu_baseline:
             result["cpu_baseline"] = cpu_baseline(B, args.cpu_seconds)

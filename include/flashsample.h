@@ -106,7 +106,11 @@ FS_API fs_status fs_sample_ex(const void* h, const void* W, int64_t B, int64_t d
 /*
  * Grouped online (chunked) variant (arXiv abstract; summary page, "Method",
  * last paragraph): one call per contiguous vocabulary chunk [v_begin, v_end),
- * with a per-row (max, argmax) carry between calls.  The result of a full
+ * with a per-row (max, argmax) carry between calls.  Calls after the first
+ * chunk are launched as programmatic dependents: a chunk's kernel may start
+ * streaming its W rows while the previous chunk's kernel still runs and waits
+ * for it only before merging the carry -- so between the chunk calls of one
+ * step, enqueue nothing on the stream that writes h, temp, W or bias.  The result of a full
  * sequence of calls equals fs_sample on the whole vocabulary bit for bit,
  * because the noise of (b, v) depends on the global id v only and the same
  * kernel family (chosen from B) computes every logit.
@@ -186,7 +190,9 @@ FS_API size_t fs_workspace_bytes(int64_t B, int64_t V);
 
 /*
  * Grow the workspace of (current device, stream) to serve calls up to
- * (B, V) without allocating; required before capturing calls in a CUDA graph.
+ * (B, V) without allocating, and create the device error word; required
+ * before capturing fs_sample / fs_sample_ex / fs_sample_chunked calls in a
+ * CUDA graph on that stream (the seed and step are then fixed in the graph).
  */
 FS_API fs_status fs_workspace_reserve(int64_t B, int64_t V, void* stream);
 

@@ -322,6 +322,10 @@ fs_status fs_sample_chunked(const void* h, const void* W_chunk, int64_t B, int64
   if (flags & ~(FS_CHUNK_FIRST | FS_CHUNK_LAST)) return fail(FS_ERR_INVALID_ARG, "unknown flags 0x%x", flags);
   const bool last = (flags & FS_CHUNK_LAST) != 0;
   Problem p{h, W_chunk, B, d, v_end - v_begin, v_begin, temp, bias_chunk, bias_row_stride, seed, step};
+  // Chunks after the first may start streaming their W rows while the
+  // previous chunk's kernel is still running (programmatic dependent launch);
+  // they wait for it only before merging into the shared carry.
+  p.pdl = (flags & FS_CHUNK_FIRST) == 0;
   FS_TRY(check_problem(p, last, out_ids, out_max));
   if (B > 0) {
     FS_TRY(check_device_ptr(carry_max, "carry_max"));
@@ -465,6 +469,8 @@ size_t fs_workspace_bytes(int64_t B, int64_t V) {
 fs_status fs_workspace_reserve(int64_t B, int64_t V, void* stream) {
   g_last_error[0] = '\0';
   if (B < 0 || V < 0) return fail(FS_ERR_INVALID_ARG, "need B >= 0 and V >= 0");
+  int* err = nullptr;
+  FS_TRY(error_word(&err));           // allocated once per device, never during capture
   Finish f{};
   return get_finish(static_cast<cudaStream_t>(stream), B, &f);
 }

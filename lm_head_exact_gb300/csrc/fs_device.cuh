@@ -173,6 +173,21 @@ __device__ __forceinline__ Best unpack_key(unsigned long long k) {
   return b;
 }
 
+// -------------------------------------------------------------------------
+// Programmatic dependent launch.  A fused kernel lets the next kernel of its
+// stream start as soon as every CTA has begun (launch_dependents), and waits
+// for the previous kernel of its stream to complete (wait) only before it
+// touches the cross-CTA finish area and the carry, which consecutive chunk
+// launches share.  Without a programmatic launch both are no-ops.
+// -------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void pdl_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // Device error word: set by kernels whose bounded waits run out; read and
 // cleared by the host through fs_device_error().
 enum DeviceError : int {

@@ -4,6 +4,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <utility>
 #include <cuda_runtime.h>
 
 #include "fs_device.cuh"
@@ -24,7 +25,30 @@ struct Problem {
   int64_t bias_stride;    // 0: one [V_local] vector shared by all rows
   uint64_t seed;
   uint64_t step;
+  // Launch as a programmatic dependent of the previous kernel of the stream
+  // (set for the 2nd..last chunk of a chunked step, whose inputs were all
+  // written before the first chunk was enqueued).
+  bool pdl = false;
 };
+
+// Launch `kernel` on `stream`, as a programmatic dependent launch when `pdl`.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                          bool pdl, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  if (pdl) {
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // How a launch finishes the sample.  The fused kernels reduce across CTAs
 // themselves: every CTA atomicMax-es its per-row candidates into `keys`

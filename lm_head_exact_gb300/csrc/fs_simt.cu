@@ -48,6 +48,7 @@ simt_fused_kernel(Problem p, Finish f) {
   __shared__ Best warp_best[kSimtWarps][BG];
   __shared__ int last_flag;
   const int n_parts = gridDim.x;
+  pdl_launch_dependents();
 
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
@@ -127,6 +128,7 @@ simt_fused_kernel(Problem p, Finish f) {
 
     if (lane < BG) warp_best[warp][lane] = best;
     __syncthreads();
+    pdl_wait();                                // the finish area is shared with the previous launch
     if (threadIdx.x < BG && b0 + threadIdx.x < p.B) {
       Best r = warp_best[0][threadIdx.x];
 #pragma unroll
@@ -152,8 +154,7 @@ cudaError_t launch_group(const Problem& p, const Finish& f, int n_parts, cudaStr
   if (e != cudaSuccess) return e;
   const int64_t groups = (p.B + BG - 1) / BG;
   dim3 grid(n_parts, static_cast<unsigned>(std::min<int64_t>(groups, 65535)));
-  simt_fused_kernel<BG><<<grid, kSimtThreads, smem, stream>>>(p, f);
-  return cudaGetLastError();
+  return launch_kernel(simt_fused_kernel<BG>, grid, dim3(kSimtThreads), smem, stream, p.pdl, p, f);
 }
 
 }  // namespace

@@ -122,6 +122,7 @@ tc_batch_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_constan
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  pdl_launch_dependents();
   const uint32_t tmem_base = *tmem_base_slot;
 
   if (warp == kProducerWarp) {
@@ -248,6 +249,7 @@ tc_batch_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_constan
     if (half == 1) half_best[row_in_tile] = best;
     asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
     if constexpr (!kStoreLogits) {
+      pdl_wait();                 // the finish area is shared with the previous launch
       if (half == 0 && row_ok) push_candidate(args.f, b, combine(best, half_best[row_in_tile]));
       finish_grid(args.f, p.B, threadIdx.x, kEpiWarps * 32, last_flag,
                   [] { asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory"); });
@@ -320,11 +322,12 @@ static cudaError_t launch_batch_impl(const Problem& p, const Finish* f, float* l
     if (!encode_kmajor_bf16(&th, ps.h, ps.B, p.d, kBK, kBM)) return cudaErrorInvalidValue;
     BatchArgs a{ps, store ? logits + b0 * p.V_local : nullptr, fs_slice, g.nbt, g.n_groups,
                 static_cast<int>((p.V_local + kBN - 1) / kBN), err};
-    if (store)
+    if (store) {
       tc_batch_kernel<true><<<g.grid, kThreads, kSmemBytes, stream>>>(th, tw, a);
-    else
-      tc_batch_kernel<false><<<g.grid, kThreads, kSmemBytes, stream>>>(th, tw, a);
-    e = cudaGetLastError();
+      e = cudaGetLastError();
+    } else {
+      e = launch_kernel(tc_batch_kernel<false>, dim3(g.grid), dim3(kThreads), kSmemBytes, stream, ps.pdl, th, tw, a);
+    }
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;

@@ -115,6 +115,7 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_constant
   __syncthreads();
   cluster_sync();                                       // both CTAs' barriers exist before any cross-CTA signal
   tc_fence_after();
+  pdl_launch_dependents();
   const uint32_t tmem_base = *tmem_base_slot;
 
   if (warp == kProducerWarp) {
@@ -228,6 +229,7 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_constant
     }
     if (half == 1) half_best[row_in_tile] = best;
     asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
+    pdl_wait();                   // the finish area is shared with the previous launch
     if (half == 0 && row_ok) push_candidate(args.f, b, combine(best, half_best[row_in_tile]));
     finish_grid(args.f, p.B, threadIdx.x, kEpiWarps * 32, last_flag,
                 [] { asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory"); });
@@ -277,8 +279,7 @@ cudaError_t launch_tc_pair(const Problem& p, const Finish& f, int* err, cudaStre
     CUtensorMap th;
     if (!encode_kmajor_bf16(&th, ps.h, ps.B, p.d, kBK, kRowsPerCta)) return cudaErrorInvalidValue;
     PairArgs a{ps, fs_slice, npt, n_groups, static_cast<int>((p.V_local + kBN - 1) / kBN), err};
-    tc_pair_kernel<<<2 * npt * n_groups, kThreads, kSmemBytes, stream>>>(th, tw, a);
-    e = cudaGetLastError();
+    e = launch_kernel(tc_pair_kernel, dim3(2 * npt * n_groups), dim3(kThreads), kSmemBytes, stream, ps.pdl, th, tw, a);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;

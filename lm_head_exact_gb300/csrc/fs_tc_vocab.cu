@@ -141,6 +141,7 @@ tc_vocab_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  pdl_launch_dependents();
   const uint32_t tmem_base = *tmem_base_slot;
 
   if (warp == kProducerWarp) {
@@ -283,6 +284,7 @@ tc_vocab_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
       tc_fence_before();
       mbar_arrive(&tempty_bar[acc]);
     }
+    pdl_wait();                   // the finish area is shared with the previous launch
 #pragma unroll
     for (int c = 0; c < C::kChunks; ++c) {
       const int b = c * C::kChunk + lane;
@@ -331,8 +333,7 @@ cudaError_t launch_bn(const Problem& p, const Finish& f, int* err, cudaStream_t 
   const int64_t n_vt = (p.V_local + kBM - 1) / kBM;
   const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(sms, n_vt)));
   VocabArgs a{p, f, n_vt, err};
-  tc_vocab_kernel<BN><<<grid, kThreads, C::kSmemBytes, stream>>>(tw, th, a);
-  return cudaGetLastError();
+  return launch_kernel(tc_vocab_kernel<BN>, dim3(grid), dim3(kThreads), C::kSmemBytes, stream, p.pdl, tw, th, a);
 }
 
 }  // namespace

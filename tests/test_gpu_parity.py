@@ -318,3 +318,62 @@ def test_back_to_back_calls_of_different_batch_sizes(fs, torch_cuda, path):
         torch.cuda.synchronize()
         compare(ids.cpu().numpy(), mx.cpu().numpy(), sampler.sample(h[:B], W, temp[:B], 3, B),
                 what=f"B={B}")
+
+
+@pytest.mark.parametrize("B", [1, 32, 256])
+def test_chunked_sequence_captured_in_cuda_graph(fs, torch_cuda, B):
+    """After fs_workspace_reserve, a whole chunked decode step (8 launches)
+    can be captured into a CUDA graph; every replay reproduces the one-shot
+    sample bit for bit."""
+    torch = torch_cuda
+    V, d, n = 20011, 256, 8
+    h, W, temp = _problem(B, V, d, seed=40 + B)
+    hd, Wd, td = to_device(h, torch), to_device(W, torch), to_device(temp, torch)
+    bounds = synthetic.chunk_bounds(V, n)
+    stream = torch.cuda.Stream()
+    cm = torch.empty(B, device="cuda")
+    ci = torch.empty(B, dtype=torch.int64, device="cuda")
+    ids = torch.empty(B, dtype=torch.int64, device="cuda")
+    mx = torch.empty(B, dtype=torch.float32, device="cuda")
+    fs.workspace_reserve(B, V, stream=stream)
+
+    def step():
+        for i, (lo, hi) in enumerate(zip(bounds[:-1], bounds[1:])):
+            fs.sample_chunked(hd, Wd[lo:hi], lo, td, 5, 9, cm, ci, i == 0, i == n - 1,
+                              out=(ids, mx), stream=stream)
+
+    with torch.cuda.stream(stream):
+        step()                                       # warm: kernels loaded, attributes set
+    torch.cuda.synchronize()
+    ref_ids, ref_mx = fs.sample(hd, Wd, td, 5, 9)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        step()
+    for _ in range(2):
+        ids.fill_(-7)
+        g.replay()
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(ids.cpu().numpy(), ref_ids.cpu().numpy())
+        np.testing.assert_array_equal(mx.cpu().numpy(), ref_mx.cpu().numpy())
+
+
+def test_many_small_chunks_overlapping_launches(fs, torch_cuda, path):
+    """97 chunks of a step launched back to back: from the second chunk on,
+    each chunk kernel may start while the previous one runs (programmatic
+    dependent launch) and only waits before merging the carry; the result
+    must still equal the one-shot sample bit for bit, step after step."""
+    torch = torch_cuda
+    B, V, d, n = 40, 30011, 128, 97
+    h, W, temp = _problem(B, V, d, seed=77)
+    hd, Wd, td = to_device(h, torch), to_device(W, torch), to_device(temp, torch)
+    bounds = synthetic.chunk_bounds(V, n)
+    cm = torch.empty(B, device="cuda")
+    ci = torch.empty(B, dtype=torch.int64, device="cuda")
+    for step in (0, 1, 2):
+        ref_ids, ref_mx = fs.sample(hd, Wd, td, 3, step)
+        for i, (lo, hi) in enumerate(zip(bounds[:-1], bounds[1:])):
+            res = fs.sample_chunked(hd, Wd[lo:hi], lo, td, 3, step, cm, ci, i == 0, i == n - 1)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(res[0].cpu().numpy(), ref_ids.cpu().numpy())
+        np.testing.assert_array_equal(res[1].cpu().numpy(), ref_mx.cpu().numpy())

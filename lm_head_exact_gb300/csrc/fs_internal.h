@@ -29,6 +29,9 @@ struct Problem {
   // (set for the 2nd..last chunk of a chunked step, whose inputs were all
   // written before the first chunk was enqueued).
   bool pdl = false;
+  // Global index of row 0 of h in this launch (a batch split over several
+  // launches); the noise counter always uses the global row.
+  int64_t row_offset = 0;
 };
 
 // Launch `kernel` on `stream`, as a programmatic dependent launch when `pdl`.

@@ -202,7 +202,7 @@ tc_batch_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_constan
     const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
     RowScan scan;
     scan.key = key;
-    scan.row = static_cast<uint32_t>(b);
+    scan.row = static_cast<uint32_t>(p.row_offset + b);
     scan.step_lo = step_lo;
     scan.step_hi = step_hi;
     scan.inv_t = rt.inv_t;
@@ -304,6 +304,7 @@ static cudaError_t launch_batch_impl(const Problem& p, const Finish* f, float* l
     ps.h = static_cast<const uint16_t*>(p.h) + b0 * p.d;
     ps.temp = p.temp + b0;
     if (p.bias != nullptr) ps.bias = p.bias + b0 * p.bias_stride;
+    ps.row_offset = p.row_offset + b0;
     Finish fs_slice{};
     if (!store) {            // this launch finishes rows [b0, b0 + ps.B)
       fs_slice = *f;

@@ -196,7 +196,7 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_constant
     const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
     RowScan scan;
     scan.key = key;
-    scan.row = static_cast<uint32_t>(b);
+    scan.row = static_cast<uint32_t>(p.row_offset + b);
     scan.step_lo = step_lo;
     scan.step_hi = step_hi;
     scan.inv_t = rt.inv_t;
@@ -264,6 +264,7 @@ cudaError_t launch_tc_pair(const Problem& p, const Finish& f, int* err, cudaStre
     ps.h = static_cast<const uint16_t*>(p.h) + b0 * p.d;
     ps.temp = p.temp + b0;
     if (p.bias != nullptr) ps.bias = p.bias + b0 * p.bias_stride;
+    ps.row_offset = p.row_offset + b0;
     Finish fs_slice = f;
     fs_slice.keys = f.keys + b0;
     if (f.carry_max != nullptr) {

@@ -377,3 +377,20 @@ def test_many_small_chunks_overlapping_launches(fs, torch_cuda, path):
         torch.cuda.synchronize()
         np.testing.assert_array_equal(res[0].cpu().numpy(), ref_ids.cpu().numpy())
         np.testing.assert_array_equal(res[1].cpu().numpy(), ref_mx.cpu().numpy())
+
+
+@pytest.mark.parametrize("forced", ["tc_batch", "tc_pair", "auto"])
+def test_batch_larger_than_one_launch(fs, torch_cuda, forced):
+    """B = 20000 exceeds what one batch-major launch covers (SMs x 128 rows),
+    so the call is split into consecutive launches that share the finish
+    ticket; every row must still match the oracle."""
+    torch = torch_cuda
+    B, V, d = 20000, 300, 64
+    h, W, temp = _problem(B, V, d, seed=91)
+    code = {"tc_batch": fs.FS_PATH_TC_BATCH, "tc_pair": fs.FS_PATH_TC_PAIR, "auto": fs.FS_PATH_AUTO}[forced]
+    fs.set_path(code)
+    try:
+        ids, mx = _run(fs, torch, h, W, temp, 8, 2)
+    finally:
+        fs.set_path(fs.FS_PATH_AUTO)
+    compare(ids, mx, sampler.sample(h, W, temp, 8, 2), what=f"B=20000 {forced}")

@@ -263,3 +263,66 @@ def sample_chunked(h_bits, W_bits, temp, seed, step, bounds, bias=None, rows=Non
         carry = combine(carry, (s.ids, s.zmax))
     return carry
 
+
+
+# --------------------------------------------------------------------------
+# Early finalization of the grouped online variant (summary page, Method,
+# last paragraph: the streaming sampler "can finalize the sample as soon as
+# later tiles can no longer overtake the running maximum").  The pages give
+# no bound; the reading here is Cauchy-Schwarz on the logit plus the largest
+# Gumbel value the uniform grid can produce.
+# --------------------------------------------------------------------------
+
+# Largest Gumbel draw: u = 1 - 2^-24, the top of the uniform grid.
+G_MAX = float(-np.log(-np.log(1.0 - 2.0 ** -24)))
+
+
+def row_norms(bits):
+    """Euclidean norm of every row of a bf16 matrix, fp64."""
+    x = bf16_to_f64(bits)
+    return np.sqrt(np.sum(x * x, axis=1))
+
+
+def score_upper_bound(h_norm, w_norm_max, bias_max, temp):
+    """Upper bound of z = (logit + bias) / T + g over a set of vocabulary rows
+    whose largest norm is w_norm_max and largest bias is bias_max:
+    |logit| <= |h| |W_v| (Cauchy-Schwarz), g <= G_MAX.  Greedy rows (T = 0)
+    have no noise; rows with an invalid T never take a sample (-inf)."""
+    T = np.asarray(temp, dtype=np.float32).astype(np.float64)
+    lim = np.asarray(h_norm, dtype=np.float64) * w_norm_max + bias_max
+    ub = np.where(T > 0, lim / np.where(T > 0, T, 1.0) + G_MAX, lim)
+    return np.where((T < 0) | np.isnan(T), -np.inf, ub)
+
+
+def sample_chunked_early(h_bits, W_bits, temp, seed, step, bounds, bias=None):
+    """The grouped online variant with early finalization: after each chunk,
+    a row is final when its carried maximum is at least the upper bound of
+    every later chunk (rows with an invalid T always are); when all rows are
+    final the remaining chunks are not read.  Returns ((ids, zmax), number of
+    chunks read).  The sample equals the one-shot sample."""
+    B = h_bits.shape[0]
+    hn = row_norms(h_bits)
+    wn = row_norms(W_bits)
+    T = np.asarray(temp, dtype=np.float32)
+    carry = (np.full(B, NO_ID, dtype=np.int64), np.full(B, -np.inf))
+    n = len(bounds) - 1
+    for i in range(n):
+        lo, hi = bounds[i], bounds[i + 1]
+        b_chunk = None if bias is None else np.asarray(bias, np.float32)[..., lo:hi]
+        s = sample(h_bits, W_bits[lo:hi], temp, seed, step, bias=b_chunk, vocab_offset=lo)
+        carry = combine(carry, (s.ids, s.zmax))
+        rest_lo = hi
+        if rest_lo >= bounds[-1]:
+            return carry, i + 1
+        w_rest = wn[rest_lo:].max()
+        if bias is None:
+            b_rest = np.zeros(B)
+        else:
+            bb = np.asarray(bias, np.float32).astype(np.float64)
+            b_rest = bb[..., rest_lo:].max(axis=-1) * np.ones(B)
+        ub = score_upper_bound(hn, w_rest, b_rest, T)
+        invalid = (T < 0) | np.isnan(T)
+        final = invalid | ((carry[0] != NO_ID) & (carry[1] >= ub))
+        if final.all():
+            return carry, i + 1
+    return carry, n

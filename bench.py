@@ -351,6 +351,27 @@ def run_ours(args):
     # the grouped online (chunked) variant: 8 and 32 contiguous vocabulary
     # chunks per decode step, each chunk one launch; the step is captured in a
     # CUDA graph and replayed (launches amortized), timed with events
+    def graph_us(step_fn, reps=20):
+        """Capture one step into a CUDA graph, replay it, µs per replay."""
+        with torch.cuda.stream(stream):
+            step_fn()
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            step_fn()
+        for _ in range(3):
+            graph.replay()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        with torch.cuda.stream(stream):
+            for _ in range(reps):
+                graph.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        del graph
+        return e0.elapsed_time(e1) / reps * 1e3
+
     chunked = []
     if not args.no_sweep:
         for b in synthetic.SHAPES["chunked"]["batches"]:
@@ -367,28 +388,56 @@ def run_ours(args):
                         fs.sample_chunked(hd_all[:b], Wd[lo:hi], lo, temp_all[:b],
                                           seed, 5, cm, ci, i == 0, i == n - 1, out=(cids, cmx), stream=stream)
 
-                with torch.cuda.stream(stream):
-                    chunk_step()
-                torch.cuda.synchronize()
-                graph = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(graph, stream=stream):
-                    chunk_step()
-                for _ in range(3):
-                    graph.replay()
-                e0 = torch.cuda.Event(enable_timing=True)
-                e1 = torch.cuda.Event(enable_timing=True)
-                e0.record(stream)
-                with torch.cuda.stream(stream):
-                    for _ in range(20):
-                        graph.replay()
-                e1.record(stream)
-                torch.cuda.synchronize()
-                us = e0.elapsed_time(e1) / 20 * 1e3
+                us = graph_us(chunk_step)
                 rf = roofline(b, d, V, us, peaks)
                 chunked.append({"workload": "chunked", "B": b, "chunks": n, "us_per_step": round(us, 2),
                                 "frac": rf["frac"], "bound": rf["bound"], "path": fs.path_for_batch(b),
                                 "launches_per_step": n, "cuda_graph": True})
-                del graph
+
+    # online early finalization (8 chunks): rows without a dominant winner
+    # ("flat", every chunk runs) and rows with a +200 spike in the first
+    # chunk ("spiked", the later chunks skip their work); the plain chunked
+    # step on the same inputs beside it.  The step includes the h row norms.
+    early = []
+    if not args.no_sweep:
+        n = 8
+        bounds = synthetic.chunk_bounds(V, n)
+        rest = fs.chunk_rest_norms(Wd, bounds, stream=stream)
+        done = torch.zeros(1, dtype=torch.int32, device="cuda")
+        for b in synthetic.SHAPES["chunked"]["batches"]:
+            cm = torch.empty(b, device="cuda")
+            ci = torch.empty(b, dtype=torch.int64, device="cuda")
+            cids = torch.empty(b, dtype=torch.int64, device="cuda")
+            cmx = torch.empty(b, dtype=torch.float32, device="cuda")
+            hn = torch.empty(b, dtype=torch.float32, device="cuda")
+            fs.workspace_reserve(b, V, stream=stream)
+            for kind in ("flat", "spiked"):
+                bias = None
+                if kind == "spiked":
+                    bias = _to_dev(synthetic.leading_spike_bias(b, V, bounds[1], 200.0), torch)
+                chunks = [(lo, hi, None if bias is None else bias[:, lo:hi])
+                          for lo, hi in zip(bounds[:-1], bounds[1:])]
+
+                def early_step():
+                    fs.row_norms(hd_all[:b], out=hn, stream=stream)
+                    for i, (lo, hi, bc) in enumerate(chunks):
+                        fs.sample_chunked_early(hd_all[:b], Wd[lo:hi], lo, temp_all[:b], seed, 5, cm, ci,
+                                                i == 0, i == n - 1, hn, rest[i], 0.0, done, bias_chunk=bc,
+                                                out=(cids, cmx), stream=stream)
+
+                def plain_step():
+                    for i, (lo, hi, bc) in enumerate(chunks):
+                        fs.sample_chunked(hd_all[:b], Wd[lo:hi], lo, temp_all[:b], seed, 5, cm, ci,
+                                          i == 0, i == n - 1, bias_chunk=bc, out=(cids, cmx), stream=stream)
+
+                us_e = graph_us(early_step)
+                done_flag = int(done.item())
+                us_p = graph_us(plain_step)
+                early.append({"workload": "chunked", "inputs": kind, "B": b, "chunks": n,
+                              "early_us_per_step": round(us_e, 2), "chunked_us_per_step": round(us_p, 2),
+                              "done_after_step": done_flag, "path": fs.path_for_batch(b),
+                              "launches_per_step": n + 1, "cuda_graph": True})
+                del chunks, bias
 
     # the unfused comparison pipeline on the same workload: GEMM -> fp32
     # logits in HBM -> softmax -> sample (the traffic fusion removes)
@@ -436,6 +485,7 @@ def run_ours(args):
             "sweep": sweep,
             "unfused": unfused,
             "chunked": chunked,
+            "early_finalization": early,
         }
         if not args.no_cpu_baseline:
             result["cpu_baseline"] = cpu_baseline(B, args.cpu_seconds)

@@ -131,6 +131,59 @@ FS_API fs_status fs_sample_chunked(const void* h, const void* W_chunk, int64_t B
                             int64_t* out_ids, float* out_max, void* stream);
 
 /*
+ * Chunked variant with online early finalization (summary page, "Method",
+ * last paragraph: the streaming sampler may stop once the later tiles can no
+ * longer overtake the running maximum).  Same arguments and result as
+ * fs_sample_chunked, plus:
+ *   h_norms [B] fp32 (device): |h_b| (Euclidean), e.g. from fs_row_norms.
+ *   rest_w_norm: an upper bound on |W_v| for every row v >= v_end of W
+ *     (0 for the last chunk), e.g. from fs_chunk_rest_norms; >= 0.
+ *   rest_bias_max: an upper bound on every bias entry at ids >= v_end
+ *     (0 without bias); +inf disables the early stop.  Not NaN.
+ *   done (device int, caller-owned): reset to 0 by the FS_CHUNK_FIRST call
+ *     (a memset enqueued before its kernel) and written by every call that
+ *     runs; a call that finds *done != 0 on entry reads no W and computes
+ *     nothing (a FS_CHUNK_LAST call still writes out_ids / out_max from the
+ *     carry).
+ * After a call, *done = 1 iff every row is final: its temperature is invalid,
+ * or its carried best perturbed score z* satisfies
+ *     z* >= U + 1e-4 |U| + 1e-3,
+ *     U = (|h_b| rest_w_norm + rest_bias_max) / T_b + 16.6356  (T_b > 0),
+ *     U =  |h_b| rest_w_norm + rest_bias_max                   (T_b == 0),
+ * where 16.6356 bounds the Gumbel value of the largest uniform the noise can
+ * produce, -log(-log(1 - 2^-24)), and the margin covers fp32 rounding.  By
+ * Cauchy-Schwarz no later id can then win, so the result equals that of
+ * fs_sample_chunked bit for bit.  As there, calls after the first are
+ * programmatic dependents of the previous call: a call may read *done before
+ * the previous one has finished and then does the work; a skipping call waits
+ * for the previous one before it ends.  B <= 4096, else FS_ERR_UNSUPPORTED.
+ */
+FS_API fs_status fs_sample_chunked_early(const void* h, const void* W_chunk, int64_t B, int64_t d,
+                                  int64_t v_begin, int64_t v_end, const float* temp,
+                                  const float* bias_chunk, int64_t bias_row_stride,
+                                  uint64_t seed, uint64_t step,
+                                  float* carry_max, int64_t* carry_ids, int flags,
+                                  const float* h_norms, float rest_w_norm, float rest_bias_max, int* done,
+                                  int64_t* out_ids, float* out_max, void* stream);
+
+/*
+ * Euclidean norms of the rows of a bf16 matrix X [n, d] (row-major, device,
+ * 16-byte aligned, d % 8 == 0), accumulated in fp32: out[r] = |X_r| (device,
+ * [n] fp32).  Asynchronous on `stream`.  n == 0 is a no-op.
+ */
+FS_API fs_status fs_row_norms(const void* X, int64_t n, int64_t d, float* out, void* stream);
+
+/*
+ * Setup for fs_sample_chunked_early: for chunks [bounds[i], bounds[i+1]) of W
+ * (bounds: host, n_chunks + 1 non-decreasing entries; W: device, the whole
+ * [bounds[n_chunks], d] matrix), rest_w_norm[i] (host, [n_chunks]) = the
+ * largest row norm of W over rows [bounds[i+1], bounds[n_chunks]), 0 when
+ * empty.  Synchronizes `stream`; allocates and frees a small device buffer.
+ */
+FS_API fs_status fs_chunk_rest_norms(const void* W, int64_t d, const int64_t* bounds, int64_t n_chunks,
+                                     float* rest_w_norm, void* stream);
+
+/*
  * The UNFUSED comparison pipeline (summary page, "Method", ops (1)-(4)):
  * a tensor-core GEMM writes fp32 logits [B, V] (+ bias) to device memory,
  * a softmax kernel reads them and writes probabilities [B, V], and a sample

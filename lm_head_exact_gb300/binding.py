@@ -33,6 +33,12 @@ SIGNATURES = {
     "fs_sample_chunked": (_int, [_c_void_p, _c_void_p, _i64, _i64, _i64, _i64, _c_void_p,
                                  _c_void_p, _i64, _u64, _u64, _c_void_p, _c_void_p, _int,
                                  _c_void_p, _c_void_p, _c_void_p]),
+    "fs_sample_chunked_early": (_int, [_c_void_p, _c_void_p, _i64, _i64, _i64, _i64, _c_void_p,
+                                       _c_void_p, _i64, _u64, _u64, _c_void_p, _c_void_p, _int,
+                                       _c_void_p, ctypes.c_float, ctypes.c_float, _c_void_p,
+                                       _c_void_p, _c_void_p, _c_void_p]),
+    "fs_row_norms": (_int, [_c_void_p, _i64, _i64, _c_void_p, _c_void_p]),
+    "fs_chunk_rest_norms": (_int, [_c_void_p, _i64, _c_void_p, _i64, _c_void_p, _c_void_p]),
     "fs_sample_unfused": (_int, [_c_void_p, _c_void_p, _i64, _i64, _i64, _c_void_p, _c_void_p, _i64,
                                  _u64, _u64, _c_void_p, _c_void_p, _c_void_p, _c_void_p]),
     "fs_sample_host": (_int, [_c_void_p, _c_void_p, _i64, _i64, _i64, _c_void_p, _c_void_p, _i64,
@@ -114,10 +120,13 @@ def _bias_args(bias, B, V):
     if bias is None:
         return ctypes.c_void_p(0), 0
     torch = _torch()
-    ptr = _dev(bias, "bias", torch.float32)
-    if bias.dim() == 1:
-        return ptr, 0
-    return ptr, bias.stride(0)
+    if isinstance(bias, torch.Tensor) and bias.dim() == 2 and bias.stride(1) == 1:
+        # a column slice of a [B, V] bias keeps its row stride
+        if not bias.is_cuda or bias.dtype != torch.float32:
+            raise FlashSampleError("FS_ERR_INVALID_ARG", "bias must be a float32 CUDA tensor (no CPU fallback)")
+        return ctypes.c_void_p(bias.data_ptr()), bias.stride(0)
+    ptr = _dev(bias, "bias", torch.float32, 1)
+    return ptr, 0
 
 
 def _outs(B, device, out):
@@ -189,6 +198,54 @@ def sample_chunked(h, W_chunk, v_begin, temp, seed, step, carry_max, carry_ids, 
         flags, _dev(ids, "out_ids") if last else ctypes.c_void_p(0),
         _dev(mx, "out_max") if last else ctypes.c_void_p(0), _stream_ptr(stream)))
     return (ids, mx) if last else None
+
+
+def sample_chunked_early(h, W_chunk, v_begin, temp, seed, step, carry_max, carry_ids, first, last,
+                         h_norms, rest_w_norm, rest_bias_max, done, bias_chunk=None, out=None, stream=None):
+    """sample_chunked with online early finalization: ``h_norms`` fp32 [B]
+    (row_norms(h)), ``rest_w_norm`` / ``rest_bias_max`` host floats bounding
+    the later chunks, ``done`` a device int32 [1] flag that the first call
+    writes and later calls read (set: they skip their work)."""
+    torch = _torch()
+    B, d = h.shape
+    v_end = v_begin + W_chunk.shape[0]
+    flags = (FS_CHUNK_FIRST if first else 0) | (FS_CHUNK_LAST if last else 0)
+    ids = mx = None
+    if last:
+        ids, mx = _outs(B, h.device, out)
+    bptr, bstride = _bias_args(bias_chunk, B, W_chunk.shape[0])
+    check(library().fs_sample_chunked_early(
+        _dev(h, "h", torch.bfloat16, 2), _dev(W_chunk, "W_chunk", torch.bfloat16, 2), B, d,
+        v_begin, v_end, _dev(temp, "temp", torch.float32, 1), bptr, bstride, seed, step,
+        _dev(carry_max, "carry_max", torch.float32), _dev(carry_ids, "carry_ids", torch.int64),
+        flags, _dev(h_norms, "h_norms", torch.float32, 1), float(rest_w_norm), float(rest_bias_max),
+        _dev(done, "done", torch.int32), _dev(ids, "out_ids") if last else ctypes.c_void_p(0),
+        _dev(mx, "out_max") if last else ctypes.c_void_p(0), _stream_ptr(stream)))
+    return (ids, mx) if last else None
+
+
+def row_norms(X, out=None, stream=None):
+    """fp32 Euclidean norms of the rows of a bf16 [n, d] device matrix."""
+    torch = _torch()
+    n, d = X.shape
+    if out is None:
+        out = torch.empty(n, dtype=torch.float32, device=X.device)
+    check(library().fs_row_norms(_dev(X, "X", torch.bfloat16, 2), n, d, _dev(out, "out", torch.float32, 1),
+                                 _stream_ptr(stream)))
+    return out
+
+
+def chunk_rest_norms(W, bounds, stream=None):
+    """Host list: for chunk i of ``bounds`` (n_chunks + 1 row offsets into W),
+    the largest row norm of W after the chunk (0 for the last).  Synchronizes."""
+    torch = _torch()
+    b = np.ascontiguousarray(np.asarray(bounds, dtype=np.int64))
+    n = len(b) - 1
+    rest = np.zeros(max(n, 0), dtype=np.float32)
+    check(library().fs_chunk_rest_norms(_dev(W, "W", torch.bfloat16, 2), W.shape[1],
+                                        ctypes.c_void_p(b.ctypes.data), n,
+                                        ctypes.c_void_p(rest.ctypes.data), _stream_ptr(stream)))
+    return [float(x) for x in rest]
 
 
 def sample_host(h_host, W, temp_host, seed, step, bias=None, out_ids=None, out_max=None,

@@ -10,6 +10,7 @@
 #include <map>
 #include <mutex>
 #include <utility>
+#include <vector>
 
 #include "flashsample.h"
 #include "fs_internal.h"
@@ -278,6 +279,61 @@ fs_status run(const Problem& p, Finish f, cudaStream_t stream) {
   return FS_OK;
 }
 
+// Early-finalization inputs of one chunk call (all unset: plain chunked call).
+// Rows one early-finalization call handles: one launch of every kernel
+// family, so the done flag is decided by a single last CTA.
+constexpr int kEarlyMaxRows = 4096;
+
+struct EarlyArgs {
+  const float* h_norms = nullptr;
+  float rest_w_norm = 0.0f;
+  float rest_bias_max = 0.0f;
+  int* done = nullptr;
+};
+
+fs_status sample_chunk(const void* h, const void* W_chunk, int64_t B, int64_t d, int64_t v_begin, int64_t v_end,
+                       const float* temp, const float* bias_chunk, int64_t bias_row_stride, uint64_t seed,
+                       uint64_t step, float* carry_max, int64_t* carry_ids, int flags, const EarlyArgs& early,
+                       int64_t* out_ids, float* out_max, void* stream) {
+  if (v_begin < 0 || v_end < v_begin)
+    return fail(FS_ERR_INVALID_ARG, "need 0 <= v_begin <= v_end (got %lld, %lld)",
+                (long long)v_begin, (long long)v_end);
+  if (v_end >= (int64_t(1) << 31)) return fail(FS_ERR_UNSUPPORTED, "v_end must be < 2^31");
+  if (flags & ~(FS_CHUNK_FIRST | FS_CHUNK_LAST)) return fail(FS_ERR_INVALID_ARG, "unknown flags 0x%x", flags);
+  const bool last = (flags & FS_CHUNK_LAST) != 0;
+  Problem p{h, W_chunk, B, d, v_end - v_begin, v_begin, temp, bias_chunk, bias_row_stride, seed, step};
+  // Chunks after the first may start streaming their W rows while the
+  // previous chunk's kernel is still running (programmatic dependent launch);
+  // they wait for it only before merging into the shared carry.
+  p.pdl = (flags & FS_CHUNK_FIRST) == 0;
+  FS_TRY(check_problem(p, last, out_ids, out_max));
+  if (B > 0) {
+    FS_TRY(check_device_ptr(carry_max, "carry_max"));
+    FS_TRY(check_aligned(carry_max, 4, "carry_max"));
+    FS_TRY(check_device_ptr(carry_ids, "carry_ids"));
+    FS_TRY(check_aligned(carry_ids, 8, "carry_ids"));
+  }
+  Finish f{};
+  f.carry_max = carry_max;
+  f.carry_ids = carry_ids;
+  f.carry_in = (flags & FS_CHUNK_FIRST) == 0;
+  f.write_out = last;
+  f.out_ids = out_ids;
+  f.out_max = out_max;
+  f.done = early.done;
+  f.h_norms = early.h_norms;
+  f.temp = temp;
+  f.rest_w_norm = early.rest_w_norm;
+  f.rest_bias_max = early.rest_bias_max;
+  if (early.done != nullptr && (flags & FS_CHUNK_FIRST) != 0) {
+    // reset before the first chunk: a later chunk, launched as a programmatic
+    // dependent, may read the flag before the first chunk finishes
+    cudaError_t e = cudaMemsetAsync(early.done, 0, sizeof(int), static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(done)");
+  }
+  return run(p, f, static_cast<cudaStream_t>(stream));
+}
+
 }  // namespace
 
 void record_error(const char* msg) { snprintf(g_last_error, sizeof(g_last_error), "%s", msg); }
@@ -315,32 +371,90 @@ fs_status fs_sample_chunked(const void* h, const void* W_chunk, int64_t B, int64
                             float* carry_max, int64_t* carry_ids, int flags,
                             int64_t* out_ids, float* out_max, void* stream) {
   g_last_error[0] = '\0';
-  if (v_begin < 0 || v_end < v_begin)
-    return fail(FS_ERR_INVALID_ARG, "need 0 <= v_begin <= v_end (got %lld, %lld)",
-                (long long)v_begin, (long long)v_end);
-  if (v_end >= (int64_t(1) << 31)) return fail(FS_ERR_UNSUPPORTED, "v_end must be < 2^31");
-  if (flags & ~(FS_CHUNK_FIRST | FS_CHUNK_LAST)) return fail(FS_ERR_INVALID_ARG, "unknown flags 0x%x", flags);
-  const bool last = (flags & FS_CHUNK_LAST) != 0;
-  Problem p{h, W_chunk, B, d, v_end - v_begin, v_begin, temp, bias_chunk, bias_row_stride, seed, step};
-  // Chunks after the first may start streaming their W rows while the
-  // previous chunk's kernel is still running (programmatic dependent launch);
-  // they wait for it only before merging into the shared carry.
-  p.pdl = (flags & FS_CHUNK_FIRST) == 0;
-  FS_TRY(check_problem(p, last, out_ids, out_max));
+  return sample_chunk(h, W_chunk, B, d, v_begin, v_end, temp, bias_chunk, bias_row_stride, seed, step, carry_max,
+                      carry_ids, flags, EarlyArgs{}, out_ids, out_max, stream);
+}
+
+fs_status fs_sample_chunked_early(const void* h, const void* W_chunk, int64_t B, int64_t d,
+                                  int64_t v_begin, int64_t v_end, const float* temp,
+                                  const float* bias_chunk, int64_t bias_row_stride,
+                                  uint64_t seed, uint64_t step,
+                                  float* carry_max, int64_t* carry_ids, int flags,
+                                  const float* h_norms, float rest_w_norm, float rest_bias_max, int* done,
+                                  int64_t* out_ids, float* out_max, void* stream) {
+  g_last_error[0] = '\0';
+  if (B > kEarlyMaxRows)
+    return fail(FS_ERR_UNSUPPORTED, "early finalization handles B <= %d (got %lld)", kEarlyMaxRows, (long long)B);
+  if (!(rest_w_norm >= 0.0f)) return fail(FS_ERR_INVALID_ARG, "rest_w_norm must be >= 0 and not NaN");
+  if (rest_bias_max != rest_bias_max) return fail(FS_ERR_INVALID_ARG, "rest_bias_max is NaN");
+  FS_TRY(check_device_ptr(done, "done"));
+  FS_TRY(check_aligned(done, 4, "done"));
   if (B > 0) {
-    FS_TRY(check_device_ptr(carry_max, "carry_max"));
-    FS_TRY(check_aligned(carry_max, 4, "carry_max"));
-    FS_TRY(check_device_ptr(carry_ids, "carry_ids"));
-    FS_TRY(check_aligned(carry_ids, 8, "carry_ids"));
+    FS_TRY(check_device_ptr(h_norms, "h_norms"));
+    FS_TRY(check_aligned(h_norms, 4, "h_norms"));
   }
-  Finish f{};
-  f.carry_max = carry_max;
-  f.carry_ids = carry_ids;
-  f.carry_in = (flags & FS_CHUNK_FIRST) == 0;
-  f.write_out = last;
-  f.out_ids = out_ids;
-  f.out_max = out_max;
-  return run(p, f, static_cast<cudaStream_t>(stream));
+  EarlyArgs early;
+  early.h_norms = h_norms;
+  early.rest_w_norm = rest_w_norm;
+  early.rest_bias_max = rest_bias_max;
+  early.done = done;
+  return sample_chunk(h, W_chunk, B, d, v_begin, v_end, temp, bias_chunk, bias_row_stride, seed, step, carry_max,
+                      carry_ids, flags, early, out_ids, out_max, stream);
+}
+
+fs_status fs_row_norms(const void* X, int64_t n, int64_t d, float* out, void* stream) {
+  g_last_error[0] = '\0';
+  FS_TRY(check_shapes(0, d, n));
+  if (n == 0) return FS_OK;
+  FS_TRY(check_device_ptr(X, "X"));
+  FS_TRY(check_aligned(X, 16, "X"));
+  FS_TRY(check_device_ptr(out, "out"));
+  FS_TRY(check_aligned(out, 4, "out"));
+  cudaError_t e = launch_row_norms(X, n, d, out, nullptr, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "row-norm kernel launch");
+  return FS_OK;
+}
+
+fs_status fs_chunk_rest_norms(const void* W, int64_t d, const int64_t* bounds, int64_t n_chunks,
+                              float* rest_w_norm, void* stream_) {
+  g_last_error[0] = '\0';
+  if (n_chunks < 0) return fail(FS_ERR_INVALID_ARG, "n_chunks must be >= 0");
+  if (n_chunks == 0) return FS_OK;
+  if (bounds == nullptr || rest_w_norm == nullptr) return fail(FS_ERR_INVALID_ARG, "bounds / rest_w_norm is NULL");
+  if (bounds[0] < 0) return fail(FS_ERR_INVALID_ARG, "bounds[0] must be >= 0");
+  for (int64_t i = 0; i < n_chunks; ++i)
+    if (bounds[i + 1] < bounds[i]) return fail(FS_ERR_INVALID_ARG, "bounds must be non-decreasing");
+  FS_TRY(check_shapes(0, d, bounds[n_chunks]));
+  if (bounds[n_chunks] > bounds[0]) {
+    FS_TRY(check_device_ptr(W, "W"));
+    FS_TRY(check_aligned(W, 16, "W"));
+  }
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  unsigned* seg = nullptr;
+  cudaError_t e = cudaMalloc(&seg, static_cast<size_t>(n_chunks) * sizeof(unsigned));
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(FS_ERR_WORKSPACE, "chunk maxima of %lld floats", (long long)n_chunks);
+  }
+  std::vector<unsigned> host(static_cast<size_t>(n_chunks), 0u);
+  e = cudaMemsetAsync(seg, 0, static_cast<size_t>(n_chunks) * sizeof(unsigned), stream);
+  for (int64_t i = 0; i < n_chunks && e == cudaSuccess; ++i)
+    e = launch_row_norms(static_cast<const char*>(W) + bounds[i] * d * 2, bounds[i + 1] - bounds[i], d, nullptr,
+                         seg + i, stream);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(host.data(), seg, static_cast<size_t>(n_chunks) * sizeof(unsigned), cudaMemcpyDeviceToHost,
+                        stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  cudaFree(seg);
+  if (e != cudaSuccess) return cuda_fail(e, "chunk row norms");
+  float rest = 0.0f;      // rows after the last chunk: none
+  for (int64_t i = n_chunks - 1; i >= 0; --i) {
+    rest_w_norm[i] = rest;
+    float m;
+    memcpy(&m, &host[static_cast<size_t>(i)], sizeof(m));
+    rest = std::max(rest, m);
+  }
+  return FS_OK;
 }
 
 fs_status fs_sample_host(const void* h_host, const void* W, int64_t B, int64_t d, int64_t V,

@@ -16,8 +16,25 @@
 
 namespace fs {
 
-// Final best of row b -> carry (chunked variant) and outputs.
-__device__ __forceinline__ void write_row(const Finish& f, int64_t b, Best best) {
+// Largest Gumbel value the uniform grid can produce, -log(-log(1 - 2^-24)) =
+// 16.63553..., rounded up.
+constexpr float kGumbelMax = 16.6356f;
+
+// Row b can no longer be overtaken by the later chunks: its best perturbed
+// score is at least their upper bound (Cauchy-Schwarz on the logit, the
+// largest bias, the largest Gumbel value), with a margin for fp32 rounding.
+__device__ __forceinline__ bool row_final(const Finish& f, int64_t b, Best best) {
+  const RowTemp rt = row_temp(f.temp[b]);
+  if (rt.mode == kRowInvalid) return true;
+  if (best.id == kNoId) return false;
+  const float lim = f.h_norms[b] * f.rest_w_norm + f.rest_bias_max;
+  const float ub = rt.mode == kRowGreedy ? lim : fmaf(lim, rt.inv_t, kGumbelMax);
+  return best.z >= ub + 1e-4f * fabsf(ub) + 1e-3f;
+}
+
+// Final best of row b -> carry (chunked variant) and outputs; returns the
+// merged best.
+__device__ __forceinline__ Best write_row(const Finish& f, int64_t b, Best best) {
   if (f.carry_max != nullptr) {
     if (f.carry_in) {
       const int64_t cid = f.carry_ids[b];
@@ -35,6 +52,30 @@ __device__ __forceinline__ void write_row(const Finish& f, int64_t b, Best best)
     f.out_ids[b] = best.id == kNoId ? -1 : static_cast<int64_t>(best.id);
     f.out_max[b] = best.id == kNoId ? -INFINITY : best.z;
   }
+  return best;
+}
+
+// Early finalization: a chunk after the first whose *done flag is set on
+// entry skips all of its work.  The flag was reset before the first chunk
+// and is only ever set within the step by a chunk that finished, after its
+// carry writes, so a stale 0 merely costs work and a 1 is always valid for
+// every later chunk.  With a programmatic dependent launch the previous
+// chunk may still be running: CTA 0 then waits for it, so that this grid
+// ends after it (the next chunk's wait covers both) and, on the last chunk,
+// writes the outputs from the complete carry.  Called by every thread at
+// kernel entry, before any barrier or TMEM allocation; returns true when
+// the CTA should exit.
+__device__ __forceinline__ bool early_skip(const Finish& f, int64_t B, bool pdl) {
+  if (f.done == nullptr || !f.carry_in) return false;
+  int done;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(done) : "l"(f.done) : "memory");
+  if (done == 0) return false;
+  if (blockIdx.x == 0 && blockIdx.y == 0) {
+    if (pdl) pdl_wait();
+    if (f.write_out)
+      for (int64_t b = threadIdx.x; b < B; b += blockDim.x) write_row(f, b, best_none());
+  }
+  return true;
 }
 
 __device__ __forceinline__ void push_candidate(const Finish& f, int64_t b, Best c) {
@@ -56,7 +97,22 @@ __device__ __forceinline__ void finish_grid(const Finish& f, int64_t B, int tid,
   bar();
   if (*flag) {
     __threadfence();
-    for (int64_t b = tid; b < B; b += n) write_row(f, b, unpack_key(atomicExch(f.keys + b, 0ull)));
+    bool all_final = true;
+    for (int64_t b = tid; b < B; b += n) {
+      const Best best = write_row(f, b, unpack_key(atomicExch(f.keys + b, 0ull)));
+      if (f.done != nullptr) all_final = all_final && row_final(f, b, best);
+    }
+    if (f.done != nullptr) {
+      bar();                                   // every thread has read *flag
+      if (tid == 0) *flag = 1;
+      bar();
+      if (!all_final) *flag = 0;
+      bar();
+      if (tid == 0) {
+        __threadfence();                       // carry writes of this CTA before the flag
+        *f.done = *flag;
+      }
+    }
     if (tid == 0) atomicExch(f.counter, 0u);
   }
 }

@@ -70,6 +70,15 @@ struct Finish {
   bool write_out;         // write out_ids / out_max (last chunk or one-shot)
   int64_t* out_ids;
   float* out_max;
+  // Early finalization of the chunked variant (nullable `done`): a chunk
+  // whose *done is set on entry does no work; the last CTA of a chunk that
+  // ran sets *done when no row can be overtaken by the later chunks, whose
+  // rows have norms <= rest_w_norm and biases <= rest_bias_max.
+  int* done = nullptr;
+  const float* h_norms = nullptr;   // [B] Euclidean norms of the rows of h
+  const float* temp = nullptr;      // [B]
+  float rest_w_norm = 0.0f;
+  float rest_bias_max = 0.0f;
 };
 
 // Kernel families selectable by batch size (or forced for tests).
@@ -102,6 +111,11 @@ cudaError_t launch_unfused_tail(const Problem& p, float* logits, float* probs, i
 cudaError_t launch_debug_wait(int* err, uint64_t timeout_ns, cudaStream_t stream);
 
 // Reduction kernel over `f.partials` (used when no fused kernel runs: V == 0).
+// Row norms |X_r| of a bf16 [n, d] matrix into out (nullable) and their
+// maximum as fp32 bits into *seg_max (nullable, atomicMax; zero it first).
+cudaError_t launch_row_norms(const void* X, int64_t n, int64_t d, float* out, unsigned* seg_max,
+                             cudaStream_t stream);
+
 cudaError_t launch_reduce(const Finish& f, int64_t B, cudaStream_t stream);
 
 // Set the calling thread's fs_last_error() text.

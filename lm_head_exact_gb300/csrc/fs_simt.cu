@@ -47,6 +47,7 @@ simt_fused_kernel(Problem p, Finish f) {
   extern __shared__ uint4 smem_h[];            // [BG][d/8] bf16x8 packets
   __shared__ Best warp_best[kSimtWarps][BG];
   __shared__ int last_flag;
+  if (early_skip(f, p.B, p.pdl)) return;
   const int n_parts = gridDim.x;
   pdl_launch_dependents();
 

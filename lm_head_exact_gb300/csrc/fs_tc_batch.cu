@@ -78,6 +78,7 @@ template <bool kStoreLogits>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_batch_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_constant__ CUtensorMap tmap_w,
                 const BatchArgs args) {
+  if (!kStoreLogits && early_skip(args.f, args.p.B, args.p.pdl)) return;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + kOffBars);

@@ -88,6 +88,7 @@ __global__ void __launch_bounds__(kThreads, VocabCfg<BN>::kCtasPerSm)
 tc_vocab_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_h,
                 const VocabArgs args) {
   using C = VocabCfg<BN>;
+  if (early_skip(args.f, args.p.B, args.p.pdl)) return;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + C::kOffBars);

@@ -137,6 +137,18 @@ def spike_bias(B, V, n_spikes=16, height=8.0):
     return bias
 
 
+def leading_spike_bias(B, V, v_hi, height, rows=None):
+    """Dense fp32 [B, V] bias for the early-finalization cases: one +height
+    spike per selected row (all rows by default) at a random id below v_hi
+    (seed 3), zero elsewhere -- rows whose winner sits in the first chunk."""
+    g = np.random.Generator(np.random.SFC64(SEED_BIAS))
+    bias = np.zeros((B, V), dtype=np.float32)
+    ids = g.integers(0, v_hi, size=B)
+    for b in (range(B) if rows is None else rows):
+        bias[b, ids[b]] = np.float32(height)
+    return bias
+
+
 _W_CACHE = {}
 
 

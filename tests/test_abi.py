@@ -65,6 +65,20 @@ def test_host_side_argument_checks(built_library):
     assert lib.fs_sample_chunked(z, z, 4, 64, 10, 5, z, z, 0, 0, 0, z, z, 1, z, z, z) == 1
     assert lib.fs_sample_chunked(z, z, 4, 64, 0, 5, z, z, 0, 0, 0, z, z, 8, z, z, z) == 1
     assert lib.fs_set_path(7) == 1
+    # early finalization: batch limit, NaN bounds, bad chunk bounds
+    assert lib.fs_sample_chunked_early(z, z, 4097, 64, 0, 5, z, z, 0, 0, 0, z, z, 1, z, 0.0, 0.0, z, z, z, z) == 2
+    assert "B <= 4096" in lib.fs_last_error().decode()
+    nan = float("nan")
+    assert lib.fs_sample_chunked_early(z, z, 4, 64, 0, 5, z, z, 0, 0, 0, z, z, 1, z, nan, 0.0, z, z, z, z) == 1
+    assert lib.fs_sample_chunked_early(z, z, 4, 64, 0, 5, z, z, 0, 0, 0, z, z, 1, z, -1.0, 0.0, z, z, z, z) == 1
+    assert lib.fs_sample_chunked_early(z, z, 4, 64, 0, 5, z, z, 0, 0, 0, z, z, 1, z, 1.0, nan, z, z, z, z) == 1
+    bounds = (ctypes.c_int64 * 3)(0, 10, 5)
+    rest = (ctypes.c_float * 2)()
+    assert lib.fs_chunk_rest_norms(z, 64, bounds, 2, rest, z) == 1
+    assert "non-decreasing" in lib.fs_last_error().decode()
+    assert lib.fs_chunk_rest_norms(z, 64, z, 0, z, z) == 0
+    assert lib.fs_row_norms(z, 0, 64, z, z) == 0
+    assert lib.fs_row_norms(z, 3, 12, z, z) == 2
     assert lib.fs_debug_noise(0, 0, -1, 1, 0, 1, z, z, z) == 1
     # B == 0 is a no-op
     assert lib.fs_sample(z, z, 0, 64, 10, z, 0, 0, z, z, z) == 0

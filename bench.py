@@ -418,12 +418,12 @@ def run_ours(args):
                 chunks = [(lo, hi, None if bias is None else bias[:, lo:hi])
                           for lo, hi in zip(bounds[:-1], bounds[1:])]
 
-                def early_step():
+                def early_step(serial=False):
                     fs.row_norms(hd_all[:b], out=hn, stream=stream)
                     for i, (lo, hi, bc) in enumerate(chunks):
                         fs.sample_chunked_early(hd_all[:b], Wd[lo:hi], lo, temp_all[:b], seed, 5, cm, ci,
                                                 i == 0, i == n - 1, hn, rest[i], 0.0, done, bias_chunk=bc,
-                                                out=(cids, cmx), stream=stream)
+                                                out=(cids, cmx), stream=stream, serial=serial)
 
                 def plain_step():
                     for i, (lo, hi, bc) in enumerate(chunks):
@@ -432,9 +432,11 @@ def run_ours(args):
 
                 us_e = graph_us(early_step)
                 done_flag = int(done.item())
+                us_s = graph_us(lambda: early_step(serial=True))
                 us_p = graph_us(plain_step)
                 early.append({"workload": "chunked", "inputs": kind, "B": b, "chunks": n,
-                              "early_us_per_step": round(us_e, 2), "chunked_us_per_step": round(us_p, 2),
+                              "early_us_per_step": round(us_e, 2), "early_serial_us_per_step": round(us_s, 2),
+                              "chunked_us_per_step": round(us_p, 2),
                               "done_after_step": done_flag, "path": fs.path_for_batch(b),
                               "launches_per_step": n + 1, "cuda_graph": True})
                 del chunks, bias

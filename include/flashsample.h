@@ -72,6 +72,7 @@ typedef enum fs_status {
 /* Flags of fs_sample_chunked. */
 #define FS_CHUNK_FIRST 1      /* ignore the incoming carry: this chunk starts the row */
 #define FS_CHUNK_LAST 2       /* write out_ids / out_max after merging this chunk */
+#define FS_CHUNK_SERIAL 4     /* start only after the previous call has finished (no overlap) */
 
 /* Kernel families (fs_set_path). */
 #define FS_PATH_AUTO 0        /* chosen from the batch size B only */
@@ -119,7 +120,8 @@ FS_API fs_status fs_sample_ex(const void* h, const void* W, int64_t B, int64_t d
  *     v_begin + j at bias_chunk[b * bias_row_stride + j]) or NULL.
  *   carry_max [B] fp32 and carry_ids [B] int64 (device, caller-owned):
  *     read unless FS_CHUNK_FIRST, always updated (ids -1 = none yet).
- *   flags: FS_CHUNK_FIRST and/or FS_CHUNK_LAST.  With FS_CHUNK_LAST,
+ *   flags: FS_CHUNK_FIRST and/or FS_CHUNK_LAST, optionally FS_CHUNK_SERIAL
+ *     (launch without the programmatic dependency).  With FS_CHUNK_LAST,
  *     out_ids / out_max are written (they may alias the carry arrays' roles
  *     but not their memory); otherwise they may be NULL.
  */
@@ -156,7 +158,11 @@ FS_API fs_status fs_sample_chunked(const void* h, const void* W_chunk, int64_t B
  * fs_sample_chunked bit for bit.  As there, calls after the first are
  * programmatic dependents of the previous call: a call may read *done before
  * the previous one has finished and then does the work; a skipping call waits
- * for the previous one before it ends.  B <= 4096, else FS_ERR_UNSUPPORTED.
+ * for the previous one before it ends.  With FS_CHUNK_SERIAL a call starts
+ * only after the previous one has finished and so always sees its flag: the
+ * better choice when rows are expected to be final early (peaked
+ * distributions), at the cost of the overlap between chunks when they are
+ * not.  B <= 4096, else FS_ERR_UNSUPPORTED.
  */
 FS_API fs_status fs_sample_chunked_early(const void* h, const void* W_chunk, int64_t B, int64_t d,
                                   int64_t v_begin, int64_t v_end, const float* temp,

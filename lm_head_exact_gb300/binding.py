@@ -17,6 +17,7 @@ LIB_PATH = os.path.join(_PKG, "libflashsample.so")
 FS_OK = 0
 FS_CHUNK_FIRST = 1
 FS_CHUNK_LAST = 2
+FS_CHUNK_SERIAL = 4
 FS_PATH_AUTO, FS_PATH_SIMT, FS_PATH_TC_VOCAB, FS_PATH_TC_BATCH, FS_PATH_TC_PAIR = 0, 1, 2, 3, 4
 
 _c_void_p = ctypes.c_void_p
@@ -179,14 +180,14 @@ def sample_ex(*args, **kwargs):
 
 
 def sample_chunked(h, W_chunk, v_begin, temp, seed, step, carry_max, carry_ids, first, last,
-                   bias_chunk=None, out=None, stream=None):
+                   bias_chunk=None, out=None, stream=None, serial=False):
     """One chunk [v_begin, v_begin + W_chunk.shape[0]) of the grouped online
     variant; updates (carry_max, carry_ids) in place and, when ``last``,
     returns (ids, max)."""
     torch = _torch()
     B, d = h.shape
     v_end = v_begin + W_chunk.shape[0]
-    flags = (FS_CHUNK_FIRST if first else 0) | (FS_CHUNK_LAST if last else 0)
+    flags = (FS_CHUNK_FIRST if first else 0) | (FS_CHUNK_LAST if last else 0) | (FS_CHUNK_SERIAL if serial else 0)
     ids = mx = None
     if last:
         ids, mx = _outs(B, h.device, out)
@@ -201,15 +202,17 @@ def sample_chunked(h, W_chunk, v_begin, temp, seed, step, carry_max, carry_ids, 
 
 
 def sample_chunked_early(h, W_chunk, v_begin, temp, seed, step, carry_max, carry_ids, first, last,
-                         h_norms, rest_w_norm, rest_bias_max, done, bias_chunk=None, out=None, stream=None):
+                         h_norms, rest_w_norm, rest_bias_max, done, bias_chunk=None, out=None, stream=None,
+                         serial=False):
     """sample_chunked with online early finalization: ``h_norms`` fp32 [B]
     (row_norms(h)), ``rest_w_norm`` / ``rest_bias_max`` host floats bounding
     the later chunks, ``done`` a device int32 [1] flag that the first call
-    writes and later calls read (set: they skip their work)."""
+    writes and later calls read (set: they skip their work).  ``serial``
+    launches the call without overlapping the previous one."""
     torch = _torch()
     B, d = h.shape
     v_end = v_begin + W_chunk.shape[0]
-    flags = (FS_CHUNK_FIRST if first else 0) | (FS_CHUNK_LAST if last else 0)
+    flags = (FS_CHUNK_FIRST if first else 0) | (FS_CHUNK_LAST if last else 0) | (FS_CHUNK_SERIAL if serial else 0)
     ids = mx = None
     if last:
         ids, mx = _outs(B, h.device, out)

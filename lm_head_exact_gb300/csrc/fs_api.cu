@@ -299,13 +299,14 @@ fs_status sample_chunk(const void* h, const void* W_chunk, int64_t B, int64_t d,
     return fail(FS_ERR_INVALID_ARG, "need 0 <= v_begin <= v_end (got %lld, %lld)",
                 (long long)v_begin, (long long)v_end);
   if (v_end >= (int64_t(1) << 31)) return fail(FS_ERR_UNSUPPORTED, "v_end must be < 2^31");
-  if (flags & ~(FS_CHUNK_FIRST | FS_CHUNK_LAST)) return fail(FS_ERR_INVALID_ARG, "unknown flags 0x%x", flags);
+  if (flags & ~(FS_CHUNK_FIRST | FS_CHUNK_LAST | FS_CHUNK_SERIAL))
+    return fail(FS_ERR_INVALID_ARG, "unknown flags 0x%x", flags);
   const bool last = (flags & FS_CHUNK_LAST) != 0;
   Problem p{h, W_chunk, B, d, v_end - v_begin, v_begin, temp, bias_chunk, bias_row_stride, seed, step};
   // Chunks after the first may start streaming their W rows while the
   // previous chunk's kernel is still running (programmatic dependent launch);
   // they wait for it only before merging into the shared carry.
-  p.pdl = (flags & FS_CHUNK_FIRST) == 0;
+  p.pdl = (flags & (FS_CHUNK_FIRST | FS_CHUNK_SERIAL)) == 0;
   FS_TRY(check_problem(p, last, out_ids, out_max));
   if (B > 0) {
     FS_TRY(check_device_ptr(carry_max, "carry_max"));

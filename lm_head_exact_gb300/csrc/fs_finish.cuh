@@ -55,29 +55,6 @@ __device__ __forceinline__ Best write_row(const Finish& f, int64_t b, Best best)
   return best;
 }
 
-// Early finalization: a chunk after the first whose *done flag is set on
-// entry skips all of its work.  The flag was reset before the first chunk
-// and is only ever set within the step by a chunk that finished, after its
-// carry writes, so a stale 0 merely costs work and a 1 is always valid for
-// every later chunk.  With a programmatic dependent launch the previous
-// chunk may still be running: CTA 0 then waits for it, so that this grid
-// ends after it (the next chunk's wait covers both) and, on the last chunk,
-// writes the outputs from the complete carry.  Called by every thread at
-// kernel entry, before any barrier or TMEM allocation; returns true when
-// the CTA should exit.
-__device__ __forceinline__ bool early_skip(const Finish& f, int64_t B, bool pdl) {
-  if (f.done == nullptr || !f.carry_in) return false;
-  int done;
-  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(done) : "l"(f.done) : "memory");
-  if (done == 0) return false;
-  if (blockIdx.x == 0 && blockIdx.y == 0) {
-    if (pdl) pdl_wait();
-    if (f.write_out)
-      for (int64_t b = threadIdx.x; b < B; b += blockDim.x) write_row(f, b, best_none());
-  }
-  return true;
-}
-
 __device__ __forceinline__ void push_candidate(const Finish& f, int64_t b, Best c) {
   if (c.id != kNoId) atomicMax(f.keys + b, pack_key(c.z, c.id));
 }
@@ -115,6 +92,40 @@ __device__ __forceinline__ void finish_grid(const Finish& f, int64_t B, int tid,
     }
     if (tid == 0) atomicExch(f.counter, 0u);
   }
+}
+
+// Early finalization: the *done flag of a chunk after the first, read at
+// kernel entry.  The flag was reset before the first chunk and is only ever
+// set within the step, by a finished chunk after its carry writes, so a 1 is
+// valid for every later chunk.  With a programmatic dependent launch the
+// previous chunk may set it while this grid's CTAs start, so different CTAs
+// of one grid may read different values: every CTA must stay correct alone.
+__device__ __forceinline__ bool early_done(const Finish& f) {
+  if (f.done == nullptr || !f.carry_in) return false;
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(f.done) : "memory");
+  return v != 0;
+}
+
+// The same, taken once per CTA: thread 0 reads the flag and every thread of
+// the CTA gets its value through `slot` (a shared-memory int).  Called by all
+// threads.
+__device__ __forceinline__ bool early_done_cta(const Finish& f, int* slot) {
+  if (f.done == nullptr || !f.carry_in) return false;
+  if (threadIdx.x == 0) *slot = early_done(f) ? 1 : 0;
+  __syncthreads();
+  return *slot != 0;
+}
+
+// A CTA that saw the flag set loads and computes nothing but still takes its
+// ticket in the cross-CTA finish (with no candidate), so that the grid's last
+// CTA -- whichever it is -- merges the carry and writes the flag and, on the
+// last chunk, the outputs.  Called by all threads of the CTA before any
+// warp-role split; `flag` is a shared-memory int.
+__device__ __forceinline__ void early_skip_cta(const Finish& f, int64_t B, bool pdl, int* flag) {
+  pdl_launch_dependents();
+  if (pdl) pdl_wait();                         // the finish area is shared with the previous launch
+  finish_grid(f, B, threadIdx.x, blockDim.x, flag, [] { __syncthreads(); });
 }
 
 }  // namespace fs

@@ -47,7 +47,10 @@ simt_fused_kernel(Problem p, Finish f) {
   extern __shared__ uint4 smem_h[];            // [BG][d/8] bf16x8 packets
   __shared__ Best warp_best[kSimtWarps][BG];
   __shared__ int last_flag;
-  if (early_skip(f, p.B, p.pdl)) return;
+  if (early_done_cta(f, &last_flag)) {
+    early_skip_cta(f, p.B, p.pdl, &last_flag);
+    return;
+  }
   const int n_parts = gridDim.x;
   pdl_launch_dependents();
 

@@ -78,7 +78,6 @@ template <bool kStoreLogits>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_batch_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_constant__ CUtensorMap tmap_w,
                 const BatchArgs args) {
-  if (!kStoreLogits && early_skip(args.f, args.p.B, args.p.pdl)) return;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + kOffBars);
@@ -89,6 +88,10 @@ tc_batch_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_constan
   uint32_t* tmem_base_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
   int* last_flag = reinterpret_cast<int*>(smem + kOffMisc + 8);
+  if (!kStoreLogits && early_done_cta(args.f, last_flag)) {
+    early_skip_cta(args.f, args.p.B, args.p.pdl, last_flag);
+    return;
+  }
   Best* half_best = reinterpret_cast<Best*>(smem + kOffHalf);
 
   const Problem& p = args.p;

@@ -68,7 +68,6 @@ struct PairArgs {
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_constant__ CUtensorMap tmap_w,
                const PairArgs args) {
-  if (early_skip(args.f, args.p.B, args.p.pdl)) return;     // the same for both CTAs of a pair
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + kOffBars);   // used in the even CTA
@@ -80,6 +79,22 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_constant
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
   int* last_flag = reinterpret_cast<int*>(smem + kOffMisc + 8);
   Best* half_best = reinterpret_cast<Best*>(smem + kOffHalf);
+  if (args.f.done != nullptr && args.f.carry_in) {
+    // Early finalization: the two CTAs of a pair must take the same decision
+    // (the running one would otherwise signal a peer that has left), so the
+    // even CTA reads the flag once and stores it into both CTAs.
+    cluster_sync();                                     // both CTAs have started: their shared memory is live
+    if (cluster_ctarank() == 0 && threadIdx.x == 0) {
+      const int skip = early_done(args.f) ? 1 : 0;
+      *last_flag = skip;
+      st_shared_cluster_u32(mapa_shared(smem_u32(last_flag), 1), static_cast<uint32_t>(skip));
+    }
+    cluster_sync();
+    if (*last_flag != 0) {
+      early_skip_cta(args.f, args.p.B, args.p.pdl, last_flag);
+      return;
+    }
+  }
 
   const Problem& p = args.p;
   const int warp = threadIdx.x >> 5;

@@ -88,7 +88,6 @@ __global__ void __launch_bounds__(kThreads, VocabCfg<BN>::kCtasPerSm)
 tc_vocab_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_h,
                 const VocabArgs args) {
   using C = VocabCfg<BN>;
-  if (early_skip(args.f, args.p.B, args.p.pdl)) return;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + C::kOffBars);
@@ -99,6 +98,10 @@ tc_vocab_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
   uint32_t* tmem_base_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
   int* last_flag = reinterpret_cast<int*>(smem + C::kOffMisc + 8);
+  if (early_done_cta(args.f, last_flag)) {
+    early_skip_cta(args.f, args.p.B, args.p.pdl, last_flag);
+    return;
+  }
   float* col_inv_t = reinterpret_cast<float*>(smem + C::kOffInvT);
   int* col_mode = reinterpret_cast<int*>(smem + C::kOffMode);
   Best* warp_best = reinterpret_cast<Best*>(smem + C::kOffBest);   // [kEpiWarps][BN]

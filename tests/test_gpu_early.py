@@ -36,7 +36,7 @@ def _problem(B, V, d, seed, w_std=0.05):
     return h, W, temps
 
 
-def _run_early(fs, torch, hd, Wd, td, bd, bounds, seed, step, rest, rest_bias):
+def _run_early(fs, torch, hd, Wd, td, bd, bounds, seed, step, rest, rest_bias, serial=False):
     """All chunk calls in order; returns (ids, max, done after each call)."""
     B = hd.shape[0]
     cm = torch.empty(B, device="cuda")
@@ -49,8 +49,7 @@ def _run_early(fs, torch, hd, Wd, td, bd, bounds, seed, step, rest, rest_bias):
     for i, (lo, hi) in enumerate(zip(bounds[:-1], bounds[1:])):
         bc = None if bd is None else bd[:, lo:hi]
         res = fs.sample_chunked_early(hd, Wd[lo:hi], lo, td, seed, step, cm, ci, i == 0, i == n - 1,
-                                      hn, rest[i], rest_bias[i], done,
-                                      bias_chunk=None if bc is None else bc.contiguous())
+                                      hn, rest[i], rest_bias[i], done, bias_chunk=bc, serial=serial)
         torch.cuda.synchronize()
         flags.append(int(done.item()))
     return res[0].cpu().numpy(), res[1].cpu().numpy(), flags
@@ -96,8 +95,9 @@ def test_chunk_rest_norms_match_oracle(fs, torch_cuda, bounds):
 
 
 # ------------------------------------------------------------------ small cases, every kernel family
+@pytest.mark.parametrize("serial", [False, True])
 @pytest.mark.parametrize("kind", ["spiked", "flat", "mixed"])
-def test_early_small_matches_oracle(fs, torch_cuda, path, kind):
+def test_early_small_matches_oracle(fs, torch_cuda, path, kind, serial):
     torch = torch_cuda
     B, V, d, n = 37, 4099, 256, 8
     h, W, temp = _problem(B, V, d, seed=21)
@@ -110,7 +110,7 @@ def test_early_small_matches_oracle(fs, torch_cuda, path, kind):
     hd, Wd, td = to_device(h, torch), to_device(W, torch), to_device(temp, torch)
     bd = None if bias is None else to_device(bias, torch)
     rest = fs.chunk_rest_norms(Wd, bounds)
-    ids, mx, flags = _run_early(fs, torch, hd, Wd, td, bd, bounds, 9, 2, rest, _rest_bias(bias, bounds))
+    ids, mx, flags = _run_early(fs, torch, hd, Wd, td, bd, bounds, 9, 2, rest, _rest_bias(bias, bounds), serial)
     ids_c, mx_c = _run_chunked(fs, torch, hd, Wd, td, bd, bounds, 9, 2)
     np.testing.assert_array_equal(ids, ids_c)
     np.testing.assert_array_equal(mx, mx_c)
@@ -164,8 +164,9 @@ def test_early_full_size_spiked_and_flat(fs, torch_cuda, B):
         assert flags == ([1] * 8 if kind == "spiked" else [0] * 7 + flags[-1:]), flags
 
 
+@pytest.mark.parametrize("serial", [False, True])
 @pytest.mark.parametrize("B", [1, 32, 256])
-def test_early_graph_replays_do_not_leak_the_flag(fs, torch_cuda, B):
+def test_early_graph_replays_do_not_leak_the_flag(fs, torch_cuda, B, serial):
     """One captured step of 32 chunks (programmatic dependent launches),
     replayed with a +400 spike in chunk 3 of every row (the chunks after it
     skip), then with the bias zeroed (no row is final): a flag left set by
@@ -195,7 +196,7 @@ def test_early_graph_replays_do_not_leak_the_flag(fs, torch_cuda, B):
         fs.row_norms(hd, out=hn, stream=stream)
         for i, (lo, hi) in enumerate(chunks):
             fs.sample_chunked_early(hd, Wd[lo:hi], lo, td, 3, 8, cm, ci, i == 0, i == n - 1, hn, rest[i], 0.0,
-                                    done, bias_chunk=bd[:, lo:hi], out=(ids, mx), stream=stream)
+                                    done, bias_chunk=bd[:, lo:hi], out=(ids, mx), stream=stream, serial=serial)
 
     with torch.cuda.stream(stream):
         step()
@@ -216,4 +217,60 @@ def test_early_graph_replays_do_not_leak_the_flag(fs, torch_cuda, B):
         if spiked:
             assert flag == 1
     compare(ids.cpu().numpy(), mx.cpu().numpy(), sampler.sample(h, W, temp, 3, 8), what=f"early graph B={B}")
+    del graph
+
+
+@pytest.mark.parametrize("B", [1, 32, 256])
+def test_early_overlapped_chunks_stress(fs, torch_cuda, B):
+    """With overlapped (programmatic dependent) launches the CTAs of one chunk
+    may start on either side of the previous chunk's flag write, so some may
+    skip and others run.  Full-size head in 32 chunks, winners planted in
+    chunk 3: 40 graph replays with the spikes and 10 without must each equal
+    the one-shot sample bit for bit and leave no device error."""
+    torch = torch_cuda
+    wl = synthetic.workload("chunked", B)
+    V, n = wl.W.shape[0], 32
+    bounds = synthetic.chunk_bounds(V, n)
+    spikes = np.zeros((B, V), np.float32)
+    g = np.random.default_rng(7 + B)
+    spikes[np.arange(B), g.integers(bounds[3], bounds[4], size=B)] = 200.0
+    hd, Wd, td = to_device(wl.h, torch), to_device(wl.W, torch), to_device(wl.temp, torch)
+    bd = to_device(spikes, torch)
+    rest = fs.chunk_rest_norms(Wd, bounds)
+    stream = torch.cuda.Stream()
+    fs.workspace_reserve(B, V, stream=stream)
+    cm = torch.empty(B, device="cuda")
+    ci = torch.empty(B, dtype=torch.int64, device="cuda")
+    ids = torch.empty(B, dtype=torch.int64, device="cuda")
+    mx = torch.empty(B, dtype=torch.float32, device="cuda")
+    hn = torch.empty(B, dtype=torch.float32, device="cuda")
+    done = torch.zeros(1, dtype=torch.int32, device="cuda")
+
+    def step():
+        fs.row_norms(hd, out=hn, stream=stream)
+        for i, (lo, hi) in enumerate(zip(bounds[:-1], bounds[1:])):
+            fs.sample_chunked_early(hd, Wd[lo:hi], lo, td, wl.seed, 2, cm, ci, i == 0, i == n - 1, hn, rest[i],
+                                    0.0, done, bias_chunk=bd[:, lo:hi], out=(ids, mx), stream=stream)
+
+    with torch.cuda.stream(stream):
+        step()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        step()
+    for spiked, reps in ((True, 40), (False, 10)):
+        if not spiked:
+            bd.zero_()
+        one_ids, one_mx = fs.sample(hd, Wd, td, wl.seed, 2, bias=bd)
+        torch.cuda.synchronize()
+        want_ids, want_mx = one_ids.cpu().numpy(), one_mx.cpu().numpy()
+        for _ in range(reps):
+            ids.fill_(-7)
+            graph.replay()
+            torch.cuda.synchronize()
+            np.testing.assert_array_equal(ids.cpu().numpy(), want_ids)
+            np.testing.assert_array_equal(mx.cpu().numpy(), want_mx)
+        if spiked:
+            assert int(done.item()) == 1
+    assert fs.device_error() == 0
     del graph

@@ -62,8 +62,10 @@ __device__ __forceinline__ void push_candidate(const Finish& f, int64_t b, Best 
 // Called by the n participating threads (index tid) of every CTA after they
 // pushed all of this CTA's candidates.  `bar()` synchronizes exactly those
 // threads; `flag` is a shared-memory int.  The last CTA of the grid writes
-// rows [0, B) and leaves keys and ticket at zero.
-template <class Bar>
+// rows [0, B) and leaves keys and ticket at zero.  kEarly = false compiles out
+// the early-finalization flag (callers that never set Finish::done and whose
+// register count matters).
+template <bool kEarly = true, class Bar>
 __device__ __forceinline__ void finish_grid(const Finish& f, int64_t B, int tid, int n, int* flag, Bar bar) {
   __threadfence();
   bar();
@@ -77,9 +79,9 @@ __device__ __forceinline__ void finish_grid(const Finish& f, int64_t B, int tid,
     bool all_final = true;
     for (int64_t b = tid; b < B; b += n) {
       const Best best = write_row(f, b, unpack_key(atomicExch(f.keys + b, 0ull)));
-      if (f.done != nullptr) all_final = all_final && row_final(f, b, best);
+      if (kEarly && f.done != nullptr) all_final = all_final && row_final(f, b, best);
     }
-    if (f.done != nullptr) {
+    if (kEarly && f.done != nullptr) {
       bar();                                   // every thread has read *flag
       if (tid == 0) *flag = 1;
       bar();

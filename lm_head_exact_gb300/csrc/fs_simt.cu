@@ -41,15 +41,20 @@ __device__ __forceinline__ float dot8(uint4 a, uint4 b, float acc) {
   return acc;
 }
 
-template <int BG>
+// kEarly: the instantiation for early-finalization chunks (Finish::done set).
+// The plain one leaves that code out: at B = 1 the grid is sized for 8 CTAs
+// per SM, which needs <= 32 registers per thread.
+template <int BG, bool kEarly>
 __global__ void __launch_bounds__(kSimtThreads)
 simt_fused_kernel(Problem p, Finish f) {
   extern __shared__ uint4 smem_h[];            // [BG][d/8] bf16x8 packets
   __shared__ Best warp_best[kSimtWarps][BG];
   __shared__ int last_flag;
-  if (early_done_cta(f, &last_flag)) {
-    early_skip_cta(f, p.B, p.pdl, &last_flag);
-    return;
+  if constexpr (kEarly) {
+    if (early_done_cta(f, &last_flag)) {
+      early_skip_cta(f, p.B, p.pdl, &last_flag);
+      return;
+    }
   }
   const int n_parts = gridDim.x;
   pdl_launch_dependents();
@@ -140,7 +145,7 @@ simt_fused_kernel(Problem p, Finish f) {
       push_candidate(f, b0 + threadIdx.x, r);
     }
   }
-  finish_grid(f, p.B, threadIdx.x, kSimtThreads, &last_flag, [] { __syncthreads(); });
+  finish_grid<kEarly>(f, p.B, threadIdx.x, kSimtThreads, &last_flag, [] { __syncthreads(); });
 }
 
 int pick_group(int64_t B, int64_t d) {
@@ -149,43 +154,42 @@ int pick_group(int64_t B, int64_t d) {
   return bg;
 }
 
-template <int BG>
-cudaError_t launch_group(const Problem& p, const Finish& f, int n_parts, cudaStream_t stream) {
+// One wave of CTAs: the SMs times the CTAs of this instantiation that fit on
+// one SM (registers and shared memory), never more than the 8-row vocabulary
+// groups.
+template <int BG, bool kEarly>
+cudaError_t launch_variant(const Problem& p, const Finish& f, cudaStream_t stream) {
   const size_t smem = static_cast<size_t>(BG) * p.d * 2;
-  cudaError_t e = cudaFuncSetAttribute(simt_fused_kernel<BG>,
+  cudaError_t e = cudaFuncSetAttribute(simt_fused_kernel<BG, kEarly>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
+  int dev = 0, sms = 0, per_sm = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, simt_fused_kernel<BG, kEarly>, kSimtThreads, smem);
+  if (e != cudaSuccess) return e;
+  const int64_t parts = std::min<int64_t>(static_cast<int64_t>(std::max(sms, 1)) * std::max(per_sm, 1),
+                                          std::max<int64_t>(1, (p.V_local + kSimtWarps - 1) / kSimtWarps));
+  const int n_parts = static_cast<int>(parts);
   const int64_t groups = (p.B + BG - 1) / BG;
   dim3 grid(n_parts, static_cast<unsigned>(std::min<int64_t>(groups, 65535)));
-  return launch_kernel(simt_fused_kernel<BG>, grid, dim3(kSimtThreads), smem, stream, p.pdl, p, f);
+  return launch_kernel(simt_fused_kernel<BG, kEarly>, grid, dim3(kSimtThreads), smem, stream, p.pdl, p, f);
+}
+
+template <int BG>
+cudaError_t launch_group(const Problem& p, const Finish& f, cudaStream_t stream) {
+  return f.done != nullptr ? launch_variant<BG, true>(p, f, stream) : launch_variant<BG, false>(p, f, stream);
 }
 
 }  // namespace
 
-static int simt_num_parts(const Problem& p, int device) {
-  int sms = 0;
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
-  if (sms <= 0) sms = 148;
-  const int bg = pick_group(p.B, p.d);
-  const int64_t smem = static_cast<int64_t>(bg) * p.d * 2;
-  int per_sm = static_cast<int>(std::min<int64_t>(2048 / kSimtThreads, (200 * 1024) / std::max<int64_t>(smem, 1)));
-  per_sm = std::max(per_sm, 1);
-  int64_t parts = static_cast<int64_t>(sms) * per_sm;
-  // never more blocks than 8-row groups of the vocabulary
-  parts = std::min<int64_t>(parts, std::max<int64_t>(1, (p.V_local + kSimtWarps - 1) / kSimtWarps));
-  return static_cast<int>(parts);
-}
-
 cudaError_t launch_simt(const Problem& p, const Finish& f, cudaStream_t stream) {
-  int dev = 0;
-  cudaGetDevice(&dev);
-  const int n_parts = simt_num_parts(p, dev);
   switch (pick_group(p.B, p.d)) {
-    case 1: return launch_group<1>(p, f, n_parts, stream);
-    case 2: return launch_group<2>(p, f, n_parts, stream);
-    case 4: return launch_group<4>(p, f, n_parts, stream);
-    default: return launch_group<8>(p, f, n_parts, stream);
+    case 1: return launch_group<1>(p, f, stream);
+    case 2: return launch_group<2>(p, f, stream);
+    case 4: return launch_group<4>(p, f, stream);
+    default: return launch_group<8>(p, f, stream);
   }
 }
 

@@ -262,6 +262,18 @@ FS_API fs_status fs_workspace_release(void);
  * the batch-size rule.  Process-wide. */
 FS_API fs_status fs_set_path(int path);
 
+/*
+ * Launch overlap of fs_sample / fs_sample_ex (1, the default, or 0;
+ * process-wide).  With 1, the vocabulary-major kernel (B <= 96) is launched
+ * as a programmatic dependent of the preceding kernel on the stream: its
+ * prologue and the first ring of W loads may run while that kernel finishes
+ * (for example the previous decode step's sampling kernel, or the model's
+ * last layer); h, temp and bias are read only after the preceding kernel has
+ * completed.  W itself is read early, so the kernel enqueued immediately
+ * before the call must not write W -- set 0 where it may.
+ */
+FS_API fs_status fs_set_launch_overlap(int enable);
+
 /* The kernel family a call with batch size B would use under the current
  * setting (FS_PATH_SIMT / FS_PATH_TC_VOCAB / FS_PATH_TC_BATCH). */
 FS_API int fs_path_for_batch(int64_t B);

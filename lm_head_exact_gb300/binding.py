@@ -50,6 +50,7 @@ SIGNATURES = {
     "fs_workspace_reserve": (_int, [_i64, _i64, _c_void_p]),
     "fs_workspace_release": (_int, []),
     "fs_set_path": (_int, [_int]),
+    "fs_set_launch_overlap": (_int, [_int]),
     "fs_path_for_batch": (_int, [_i64]),
     "fs_profile_events": (_int, [_c_void_p, _c_void_p]),
     "fs_device_error": (_int, [ctypes.POINTER(_int)]),
@@ -296,6 +297,12 @@ def debug_noise(seed, step, row0, n_rows, v0, n_vocab, stream=None):
 
 def set_path(path):
     check(library().fs_set_path(path))
+
+
+def set_launch_overlap(enable):
+    """Overlapped (programmatic dependent) launch of one-shot calls: True by
+    default; False where the kernel enqueued just before a call may write W."""
+    check(library().fs_set_launch_overlap(1 if enable else 0))
 
 
 def path_for_batch(B):

@@ -22,6 +22,7 @@ thread_local char g_last_error[512] = "";
 thread_local cudaEvent_t g_prof_start = nullptr;
 thread_local cudaEvent_t g_prof_stop = nullptr;
 std::atomic<int> g_forced_path{kPathAuto};
+std::atomic<int> g_launch_overlap{1};
 
 fs_status fail(fs_status s, const char* fmt, ...) {
   va_list ap;
@@ -238,7 +239,7 @@ int resolve_path(int64_t B, int64_t d) {
 }
 
 // One fused launch (kernel + in-kernel cross-CTA finish) for one problem.
-fs_status run(const Problem& p, Finish f, cudaStream_t stream) {
+fs_status run(Problem p, Finish f, cudaStream_t stream) {
   if (p.B == 0) return FS_OK;
   if (p.V_local == 0) {                 // no vocabulary: every row gets "no sample"
     f.partials = nullptr;
@@ -249,6 +250,10 @@ fs_status run(const Problem& p, Finish f, cudaStream_t stream) {
   }
   FS_TRY(get_finish(stream, p.B, &f));
   const int path = resolve_path(p.B, p.d);
+  if (p.defer_inputs && path != kPathTcVocab) {   // only that kernel defers its input reads
+    p.defer_inputs = false;
+    p.pdl = false;
+  }
   int* err = nullptr;
   if (path != kPathSimt) FS_TRY(error_word(&err));
   cudaError_t e = cudaSuccess;
@@ -352,6 +357,11 @@ fs_status fs_sample_ex(const void* h, const void* W, int64_t B, int64_t d, int64
   g_last_error[0] = '\0';
   Problem p{h, W, B, d, V, 0, temp, bias, bias_row_stride, seed, step};
   FS_TRY(check_problem(p, true, out_ids, out_max));
+  // Programmatic dependent launch: the kernel's prologue and first W loads
+  // may overlap the tail of the preceding kernel of the stream; h, temp and
+  // bias are read only after its dependency wait.
+  p.pdl = g_launch_overlap.load() != 0;
+  p.defer_inputs = p.pdl;
   Finish f{};
   f.write_out = true;
   f.out_ids = out_ids;
@@ -612,6 +622,13 @@ fs_status fs_workspace_release(void) {
 fs_status fs_set_path(int path) {
   if (path < FS_PATH_AUTO || path > FS_PATH_TC_PAIR) return fail(FS_ERR_INVALID_ARG, "unknown path %d", path);
   g_forced_path.store(path);
+  return FS_OK;
+}
+
+fs_status fs_set_launch_overlap(int enable) {
+  g_last_error[0] = '\0';
+  if (enable != 0 && enable != 1) return fail(FS_ERR_INVALID_ARG, "enable must be 0 or 1 (got %d)", enable);
+  g_launch_overlap.store(enable);
   return FS_OK;
 }
 

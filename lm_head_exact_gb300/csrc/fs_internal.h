@@ -29,6 +29,11 @@ struct Problem {
   // (set for the 2nd..last chunk of a chunked step, whose inputs were all
   // written before the first chunk was enqueued).
   bool pdl = false;
+  // With pdl: the preceding kernel may still be writing h, temp or bias (a
+  // one-shot call after the model's last layer), so the kernel reads them
+  // only after its dependency wait; only the static W is prefetched before.
+  // Clear for chunks, whose inputs are all written before the first chunk.
+  bool defer_inputs = false;
   // Global index of row 0 of h in this launch (a batch split over several
   // launches); the noise counter always uses the global row.
   int64_t row_offset = 0;

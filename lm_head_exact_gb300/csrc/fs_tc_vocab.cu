@@ -139,10 +139,12 @@ tc_vocab_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
     tmem_alloc(tmem_base_slot, C::kTmemCols);
     tmem_relinquish();
   }
-  for (int b = threadIdx.x; b < BN; b += kThreads) {
-    const RowTemp rt = row_temp(b < B ? p.temp[b] : -1.0f);
-    col_inv_t[b] = rt.inv_t;
-    col_mode[b] = rt.mode;
+  if (!p.defer_inputs) {
+    for (int b = threadIdx.x; b < BN; b += kThreads) {
+      const RowTemp rt = row_temp(b < B ? p.temp[b] : -1.0f);
+      col_inv_t[b] = rt.inv_t;
+      col_mode[b] = rt.mode;
+    }
   }
   for (int i = threadIdx.x; i < kEpiWarps * BN; i += kThreads) warp_best[i] = best_none();
   tc_fence_before();
@@ -160,6 +162,18 @@ tc_vocab_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
       uint32_t phase = 0;
       int64_t n_issued = 0;
       bool ok = true;
+      // With deferred inputs the first ring of stages gets its W boxes before
+      // the dependency wait and its h boxes after it (each stage's barrier
+      // expects both from the start).  The first kStages issues are stages
+      // 0, 1, ... and K steps 0, 1, ... modulo n_kb.
+      bool h_ready = !p.defer_inputs;
+      auto load_deferred_h = [&]() {
+        pdl_wait();
+        for (int64_t i = 0; i < n_issued; ++i)
+          tma_load_2d(smem + C::kOffB + i * C::kBTileBytes, &tmap_h, &full_bar[i],
+                      static_cast<int32_t>((i % n_kb) * kBK), 0, pol_h);
+        h_ready = true;
+      };
       for (int t = 0; t < n_tiles && ok; ++t) {
         const int64_t row = tile_row(t);
         // rows past V (last tile) are zero-filled and still count as transferred bytes
@@ -170,11 +184,13 @@ tc_vocab_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
           uint8_t* b_dst = smem + C::kOffB + stage * C::kBTileBytes;
           mbar_arrive_expect_tx(&full_bar[stage], bytes);
           tma_load_2d(a_dst, &tmap_w, &full_bar[stage], kb * kBK, static_cast<int32_t>(row), pol_w);
-          tma_load_2d(b_dst, &tmap_h, &full_bar[stage], kb * kBK, 0, pol_h);
+          if (h_ready) tma_load_2d(b_dst, &tmap_h, &full_bar[stage], kb * kBK, 0, pol_h);
           ++n_issued;
           if (++stage == C::kStages) { stage = 0; phase ^= 1; }
+          if (!h_ready && n_issued == C::kStages) load_deferred_h();
         }
       }
+      if (!h_ready) load_deferred_h();   // fewer issues than stages (or an early stop)
       if (!ok) {
         // drain: never leave with copies in flight into this CTA's shared
         // memory -- wait (bounded) for the last load issued into every stage
@@ -226,6 +242,15 @@ tc_vocab_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
     // 32 rows in increasing id order: consecutive ids share one Philox call
     // and the running (max, argmax) of (warp, column) stays in registers
     // across all of the CTA's tiles -- no cross-lane reduction per tile.
+    if (p.defer_inputs) {        // temp (and bias) may come from the preceding kernel
+      pdl_wait();
+      for (int b = threadIdx.x; b < BN; b += kEpiWarps * 32) {
+        const RowTemp rt = row_temp(b < B ? p.temp[b] : -1.0f);
+        col_inv_t[b] = rt.inv_t;
+        col_mode[b] = rt.mode;
+      }
+      asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
+    }
     const PhiloxKey key{static_cast<uint32_t>(p.seed), static_cast<uint32_t>(p.seed >> 32)};
     const uint32_t step_lo = static_cast<uint32_t>(p.step);
     const uint32_t step_hi = static_cast<uint32_t>(p.step >> 32);

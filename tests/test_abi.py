@@ -65,6 +65,7 @@ def test_host_side_argument_checks(built_library):
     assert lib.fs_sample_chunked(z, z, 4, 64, 10, 5, z, z, 0, 0, 0, z, z, 1, z, z, z) == 1
     assert lib.fs_sample_chunked(z, z, 4, 64, 0, 5, z, z, 0, 0, 0, z, z, 8, z, z, z) == 1
     assert lib.fs_set_path(7) == 1
+    assert lib.fs_set_launch_overlap(2) == 1
     # early finalization: batch limit, NaN bounds, bad chunk bounds
     assert lib.fs_sample_chunked_early(z, z, 4097, 64, 0, 5, z, z, 0, 0, 0, z, z, 1, z, 0.0, 0.0, z, z, z, z) == 2
     assert "B <= 4096" in lib.fs_last_error().decode()

@@ -264,9 +264,10 @@ FS_API fs_status fs_set_path(int path);
 
 /*
  * Launch overlap of fs_sample / fs_sample_ex (1, the default, or 0;
- * process-wide).  With 1, the vocabulary-major kernel (B <= 96) is launched
- * as a programmatic dependent of the preceding kernel on the stream: its
- * prologue and the first ring of W loads may run while that kernel finishes
+ * process-wide).  With 1, the tensor-core kernels (B >= 2, except the CTA-pair
+ * kernel at B <= 256, where it measured slower) are launched
+ * as programmatic dependents of the preceding kernel on the stream: their
+ * prologues and first rings of W loads may run while that kernel finishes
  * (for example the previous decode step's sampling kernel, or the model's
  * last layer); h, temp and bias are read only after the preceding kernel has
  * completed.  W itself is read early, so the kernel enqueued immediately

@@ -250,7 +250,10 @@ fs_status run(Problem p, Finish f, cudaStream_t stream) {
   }
   FS_TRY(get_finish(stream, p.B, &f));
   const int path = resolve_path(p.B, p.d);
-  if (p.defer_inputs && path != kPathTcVocab) {   // only that kernel defers its input reads
+  // The tensor-core kernels defer their input reads; the overlap was measured
+  // to cost 2-4 us for the CTA-pair kernel at B <= 256 on GB300 (and to save
+  // 4-6 us everywhere else), so those calls launch plainly.
+  if (p.defer_inputs && (path == kPathSimt || (path == kPathTcPair && p.B <= 256))) {
     p.defer_inputs = false;
     p.pdl = false;
   }

@@ -33,6 +33,8 @@ struct Problem {
   // one-shot call after the model's last layer), so the kernel reads them
   // only after its dependency wait; only the static W is prefetched before.
   // Clear for chunks, whose inputs are all written before the first chunk.
+  // Honoured by the tensor-core kernels (the CUDA-core kernel is launched
+  // without the dependency instead).
   bool defer_inputs = false;
   // Global index of row 0 of h in this launch (a batch split over several
   // launches); the noise counter always uses the global row.

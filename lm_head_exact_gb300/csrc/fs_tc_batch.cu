@@ -138,19 +138,32 @@ tc_batch_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_constan
       uint32_t phase = 0;
       int64_t n_issued = 0;
       bool ok = true;
+      // Deferred inputs: the first ring of stages (stage i = K step i mod
+      // n_kb) gets its W boxes before the dependency wait, its h boxes after.
+      bool h_ready = kStoreLogits || !p.defer_inputs;
+      auto load_deferred_h = [&]() {
+        pdl_wait();
+        for (int64_t i = 0; i < n_issued; ++i)
+          tma_load_2d(smem + kOffA + i * kATileBytes, &tmap_h, &full_bar[i], static_cast<int32_t>((i % n_kb) * kBK),
+                      bt * kBM, pol_h);
+        h_ready = true;
+      };
       for (int t = 0; t < n_tiles && ok; ++t) {
         const int vt = q + t * args.n_groups;
         for (int kb = 0; kb < n_kb; ++kb) {
           if (!mbar_wait(&empty_bar[stage], phase ^ 1, args.err, abort_flag)) { ok = false; break; }
           mbar_arrive_expect_tx(&full_bar[stage], kATileBytes + kBTileBytes);
-          tma_load_2d(smem + kOffA + stage * kATileBytes, &tmap_h, &full_bar[stage], kb * kBK, bt * kBM,
-                      pol_h);
+          if (h_ready)
+            tma_load_2d(smem + kOffA + stage * kATileBytes, &tmap_h, &full_bar[stage], kb * kBK, bt * kBM,
+                        pol_h);
           tma_load_2d(smem + kOffB + stage * kBTileBytes, &tmap_w, &full_bar[stage], kb * kBK, vt * kBN,
                       pol_w);
           ++n_issued;
           if (++stage == kStages) { stage = 0; phase ^= 1; }
+          if (!h_ready && n_issued == kStages) load_deferred_h();
         }
       }
+      if (!h_ready) load_deferred_h();   // fewer issues than stages (or an early stop)
       if (!ok) {
         volatile int no_abort = 0;
         for (int64_t i = std::max<int64_t>(0, n_issued - kStages); i < n_issued; ++i)
@@ -197,6 +210,7 @@ tc_batch_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_constan
     const int row_in_tile = quad * 32 + lane;
     const int64_t b = static_cast<int64_t>(bt) * kBM + row_in_tile;
     const bool row_ok = b < p.B;
+    if (!kStoreLogits && p.defer_inputs) pdl_wait();   // temp (and bias) may come from the preceding kernel
     const RowTemp rt = row_temp(row_ok ? p.temp[b] : -1.0f);
     const bool active = row_ok && rt.mode != kRowInvalid;
     const bool greedy = rt.mode == kRowGreedy;

@@ -143,20 +143,33 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_constant
       uint32_t phase = 0;
       int64_t n_issued = 0;
       bool ok = true;
+      const int h_row = pt * 2 * kRowsPerCta + static_cast<int>(rank) * kRowsPerCta;
+      // Deferred inputs: the first ring of stages (stage i = K step i mod
+      // n_kb) gets its W boxes before the dependency wait, its h boxes after.
+      bool h_ready = !p.defer_inputs;
+      auto load_deferred_h = [&]() {
+        pdl_wait();
+        for (int64_t i = 0; i < n_issued; ++i)
+          tma_load_2d_pair(smem + kOffA + i * kATileBytes, &tmap_h, mapa_shared(smem_u32(&full_bar[i]), 0),
+                           static_cast<int32_t>((i % n_kb) * kBK), h_row, pol_h);
+        h_ready = true;
+      };
       for (int t = 0; t < n_tiles && ok; ++t) {
         const int vt = q + t * args.n_groups;
         for (int kb = 0; kb < n_kb; ++kb) {
           if (!mbar_wait(&empty_bar[stage], phase ^ 1, args.err, abort_flag)) { ok = false; break; }
           const uint32_t leader_full = mapa_shared(smem_u32(&full_bar[stage]), 0);
           if (rank == 0) mbar_arrive_expect_tx(&full_bar[stage], 2 * (kATileBytes + kBTileBytes));
-          tma_load_2d_pair(smem + kOffA + stage * kATileBytes, &tmap_h, leader_full, kb * kBK,
-                           pt * 2 * kRowsPerCta + static_cast<int>(rank) * kRowsPerCta, pol_h);
+          if (h_ready)
+            tma_load_2d_pair(smem + kOffA + stage * kATileBytes, &tmap_h, leader_full, kb * kBK, h_row, pol_h);
           tma_load_2d_pair(smem + kOffB + stage * kBTileBytes, &tmap_w, leader_full, kb * kBK,
                            vt * kBN + static_cast<int>(rank) * (kBN / 2), pol_w);
           ++n_issued;
           if (++stage == kStages) { stage = 0; phase ^= 1; }
+          if (!h_ready && n_issued == kStages) load_deferred_h();
         }
       }
+      if (!h_ready) load_deferred_h();   // fewer issues than stages (or an early stop)
       if (!ok && rank == 0) {
         volatile int no_abort = 0;
         for (int64_t i = std::max<int64_t>(0, n_issued - kStages); i < n_issued; ++i)
@@ -203,6 +216,7 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_constant
     const int row_in_tile = quad * 32 + lane;
     const int64_t b = static_cast<int64_t>(pt) * 2 * kRowsPerCta + static_cast<int64_t>(rank) * kRowsPerCta + row_in_tile;
     const bool row_ok = b < p.B;
+    if (p.defer_inputs) pdl_wait();   // temp (and bias) may come from the preceding kernel
     const RowTemp rt = row_temp(row_ok ? p.temp[b] : -1.0f);
     const bool active = row_ok && rt.mode != kRowInvalid;
     const bool greedy = rt.mode == kRowGreedy;
@@ -262,15 +276,35 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_constant
 
 }  // namespace
 
+// CTA pairs that can be resident at once: a pair needs two SMs of one GPC,
+// so with GPCs of odd SM counts this can be below SMs / 2.  A persistent grid
+// larger than that would run its last pairs as a second wave.
+static int resident_pairs(int dev, int sms) {
+  static int cached[64] = {0};
+  if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
+  int n = 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * (sms / 2)));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  if (cudaOccupancyMaxActiveClusters(&n, tc_pair_kernel, &cfg) != cudaSuccess || n <= 0) {
+    cudaGetLastError();
+    n = sms / 2;
+  }
+  n = std::min(n, sms / 2);
+  if (dev >= 0 && dev < 64) cached[dev] = n;
+  return n;
+}
+
 cudaError_t launch_tc_pair(const Problem& p, const Finish& f, int* err, cudaStream_t stream) {
   if (p.d < kBK || p.V_local <= 0) return cudaErrorNotSupported;
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (sms <= 0) sms = 148;
-  const int pairs = sms / 2;
   cudaError_t e = cudaFuncSetAttribute(tc_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
+  const int pairs = resident_pairs(dev, sms);
   CUtensorMap tw;
   if (!encode_kmajor_bf16(&tw, p.W, p.V_local, p.d, kBK, kBN / 2)) return cudaErrorInvalidValue;
   const int64_t slice = static_cast<int64_t>(pairs) * 2 * kRowsPerCta;

@@ -394,3 +394,38 @@ def test_batch_larger_than_one_launch(fs, torch_cuda, forced):
     finally:
         fs.set_path(fs.FS_PATH_AUTO)
     compare(ids, mx, sampler.sample(h, W, temp, 8, 2), what=f"B=20000 {forced}")
+
+
+# ------------------------------------------------------------------ launch overlap
+@pytest.mark.parametrize("B", [2, 16, 96, 128, 256, 300])
+def test_launch_overlap_gives_identical_results(fs, torch_cuda, B):
+    """Back-to-back one-shot calls launched as programmatic dependents (the
+    default) equal the same calls launched plainly, bit for bit -- also when a
+    torch kernel rewrites h and T between two calls on the same stream."""
+    torch = torch_cuda
+    h, W, temp = _problem(B, 5000, 256, seed=60 + B)
+    h2, _, temp2 = _problem(B, 1, 256, seed=61 + B)
+    hd, Wd, td = to_device(h, torch), to_device(W, torch), to_device(temp, torch)
+    h2d, t2d = to_device(h2, torch), to_device(temp2, torch)
+
+    def run(overlap):
+        fs.set_launch_overlap(overlap)
+        try:
+            x, t = hd.clone(), td.clone()
+            outs = []
+            for step in range(3):
+                outs.append(fs.sample(x, Wd, t, 5, step))
+            x.copy_(h2d)
+            t.copy_(t2d)
+            outs.append(fs.sample(x, Wd, t, 5, 3))
+            outs.append(fs.sample(x, Wd, t, 5, 4))
+            torch.cuda.synchronize()
+            return [(i.cpu().numpy(), m.cpu().numpy()) for i, m in outs]
+        finally:
+            fs.set_launch_overlap(True)
+
+    on, off = run(True), run(False)
+    for (i1, m1), (i0, m0) in zip(on, off):
+        np.testing.assert_array_equal(i1, i0)
+        np.testing.assert_array_equal(m1, m0)
+    compare(on[3][0], on[3][1], sampler.sample(h2, W, temp2, 5, 3), what=f"overlap B={B}")

@@ -12,11 +12,14 @@ Arithmetic is fp64 throughout.  Modules:
 
 * ``philox``  -- Philox-4x32-10 counter-based generator (Salmon et al., SC'11).
 * ``sampler`` -- logits, temperature, Gumbel noise, the total-order argmax,
-  and the one-shot / partitioned / chunked / sharded samplers built on them.
+  and the one-shot / partitioned / chunked / sharded samplers built on them;
+  the early-finalization bound of the chunked sampler.
+* ``topk``    -- Gumbel-top-k: the k best perturbed scores per row (k draws
+  without replacement), and its partitioned form.
 
 Pins (what ties each function to something other than itself) live in
 ``tests/test_oracle_*.py``; every function here is pinned, none is
 "parity unpinned".
 """
 
-from . import philox, sampler  # noqa: F401
+from . import philox, sampler, topk  # noqa: F401

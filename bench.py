@@ -449,6 +449,30 @@ def run_ours(args):
                               "launches_per_step": n + 1, "cuda_graph": True})
                 del chunks, bias
 
+    # Gumbel-top-k (k ids per row without replacement) on the same head:
+    # the batch-major kernel with a per-row list epilogue + a merge launch
+    topk = []
+    if not args.no_sweep:
+        for b, k in ((1, 8), (16, 8), (16, 16), (64, 8), (256, 8), (1024, 4)):
+            hsrc = hd_all if b <= bmax else h_big
+            tsrc = temp_all if b <= bmax else t_big
+            ids_k = torch.empty((b, k), dtype=torch.int64, device="cuda")
+            z_k = torch.empty((b, k), dtype=torch.float32, device="cuda")
+            with torch.cuda.stream(stream):
+                for i in range(3):
+                    fs.sample_topk(hsrc[:b], Wd, tsrc[:b], seed, i, k, out=(ids_k, z_k), stream=stream)
+                k0 = torch.cuda.Event(enable_timing=True)
+                k1 = torch.cuda.Event(enable_timing=True)
+                k0.record(stream)
+                for i in range(20):
+                    fs.sample_topk(hsrc[:b], Wd, tsrc[:b], seed, 3 + i, k, out=(ids_k, z_k), stream=stream)
+                k1.record(stream)
+            torch.cuda.synchronize()
+            us = k0.elapsed_time(k1) / 20 * 1e3
+            rf = roofline(b, d, V, us, peaks)
+            topk.append({"workload": "llama3_8b", "B": b, "k": k, "us_per_step": round(us, 2), "frac": rf["frac"],
+                         "bound": rf["bound"], "launches_per_step": 2})
+
     # the unfused comparison pipeline on the same workload: GEMM -> fp32
     # logits in HBM -> softmax -> sample (the traffic fusion removes)
     unfused = None
@@ -497,6 +521,7 @@ def run_ours(args):
             "unfused": unfused,
             "chunked": chunked,
             "early_finalization": early,
+            "topk": topk,
         }
         if not args.no_cpu_baseline:
             result["cpu_baseline"] = cpu_baseline(B, args.cpu_seconds)

@@ -190,6 +190,30 @@ FS_API fs_status fs_chunk_rest_norms(const void* W, int64_t d, const int64_t* bo
                                      float* rest_w_norm, void* stream);
 
 /*
+ * Gumbel-top-k: k ids per row drawn WITHOUT replacement from
+ * softmax(logits / T) (each next id from the renormalized remaining mass),
+ * fused into the LM-head matmul like fs_sample_ex.  The summary page cites
+ * Gumbel-top-k sampling among the related work; with the sampler's own
+ * perturbed scores z (same noise, same temperature and bias handling), the
+ * k ids of largest z are that draw.  Row b's result, best first under the
+ * sampler's total order (a larger z, then a smaller id), is out_ids[b * k + j]
+ * (int64) and out_z[b * k + j] (fp32, the perturbed score; the logit for
+ * T == 0 rows, i.e. the top-k logits); -inf and NaN scores are never chosen,
+ * and rows with fewer than k choosable ids (or an invalid T) are padded with
+ * id -1 and z -inf.  k = 1 gives fs_sample_ex's ids.
+ *   1 <= k <= 16 (else FS_ERR_INVALID_ARG); B <= 4096 and d >= 64 (else
+ *   FS_ERR_UNSUPPORTED).  Two launches: the batch-major tensor-core kernel
+ *   with a per-row K-list epilogue (K = 4, 8 or 16 >= k), writing one list per
+ *   (row, CTA group) to library workspace, then a warp-per-row merge.  The
+ *   workspace grows on the first call of a size; capture in a CUDA graph only
+ *   after an eager call of the same B.
+ */
+FS_API fs_status fs_sample_topk(const void* h, const void* W, int64_t B, int64_t d, int64_t V,
+                                const float* temp, const float* bias, int64_t bias_row_stride,
+                                uint64_t seed, uint64_t step, int k,
+                                int64_t* out_ids, float* out_z, void* stream);
+
+/*
  * The UNFUSED comparison pipeline (summary page, "Method", ops (1)-(4)):
  * a tensor-core GEMM writes fp32 logits [B, V] (+ bias) to device memory,
  * a softmax kernel reads them and writes probabilities [B, V], and a sample

@@ -40,6 +40,8 @@ SIGNATURES = {
                                        _c_void_p, _c_void_p, _c_void_p]),
     "fs_row_norms": (_int, [_c_void_p, _i64, _i64, _c_void_p, _c_void_p]),
     "fs_chunk_rest_norms": (_int, [_c_void_p, _i64, _c_void_p, _i64, _c_void_p, _c_void_p]),
+    "fs_sample_topk": (_int, [_c_void_p, _c_void_p, _i64, _i64, _i64, _c_void_p, _c_void_p, _i64,
+                              _u64, _u64, _int, _c_void_p, _c_void_p, _c_void_p]),
     "fs_sample_unfused": (_int, [_c_void_p, _c_void_p, _i64, _i64, _i64, _c_void_p, _c_void_p, _i64,
                                  _u64, _u64, _c_void_p, _c_void_p, _c_void_p, _c_void_p]),
     "fs_sample_host": (_int, [_c_void_p, _c_void_p, _i64, _i64, _i64, _c_void_p, _c_void_p, _i64,
@@ -178,6 +180,25 @@ def sample_unfused(h, W, temp, seed, step, bias=None, logits_out=None, out=None,
 def sample_ex(*args, **kwargs):
     """Alias of ``sample`` (the bias argument maps to fs_sample_ex)."""
     return sample(*args, **kwargs)
+
+
+def sample_topk(h, W, temp, seed, step, k, bias=None, out=None, stream=None):
+    """Gumbel-top-k: k ids per row without replacement, best first.
+    Returns (ids int64 [B, k], z fp32 [B, k]); -1 / -inf where a row has
+    fewer than k choosable ids."""
+    torch = _torch()
+    B, d = h.shape
+    V = W.shape[0]
+    if out is None:
+        out = (torch.empty((B, k), dtype=torch.int64, device=h.device),
+               torch.empty((B, k), dtype=torch.float32, device=h.device))
+    ids, z = out
+    bptr, bstride = _bias_args(bias, B, V)
+    check(library().fs_sample_topk(
+        _dev(h, "h", torch.bfloat16, 2), _dev(W, "W", torch.bfloat16, 2), B, d, V,
+        _dev(temp, "temp", torch.float32, 1), bptr, bstride, seed, step, int(k),
+        _dev(ids, "out_ids", torch.int64, 2), _dev(z, "out_z", torch.float32, 2), _stream_ptr(stream)))
+    return ids, z
 
 
 def sample_chunked(h, W_chunk, v_begin, temp, seed, step, carry_max, carry_ids, first, last,

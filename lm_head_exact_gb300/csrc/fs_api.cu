@@ -51,6 +51,8 @@ struct Workspace {
   size_t unfused_bytes = 0;
   void* host_out = nullptr;     // pinned host landing area of fs_sample_host's results
   size_t host_out_bytes = 0;
+  void* topk = nullptr;         // per-(row, CTA group) candidate lists of fs_sample_topk
+  size_t topk_bytes = 0;
 };
 
 std::mutex g_ws_mutex;
@@ -291,6 +293,10 @@ fs_status run(Problem p, Finish f, cudaStream_t stream) {
 // Rows one early-finalization call handles: one launch of every kernel
 // family, so the done flag is decided by a single last CTA.
 constexpr int kEarlyMaxRows = 4096;
+
+// Gumbel-top-k limits: list length per row, and rows (one launch).
+constexpr int kTopKMax = 16;
+constexpr int kTopKMaxRows = 4096;
 
 struct EarlyArgs {
   const float* h_norms = nullptr;
@@ -545,6 +551,47 @@ fs_status fs_sample_host(const void* h_host, const void* W, int64_t B, int64_t d
   return FS_OK;
 }
 
+fs_status fs_sample_topk(const void* h, const void* W, int64_t B, int64_t d, int64_t V,
+                         const float* temp, const float* bias, int64_t bias_row_stride,
+                         uint64_t seed, uint64_t step, int k,
+                         int64_t* out_ids, float* out_z, void* stream_) {
+  g_last_error[0] = '\0';
+  if (k < 1 || k > kTopKMax) return fail(FS_ERR_INVALID_ARG, "k must be in [1, %d] (got %d)", kTopKMax, k);
+  Problem p{h, W, B, d, V, 0, temp, bias, bias_row_stride, seed, step};
+  FS_TRY(check_problem(p, true, out_ids, out_z));
+  if (B == 0) return FS_OK;
+  if (B > kTopKMaxRows)
+    return fail(FS_ERR_UNSUPPORTED, "fs_sample_topk handles B <= %d (got %lld)", kTopKMaxRows, (long long)B);
+  if (V > 0 && d < 64) return fail(FS_ERR_UNSUPPORTED, "fs_sample_topk needs d >= 64 (got %lld)", (long long)d);
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  int dev;
+  FS_TRY(current_device(&dev));
+  const int K = k <= 4 ? 4 : (k <= 8 ? 8 : 16);
+  // overlapped launch as for fs_sample_ex: W prefetched before the dependency
+  // wait, h / temp / bias read and the shared partials written after it
+  p.pdl = g_launch_overlap.load() != 0;
+  p.defer_inputs = p.pdl;
+  const int parts = V > 0 ? tc_topk_parts(B, dev) : 0;
+  const size_t need = std::max<size_t>(static_cast<size_t>(B) * parts * K * sizeof(Partial), 256);
+  Partial* partials = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_ws_mutex);
+    Workspace& ws = g_workspaces[{dev, stream}];
+    FS_TRY(grow(&ws.topk, &ws.topk_bytes, need, stream));
+    partials = static_cast<Partial*>(ws.topk);
+  }
+  cudaError_t e = cudaSuccess;
+  if (V > 0) {
+    int* err = nullptr;
+    FS_TRY(error_word(&err));
+    e = launch_tc_topk(p, K, partials, err, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "top-k kernel launch");
+  }
+  e = launch_topk_merge(partials, parts * K, B, k, out_ids, out_z, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "top-k merge launch");
+  return FS_OK;
+}
+
 fs_status fs_sample_unfused(const void* h, const void* W, int64_t B, int64_t d, int64_t V,
                             const float* temp, const float* bias, int64_t bias_row_stride,
                             uint64_t seed, uint64_t step, int64_t* out_ids, float* out_max,
@@ -614,6 +661,7 @@ fs_status fs_workspace_release(void) {
       if (it->second.unfused) cudaFree(it->second.unfused);
       if (it->second.host_out) cudaFreeHost(it->second.host_out);
       if (it->second.staging) cudaFree(it->second.staging);
+      if (it->second.topk) cudaFree(it->second.topk);
       it = g_workspaces.erase(it);
     } else {
       ++it;

@@ -123,6 +123,15 @@ cudaError_t launch_debug_wait(int* err, uint64_t timeout_ns, cudaStream_t stream
 cudaError_t launch_row_norms(const void* X, int64_t n, int64_t d, float* out, unsigned* seg_max,
                              cudaStream_t stream);
 
+// Gumbel-top-k: the batch-major kernel in top-K mode (K in {4, 8, 16}, one
+// launch, B <= one launch's rows) writes per-(row, CTA group) lists to
+// partials [B, tc_topk_parts(B), K]; launch_topk_merge then merges each row's
+// lists into its k <= K best (out_ids / out_z [B, k]; -1 / -inf padded).
+int tc_topk_parts(int64_t B, int device);
+cudaError_t launch_tc_topk(const Problem& p, int K, Partial* partials, int* err, cudaStream_t stream);
+cudaError_t launch_topk_merge(const Partial* partials, int n_cand, int64_t B, int k, int64_t* out_ids, float* out_z,
+                              cudaStream_t stream);
+
 cudaError_t launch_reduce(const Finish& f, int64_t B, cudaStream_t stream);
 
 // Set the calling thread's fs_last_error() text.

@@ -34,6 +34,91 @@ reduce_kernel(Finish f, int64_t B) {
   if (lane == 0) write_row(f, b, best);
 }
 
+// Gumbel-top-k merge, one 256-thread block per row over the row's n_cand
+// candidates (the per-CTA-group lists; ids unique, empty entries kNoId).
+// Each lane holds at most kMergePerLane candidates in registers.  Round j of
+// a selection picks the best candidate that ranks after the one picked in
+// round j - 1 (warp shuffles only), so k rounds give the k best in order.
+// Level 1: each warp selects the k best of its slice of the candidates into
+// shared memory; level 2: warp 0 selects the k best of those 8 k.
+constexpr int kMergeThreads = 256;
+constexpr int kMergeWarps = kMergeThreads / 32;
+constexpr int kMergePerLane = 12;
+constexpr int kTopKMaxList = 16;
+
+__device__ __forceinline__ Best select_after(const float (&cz)[kMergePerLane], const int32_t (&ci)[kMergePerLane],
+                                             float pz, int32_t pid) {
+  Best best = best_none();
+#pragma unroll
+  for (int i = 0; i < kMergePerLane; ++i)
+    if (ci[i] != kNoId && beats(pz, pid, cz[i], ci[i]) && beats(cz[i], ci[i], best.z, best.id)) {
+      best.z = cz[i];
+      best.id = ci[i];
+    }
+  return warp_combine(best);
+}
+
+__global__ void __launch_bounds__(kMergeThreads)
+topk_merge_kernel(const Partial* __restrict__ partials, int n_cand, int k, int64_t* __restrict__ out_ids,
+                  float* __restrict__ out_z) {
+  __shared__ Best level1[kMergeWarps][kTopKMaxList];
+  pdl_launch_dependents();      // the next call's kernel may start its W prefetch
+  pdl_wait();                   // launched as a dependent of the kernel that wrote the partials
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int64_t b = blockIdx.x;
+  const Partial* row = partials + b * n_cand;
+  // this warp's slice of the candidates, strided over its lanes
+  const int per_warp = (n_cand + kMergeWarps - 1) / kMergeWarps;
+  const int lo = warp * per_warp;
+  const int hi = min(n_cand, lo + per_warp);
+  float cz[kMergePerLane];
+  int32_t ci[kMergePerLane];
+#pragma unroll
+  for (int i = 0; i < kMergePerLane; ++i) {
+    const int j = lo + lane + 32 * i;
+    if (j < hi) {
+      const Partial c = row[j];
+      cz[i] = c.z;
+      ci[i] = c.id;
+    } else {
+      cz[i] = -INFINITY;
+      ci[i] = kNoId;
+    }
+  }
+  float pz = INFINITY;          // (+inf, -1) ranks before every candidate
+  int32_t pid = -1;
+  for (int j = 0; j < k; ++j) {
+    const Best w = select_after(cz, ci, pz, pid);
+    if (lane == 0) level1[warp][j] = w;
+    pz = w.z;
+    pid = w.id;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    // level 2: the 8 k level-1 entries, at most 4 per lane
+#pragma unroll
+    for (int i = 0; i < kMergePerLane; ++i) {
+      const int j = lane + 32 * i;
+      const bool ok = i < 4 && j < kMergeWarps * k;
+      const Best c = ok ? level1[j / k][j % k] : best_none();
+      cz[i] = c.z;
+      ci[i] = c.id;
+    }
+    pz = INFINITY;
+    pid = -1;
+    for (int j = 0; j < k; ++j) {
+      const Best w = select_after(cz, ci, pz, pid);
+      if (lane == 0) {
+        out_ids[b * k + j] = w.id == kNoId ? -1 : static_cast<int64_t>(w.id);
+        out_z[b * k + j] = w.id == kNoId ? -INFINITY : w.z;
+      }
+      pz = w.z;
+      pid = w.id;
+    }
+  }
+}
+
 __global__ void debug_noise_kernel(uint64_t seed, uint64_t step, int64_t row0, int64_t n_rows,
                                    int64_t v0, int64_t n_vocab, uint32_t* words, float* gumbel) {
   const int64_t n = n_rows * n_vocab;
@@ -78,6 +163,15 @@ cudaError_t launch_reduce(const Finish& f, int64_t B, cudaStream_t stream) {
   const unsigned blocks = static_cast<unsigned>((B + kRowsPerBlock - 1) / kRowsPerBlock);
   reduce_kernel<<<blocks, kReduceThreads, 0, stream>>>(f, B);
   return cudaGetLastError();
+}
+
+cudaError_t launch_topk_merge(const Partial* partials, int n_cand, int64_t B, int k, int64_t* out_ids, float* out_z,
+                              cudaStream_t stream) {
+  if (B == 0) return cudaSuccess;
+  if (k < 1 || k > kTopKMaxList || n_cand > kMergeThreads * kMergePerLane || B > 2147483647)
+    return cudaErrorInvalidValue;
+  return launch_kernel(topk_merge_kernel, dim3(static_cast<unsigned>(B)), dim3(kMergeThreads), 0, stream, true,
+                       partials, n_cand, k, out_ids, out_z);
 }
 
 cudaError_t launch_debug_noise(uint64_t seed, uint64_t step, int64_t row0, int64_t n_rows,

@@ -60,12 +60,15 @@ constexpr int kOffBars = kOffB + kStages * kBTileBytes;
 constexpr int kNumBars = 2 * kStages + 5;
 constexpr int kOffMisc = kOffBars + kNumBars * 8;
 constexpr int kOffHalf = kOffMisc + 16;                            // Best[128]: second-half results
-constexpr int kSmemBytes = kOffHalf + kBM * 8 + 1024;
+constexpr int kOffTopK = kOffHalf + kBM * 8;                       // top-k mode: Partial[128][K] of the second half
+constexpr int kSmemBytes = kOffTopK + 1024;
+constexpr int smem_bytes(int top_k) { return kSmemBytes + kBM * top_k * 8; }
 
 struct BatchArgs {
   Problem p;            // rows [0, p.B) of this launch's batch slice
   float* logits;        // store-logits mode: [B_slice, V_local] fp32 (row stride V_local)
-  Finish f;             // sampling mode: cross-CTA finish of this slice's rows
+  Finish f;             // sampling mode: cross-CTA finish of this slice's rows;
+                        // top-k mode: f.partials [B, f.n_parts, K], part = CTA group
   int nbt;              // batch tiles of this launch
   int n_groups;         // CTA groups = gridDim.x / nbt
   int n_vt;             // vocabulary tiles = ceil(V_local / 256)
@@ -74,7 +77,10 @@ struct BatchArgs {
 
 // kStoreLogits = false: fused sampling epilogue.  true: the unfused
 // comparison path's plain GEMM epilogue, storing logits (+ bias) to HBM.
-template <bool kStoreLogits>
+// kTopK > 0 (with kStoreLogits = false): Gumbel-top-k epilogue -- every
+// thread keeps its batch row's K best perturbed scores, and each CTA writes
+// its per-row list to f.partials for the merge kernel (no in-kernel finish).
+template <bool kStoreLogits, int kTopK = 0>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_batch_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_constant__ CUtensorMap tmap_w,
                 const BatchArgs args) {
@@ -88,7 +94,7 @@ tc_batch_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_constan
   uint32_t* tmem_base_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
   int* last_flag = reinterpret_cast<int*>(smem + kOffMisc + 8);
-  if (!kStoreLogits && early_done_cta(args.f, last_flag)) {
+  if (!kStoreLogits && kTopK == 0 && early_done_cta(args.f, last_flag)) {
     early_skip_cta(args.f, args.p.B, args.p.pdl, last_flag);
     return;
   }
@@ -227,6 +233,8 @@ tc_batch_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_constan
     scan.greedy = greedy;
     scan.bias_row = p.bias != nullptr ? p.bias + b * p.bias_stride : nullptr;
     Best best = best_none();
+    TopList<(kTopK > 0 ? kTopK : 1)> list;
+    topk_init(list);
 
     for (int t = 0; t < n_tiles; ++t) {
       const int acc = t & 1;
@@ -254,19 +262,45 @@ tc_batch_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_constan
             }
           }
         } else if (active && v0 < p.V_local) {
-          if (scan.bias_row != nullptr)
-            scan32<true>(r, v0, p.V_local, p.v_offset, scan, best);
-          else
-            scan32<false>(r, v0, p.V_local, p.v_offset, scan, best);
+          if constexpr (kTopK > 0) {
+            if (scan.bias_row != nullptr)
+              scan32_topk<true>(r, v0, p.V_local, p.v_offset, scan, list);
+            else
+              scan32_topk<false>(r, v0, p.V_local, p.v_offset, scan, list);
+          } else {
+            if (scan.bias_row != nullptr)
+              scan32<true>(r, v0, p.V_local, p.v_offset, scan, best);
+            else
+              scan32<false>(r, v0, p.V_local, p.v_offset, scan, best);
+          }
         }
       }
       tc_fence_before();
       mbar_arrive(&tempty_bar[acc]);
     }
+    if constexpr (kTopK > 0) {
+      // merge the two column halves' lists, then one list per (row, group)
+      Partial* other = reinterpret_cast<Partial*>(smem + kOffTopK) + row_in_tile * kTopK;
+      if (half == 1) {
+#pragma unroll
+        for (int j = 0; j < kTopK; ++j) other[j] = Partial{list.z[j], list.id[j]};
+      }
+      asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
+      if (p.pdl) pdl_wait();      // the previous call's merge kernel may still read the partials
+      if (half == 0 && row_ok) {
+#pragma unroll
+        for (int j = 0; j < kTopK; ++j) topk_offer(list, other[j].z, other[j].id);
+        Partial* dst = args.f.partials + (b * args.f.n_parts + q) * kTopK;
+#pragma unroll
+        for (int j = 0; j < kTopK; ++j) dst[j] = Partial{list.z[j], list.id[j]};
+      }
+    }
     // combine the two column halves of each row, then one candidate per (row, group)
-    if (half == 1) half_best[row_in_tile] = best;
-    asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
-    if constexpr (!kStoreLogits) {
+    if constexpr (kTopK == 0) {
+      if (half == 1) half_best[row_in_tile] = best;
+      asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
+    }
+    if constexpr (!kStoreLogits && kTopK == 0) {
       pdl_wait();                 // the finish area is shared with the previous launch
       if (half == 0 && row_ok) push_candidate(args.f, b, combine(best, half_best[row_in_tile]));
       finish_grid(args.f, p.B, threadIdx.x, kEpiWarps * 32, last_flag,
@@ -310,8 +344,8 @@ static cudaError_t launch_batch_impl(const Problem& p, const Finish* f, float* l
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (sms <= 0) sms = 148;
   const bool store = logits != nullptr;
-  cudaError_t e = store ? cudaFuncSetAttribute(tc_batch_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes)
-                        : cudaFuncSetAttribute(tc_batch_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  cudaError_t e = store ? cudaFuncSetAttribute(tc_batch_kernel<true, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes)
+                        : cudaFuncSetAttribute(tc_batch_kernel<false, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   CUtensorMap tw;
   if (!encode_kmajor_bf16(&tw, p.W, p.V_local, p.d, kBK, kBN)) return cudaErrorInvalidValue;
@@ -342,10 +376,10 @@ static cudaError_t launch_batch_impl(const Problem& p, const Finish* f, float* l
     BatchArgs a{ps, store ? logits + b0 * p.V_local : nullptr, fs_slice, g.nbt, g.n_groups,
                 static_cast<int>((p.V_local + kBN - 1) / kBN), err};
     if (store) {
-      tc_batch_kernel<true><<<g.grid, kThreads, kSmemBytes, stream>>>(th, tw, a);
+      tc_batch_kernel<true, 0><<<g.grid, kThreads, kSmemBytes, stream>>>(th, tw, a);
       e = cudaGetLastError();
     } else {
-      e = launch_kernel(tc_batch_kernel<false>, dim3(g.grid), dim3(kThreads), kSmemBytes, stream, ps.pdl, th, tw, a);
+      e = launch_kernel(tc_batch_kernel<false, 0>, dim3(g.grid), dim3(kThreads), kSmemBytes, stream, ps.pdl, th, tw, a);
     }
     if (e != cudaSuccess) return e;
   }
@@ -358,6 +392,46 @@ cudaError_t launch_tc_batch(const Problem& p, const Finish& f, int* err, cudaStr
 
 cudaError_t launch_tc_logits(const Problem& p, float* logits, int* err, cudaStream_t stream) {
   return launch_batch_impl(p, nullptr, logits, err, stream);
+}
+
+int tc_topk_parts(int64_t B, int device) {
+  int sms = 0;
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
+  if (sms <= 0) sms = 148;
+  return batch_geometry(B, sms).n_groups;
+}
+
+template <int K>
+static cudaError_t launch_topk_k(const Problem& p, Partial* partials, int* err, cudaStream_t stream) {
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (sms <= 0) sms = 148;
+  if (p.B > static_cast<int64_t>(sms) * kBM) return cudaErrorNotSupported;   // one launch
+  cudaError_t e = cudaFuncSetAttribute(tc_batch_kernel<false, K>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       smem_bytes(K));
+  if (e != cudaSuccess) return e;
+  CUtensorMap tw, th;
+  if (!encode_kmajor_bf16(&tw, p.W, p.V_local, p.d, kBK, kBN)) return cudaErrorInvalidValue;
+  if (!encode_kmajor_bf16(&th, p.h, p.B, p.d, kBK, kBM)) return cudaErrorInvalidValue;
+  const BatchGeometry g = batch_geometry(p.B, sms);
+  Problem ps = p;
+  Finish f{};
+  f.partials = partials;
+  f.n_parts = g.n_groups;
+  BatchArgs a{ps, nullptr, f, g.nbt, g.n_groups, static_cast<int>((p.V_local + kBN - 1) / kBN), err};
+  return launch_kernel(tc_batch_kernel<false, K>, dim3(g.grid), dim3(kThreads), smem_bytes(K), stream, ps.pdl, th,
+                       tw, a);
+}
+
+cudaError_t launch_tc_topk(const Problem& p, int K, Partial* partials, int* err, cudaStream_t stream) {
+  if (p.d < kBK || p.V_local <= 0) return cudaErrorNotSupported;
+  switch (K) {
+    case 4: return launch_topk_k<4>(p, partials, err, stream);
+    case 8: return launch_topk_k<8>(p, partials, err, stream);
+    case 16: return launch_topk_k<16>(p, partials, err, stream);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace fs

@@ -66,6 +66,11 @@ def test_host_side_argument_checks(built_library):
     assert lib.fs_sample_chunked(z, z, 4, 64, 0, 5, z, z, 0, 0, 0, z, z, 8, z, z, z) == 1
     assert lib.fs_set_path(7) == 1
     assert lib.fs_set_launch_overlap(2) == 1
+    # top-k: k outside [1, 16] is refused before anything else
+    assert lib.fs_sample_topk(z, z, 4, 64, 10, z, z, 0, 0, 0, 0, z, z, z) == 1
+    assert lib.fs_sample_topk(z, z, 4, 64, 10, z, z, 0, 0, 0, 17, z, z, z) == 1
+    assert "k must be" in lib.fs_last_error().decode()
+    assert lib.fs_sample_topk(z, z, 0, 64, 10, z, z, 0, 0, 0, 4, z, z, z) == 0   # B == 0
     # early finalization: batch limit, NaN bounds, bad chunk bounds
     assert lib.fs_sample_chunked_early(z, z, 4097, 64, 0, 5, z, z, 0, 0, 0, z, z, 1, z, 0.0, 0.0, z, z, z, z) == 2
     assert "B <= 4096" in lib.fs_last_error().decode()

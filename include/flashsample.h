@@ -190,6 +190,23 @@ FS_API fs_status fs_chunk_rest_norms(const void* W, int64_t d, const int64_t* bo
                                      float* rest_w_norm, void* stream);
 
 /*
+ * Tensor-parallel variant, final step (summary page, Method, third
+ * paragraph; abstract): each of R ranks samples its own vocabulary shard
+ * [v_begin, v_end) -- fs_sample_chunked with FS_CHUNK_FIRST | FS_CHUNK_LAST,
+ * so ids are global and the noise is that of the whole-vocabulary call --
+ * the ranks exchange only the per-row (max, id) pairs, and this call picks,
+ * per row, the best pair under the sampler's total order.  The result equals
+ * fs_sample over the whole vocabulary bit for bit (same kernel family for
+ * the same B).
+ *   shard_max [R, B] fp32 and shard_ids [R, B] int64 (device; shard r's row b
+ *   at r * B + b; id -1 = no sample from that shard).
+ *   out_ids [B] int64, out_max [B] fp32 (device); -1 / -inf when no shard has
+ *   a sample.  R == 0 gives -1 everywhere; B == 0 is a no-op.
+ */
+FS_API fs_status fs_combine_shards(const float* shard_max, const int64_t* shard_ids, int64_t R, int64_t B,
+                                   int64_t* out_ids, float* out_max, void* stream);
+
+/*
  * Gumbel-top-k: k ids per row drawn WITHOUT replacement from
  * softmax(logits / T) (each next id from the renormalized remaining mass),
  * fused into the LM-head matmul like fs_sample_ex.  The summary page cites

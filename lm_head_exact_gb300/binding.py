@@ -40,6 +40,7 @@ SIGNATURES = {
                                        _c_void_p, _c_void_p, _c_void_p]),
     "fs_row_norms": (_int, [_c_void_p, _i64, _i64, _c_void_p, _c_void_p]),
     "fs_chunk_rest_norms": (_int, [_c_void_p, _i64, _c_void_p, _i64, _c_void_p, _c_void_p]),
+    "fs_combine_shards": (_int, [_c_void_p, _c_void_p, _i64, _i64, _c_void_p, _c_void_p, _c_void_p]),
     "fs_sample_topk": (_int, [_c_void_p, _c_void_p, _i64, _i64, _i64, _c_void_p, _c_void_p, _i64,
                               _u64, _u64, _int, _c_void_p, _c_void_p, _c_void_p]),
     "fs_sample_unfused": (_int, [_c_void_p, _c_void_p, _i64, _i64, _i64, _c_void_p, _c_void_p, _i64,
@@ -180,6 +181,52 @@ def sample_unfused(h, W, temp, seed, step, bias=None, logits_out=None, out=None,
 def sample_ex(*args, **kwargs):
     """Alias of ``sample`` (the bias argument maps to fs_sample_ex)."""
     return sample(*args, **kwargs)
+
+
+def combine_shards(shard_max, shard_ids, out=None, stream=None):
+    """Tensor-parallel final step: per row, the best of the R shards' (max,
+    id) pairs (shard_max fp32 [R, B], shard_ids int64 [R, B], device).
+    Returns (ids int64 [B], max fp32 [B])."""
+    torch = _torch()
+    R, B = shard_max.shape
+    ids, mx = _outs(B, shard_max.device, out)
+    check(library().fs_combine_shards(
+        _dev(shard_max, "shard_max", torch.float32, 2), _dev(shard_ids, "shard_ids", torch.int64, 2), R, B,
+        _dev(ids, "out_ids"), _dev(mx, "out_max"), _stream_ptr(stream)))
+    return ids, mx
+
+
+def tp_exchange(local_max, local_ids, group=None):
+    """Exchange each rank's per-row (max, id) with the other ranks of
+    ``group``: 8 bytes per row per rank (the fp32 max's bits and the id as
+    int32), one all_gather.  Returns (all_max fp32 [R, B], all_ids int64
+    [R, B]) on the inputs' device.  Communication plumbing only (NCCL for CUDA
+    tensors, gloo for host tensors); the sample itself is computed by the
+    library's kernels."""
+    torch = _torch()
+    import torch.distributed as dist
+    R = dist.get_world_size(group)
+    packed = torch.stack([local_max.contiguous().view(torch.int32), local_ids.to(torch.int32)], dim=1)
+    parts = [torch.empty_like(packed) for _ in range(R)]
+    dist.all_gather(parts, packed, group=group)
+    allp = torch.stack(parts)
+    return allp[..., 0].contiguous().view(torch.float32), allp[..., 1].to(torch.int64)
+
+
+def sample_tp(h, W_shard, v_begin, temp, seed, step, group=None, bias_shard=None, stream=None):
+    """Tensor-parallel sample: this rank holds vocabulary rows [v_begin,
+    v_begin + W_shard.shape[0]); it samples its shard with global ids, the
+    ranks exchange the per-row (max, id) pairs, and the combine picks the
+    winner.  Every rank returns the same (ids, max), equal to sample() over
+    the whole vocabulary."""
+    torch = _torch()
+    B = h.shape[0]
+    cm = torch.empty(B, dtype=torch.float32, device=h.device)
+    ci = torch.empty(B, dtype=torch.int64, device=h.device)
+    local = sample_chunked(h, W_shard, v_begin, temp, seed, step, cm, ci, True, True, bias_chunk=bias_shard,
+                           stream=stream)
+    all_max, all_ids = tp_exchange(local[1], local[0], group=group)
+    return combine_shards(all_max, all_ids, stream=stream)
 
 
 def sample_topk(h, W, temp, seed, step, k, bias=None, out=None, stream=None):

@@ -551,6 +551,27 @@ fs_status fs_sample_host(const void* h_host, const void* W, int64_t B, int64_t d
   return FS_OK;
 }
 
+fs_status fs_combine_shards(const float* shard_max, const int64_t* shard_ids, int64_t R, int64_t B,
+                            int64_t* out_ids, float* out_max, void* stream) {
+  g_last_error[0] = '\0';
+  if (R < 0 || B < 0) return fail(FS_ERR_INVALID_ARG, "need R >= 0 and B >= 0 (got %lld, %lld)", (long long)R,
+                                  (long long)B);
+  if (B == 0) return FS_OK;
+  if (R > 0) {
+    FS_TRY(check_device_ptr(shard_max, "shard_max"));
+    FS_TRY(check_aligned(shard_max, 4, "shard_max"));
+    FS_TRY(check_device_ptr(shard_ids, "shard_ids"));
+    FS_TRY(check_aligned(shard_ids, 8, "shard_ids"));
+  }
+  FS_TRY(check_device_ptr(out_ids, "out_ids"));
+  FS_TRY(check_aligned(out_ids, 8, "out_ids"));
+  FS_TRY(check_device_ptr(out_max, "out_max"));
+  FS_TRY(check_aligned(out_max, 4, "out_max"));
+  cudaError_t e = launch_combine_shards(shard_max, shard_ids, R, B, out_ids, out_max, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "combine kernel launch");
+  return FS_OK;
+}
+
 fs_status fs_sample_topk(const void* h, const void* W, int64_t B, int64_t d, int64_t V,
                          const float* temp, const float* bias, int64_t bias_row_stride,
                          uint64_t seed, uint64_t step, int k,

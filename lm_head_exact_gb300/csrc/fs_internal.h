@@ -132,6 +132,10 @@ cudaError_t launch_tc_topk(const Problem& p, int K, Partial* partials, int* err,
 cudaError_t launch_topk_merge(const Partial* partials, int n_cand, int64_t B, int k, int64_t* out_ids, float* out_z,
                               cudaStream_t stream);
 
+// Tensor-parallel combine: out[b] = best over r of (shard_max[r, b], shard_ids[r, b]).
+cudaError_t launch_combine_shards(const float* shard_max, const int64_t* shard_ids, int64_t R, int64_t B,
+                                  int64_t* out_ids, float* out_max, cudaStream_t stream);
+
 cudaError_t launch_reduce(const Finish& f, int64_t B, cudaStream_t stream);
 
 // Set the calling thread's fs_last_error() text.

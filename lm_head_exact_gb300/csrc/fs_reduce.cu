@@ -34,6 +34,26 @@ reduce_kernel(Finish f, int64_t B) {
   if (lane == 0) write_row(f, b, best);
 }
 
+// Cross-shard combine of the tensor-parallel variant: row b's result is the
+// best of the R shards' (max, id) pairs under the total order (id -1 = none).
+__global__ void __launch_bounds__(kReduceThreads)
+combine_shards_kernel(const float* __restrict__ shard_max, const int64_t* __restrict__ shard_ids, int64_t R, int64_t B,
+                      int64_t* __restrict__ out_ids, float* __restrict__ out_max) {
+  const int64_t b = static_cast<int64_t>(blockIdx.x) * kReduceThreads + threadIdx.x;
+  if (b >= B) return;
+  Best best = best_none();
+  for (int64_t r = 0; r < R; ++r) {
+    const int64_t id = shard_ids[r * B + b];
+    if (id < 0 || id >= kNoId) continue;
+    Best c;
+    c.z = shard_max[r * B + b];
+    c.id = static_cast<int32_t>(id);
+    best = combine(best, c);
+  }
+  out_ids[b] = best.id == kNoId ? -1 : static_cast<int64_t>(best.id);
+  out_max[b] = best.id == kNoId ? -INFINITY : best.z;
+}
+
 // Gumbel-top-k merge, one 256-thread block per row over the row's n_cand
 // candidates (the per-CTA-group lists; ids unique, empty entries kNoId).
 // Each lane holds at most kMergePerLane candidates in registers.  Round j of
@@ -162,6 +182,16 @@ cudaError_t launch_reduce(const Finish& f, int64_t B, cudaStream_t stream) {
   if (B == 0) return cudaSuccess;
   const unsigned blocks = static_cast<unsigned>((B + kRowsPerBlock - 1) / kRowsPerBlock);
   reduce_kernel<<<blocks, kReduceThreads, 0, stream>>>(f, B);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine_shards(const float* shard_max, const int64_t* shard_ids, int64_t R, int64_t B,
+                                  int64_t* out_ids, float* out_max, cudaStream_t stream) {
+  if (B == 0) return cudaSuccess;
+  const int64_t blocks = (B + kReduceThreads - 1) / kReduceThreads;
+  if (blocks > 2147483647) return cudaErrorInvalidValue;
+  combine_shards_kernel<<<static_cast<unsigned>(blocks), kReduceThreads, 0, stream>>>(shard_max, shard_ids, R, B,
+                                                                                      out_ids, out_max);
   return cudaGetLastError();
 }
 

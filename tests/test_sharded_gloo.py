@@ -69,6 +69,41 @@ def test_sharded_combine_equals_one_shot(tmp_path):
     np.testing.assert_array_equal(got["zmax"], ref.zmax)
 
 
+def _exchange_worker(rank, world, port, out_path):
+    """The library's exchange step (binding.tp_exchange, 8 bytes per row per
+    rank over gloo) carrying oracle shard samples of uneven shards."""
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    from oracle import sampler
+    from lm_head_exact_gb300 import binding
+    h, W, temp = _problem()
+    V = W.shape[0]
+    bounds = {2: [0, 5, V], 3: [0, 5, 1400, V]}[world]
+    lo, hi = bounds[rank], bounds[rank + 1]
+    s = sampler.sample(h, W[lo:hi], temp, 77, 3, vocab_offset=lo)
+    local_max = torch.from_numpy(s.zmax.astype(np.float32))
+    all_max, all_ids = binding.tp_exchange(local_max, torch.from_numpy(s.ids))
+    assert all_max.shape == (world, len(s.ids)) and all_ids.dtype == torch.int64
+    acc = (np.full(len(s.ids), -1, np.int64), np.full(len(s.ids), -np.inf))
+    for r in range(world):
+        acc = sampler.combine(acc, (all_ids[r].numpy(), all_max[r].numpy().astype(np.float64)))
+    if rank == 0:
+        np.savez(out_path, ids=acc[0], zmax=acc[1])
+    dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("world", [2, 3])
+def test_tp_exchange_carries_the_shard_samples(tmp_path, world):
+    from oracle import sampler
+    out = str(tmp_path / "exchanged.npz")
+    mp.start_processes(_exchange_worker, args=(world, _free_port(), out), nprocs=world, start_method="spawn")
+    got = np.load(out)
+    h, W, temp = _problem()
+    ref = sampler.sample(h, W, temp, 77, 3)
+    np.testing.assert_array_equal(got["ids"], ref.ids)
+    np.testing.assert_array_equal(got["zmax"], ref.zmax.astype(np.float32).astype(np.float64))
+
+
 def _timing_worker(rank, world, port, out_path):
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
     dist.init_process_group("gloo", rank=rank, world_size=world)

@@ -59,21 +59,38 @@ __device__ __forceinline__ void push_candidate(const Finish& f, int64_t b, Best 
   if (c.id != kNoId) atomicMax(f.keys + b, pack_key(c.z, c.id));
 }
 
+// Barrier over the 128 / 256 epilogue threads (named barrier 1) that also
+// ANDs a predicate over them.
+template <int kCount>
+__device__ __forceinline__ bool named_bar1_and(bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.and.pred q, 1, %2, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(pred)), "n"(kCount)
+      : "memory");
+  return r != 0;
+}
+
+__device__ __forceinline__ bool cta_bar_and(bool pred) { return __syncthreads_and(pred) != 0; }
+
 // Called by the n participating threads (index tid) of every CTA after they
-// pushed all of this CTA's candidates.  `bar()` synchronizes exactly those
-// threads; `flag` is a shared-memory int.  The last CTA of the grid writes
-// rows [0, B) and leaves keys and ticket at zero.  kEarly = false compiles out
-// the early-finalization flag (callers that never set Finish::done and whose
-// register count matters).
-template <bool kEarly = true, class Bar>
-__device__ __forceinline__ void finish_grid(const Finish& f, int64_t B, int tid, int n, int* flag, Bar bar) {
+// pushed all of this CTA's candidates.  `bar_and(p)` synchronizes exactly
+// those threads and returns the AND of their p; `flag` is a shared-memory
+// int.  The last CTA of the grid writes rows [0, B) and leaves keys and
+// ticket at zero.  kEarly = false compiles out the early-finalization flag
+// (callers that never set Finish::done and whose register count matters).
+// The flag needs no fence of its own: a later chunk reads the carry only
+// after its dependency wait (or in stream order).
+template <bool kEarly = true, class BarAnd>
+__device__ __forceinline__ void finish_grid(const Finish& f, int64_t B, int tid, int n, int* flag, BarAnd bar_and) {
   __threadfence();
-  bar();
+  bar_and(true);
   if (tid == 0) {
     const unsigned total = gridDim.x * gridDim.y * gridDim.z;
     *flag = atomicAdd(f.counter, 1u) == total - 1;
   }
-  bar();
+  bar_and(true);
   if (*flag) {
     __threadfence();
     bool all_final = true;
@@ -82,15 +99,8 @@ __device__ __forceinline__ void finish_grid(const Finish& f, int64_t B, int tid,
       if (kEarly && f.done != nullptr) all_final = all_final && row_final(f, b, best);
     }
     if (kEarly && f.done != nullptr) {
-      bar();                                   // every thread has read *flag
-      if (tid == 0) *flag = 1;
-      bar();
-      if (!all_final) *flag = 0;
-      bar();
-      if (tid == 0) {
-        __threadfence();                       // carry writes of this CTA before the flag
-        *f.done = *flag;
-      }
+      all_final = bar_and(all_final);
+      if (tid == 0) *f.done = all_final ? 1 : 0;
     }
     if (tid == 0) atomicExch(f.counter, 0u);
   }
@@ -102,10 +112,12 @@ __device__ __forceinline__ void finish_grid(const Finish& f, int64_t B, int tid,
 // valid for every later chunk.  With a programmatic dependent launch the
 // previous chunk may set it while this grid's CTAs start, so different CTAs
 // of one grid may read different values: every CTA must stay correct alone.
+// A relaxed load is enough: the decision only chooses whether to compute, and
+// the carry is read after the dependency wait (or in stream order).
 __device__ __forceinline__ bool early_done(const Finish& f) {
   if (f.done == nullptr || !f.carry_in) return false;
   int v;
-  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(f.done) : "memory");
+  asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(f.done) : "memory");
   return v != 0;
 }
 
@@ -127,7 +139,7 @@ __device__ __forceinline__ bool early_done_cta(const Finish& f, int* slot) {
 __device__ __forceinline__ void early_skip_cta(const Finish& f, int64_t B, bool pdl, int* flag) {
   pdl_launch_dependents();
   if (pdl) pdl_wait();                         // the finish area is shared with the previous launch
-  finish_grid(f, B, threadIdx.x, blockDim.x, flag, [] { __syncthreads(); });
+  finish_grid(f, B, threadIdx.x, blockDim.x, flag, cta_bar_and);
 }
 
 }  // namespace fs

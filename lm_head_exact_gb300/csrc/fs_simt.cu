@@ -145,7 +145,7 @@ simt_fused_kernel(Problem p, Finish f) {
       push_candidate(f, b0 + threadIdx.x, r);
     }
   }
-  finish_grid<kEarly>(f, p.B, threadIdx.x, kSimtThreads, &last_flag, [] { __syncthreads(); });
+  finish_grid<kEarly>(f, p.B, threadIdx.x, kSimtThreads, &last_flag, cta_bar_and);
 }
 
 int pick_group(int64_t B, int64_t d) {

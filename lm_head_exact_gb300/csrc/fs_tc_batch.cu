@@ -304,7 +304,7 @@ tc_batch_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_constan
       pdl_wait();                 // the finish area is shared with the previous launch
       if (half == 0 && row_ok) push_candidate(args.f, b, combine(best, half_best[row_in_tile]));
       finish_grid(args.f, p.B, threadIdx.x, kEpiWarps * 32, last_flag,
-                  [] { asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory"); });
+                  named_bar1_and<kEpiWarps * 32>);
     }
   }
 

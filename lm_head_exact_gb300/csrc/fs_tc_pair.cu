@@ -24,6 +24,7 @@
 #include <cuda.h>
 
 #include <algorithm>
+#include <atomic>
 
 #include "fs_epilogue.cuh"
 #include "fs_finish.cuh"
@@ -262,7 +263,7 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_constant
     pdl_wait();                   // the finish area is shared with the previous launch
     if (half == 0 && row_ok) push_candidate(args.f, b, combine(best, half_best[row_in_tile]));
     finish_grid(args.f, p.B, threadIdx.x, kEpiWarps * 32, last_flag,
-                [] { asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory"); });
+                named_bar1_and<kEpiWarps * 32>);
   }
 
   // ---- teardown: neither CTA leaves (or frees TMEM) while the pair's MMAs or
@@ -280,8 +281,11 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_constant
 // so with GPCs of odd SM counts this can be below SMs / 2.  A persistent grid
 // larger than that would run its last pairs as a second wave.
 static int resident_pairs(int dev, int sms) {
-  static int cached[64] = {0};
-  if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
+  static std::atomic<int> cached[64];         // zero-initialized (static storage)
+  if (dev >= 0 && dev < 64) {
+    const int c = cached[dev].load(std::memory_order_relaxed);
+    if (c > 0) return c;
+  }
   int n = 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(2 * (sms / 2)));
@@ -292,7 +296,7 @@ static int resident_pairs(int dev, int sms) {
     n = sms / 2;
   }
   n = std::min(n, sms / 2);
-  if (dev >= 0 && dev < 64) cached[dev] = n;
+  if (dev >= 0 && dev < 64) cached[dev].store(n, std::memory_order_relaxed);
   return n;
 }
 

@@ -336,7 +336,7 @@ tc_vocab_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
       push_candidate(args.f, b, r);
     }
     finish_grid(args.f, B, threadIdx.x, kEpiWarps * 32, last_flag,
-                [] { asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory"); });
+                named_bar1_and<kEpiWarps * 32>);
   }
 
   // ---- teardown

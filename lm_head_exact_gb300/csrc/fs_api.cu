@@ -592,7 +592,10 @@ fs_status fs_sample_topk(const void* h, const void* W, int64_t B, int64_t d, int
   // wait, h / temp / bias read and the shared partials written after it
   p.pdl = g_launch_overlap.load() != 0;
   p.defer_inputs = p.pdl;
-  const int parts = V > 0 ? tc_topk_parts(B, dev) : 0;
+  // B <= 32: the vocabulary-major kernel (one lane per batch column keeps the
+  // lists); larger B: the batch-major kernel (one thread per batch row).
+  const bool vocab_major = B <= 32;
+  const int parts = V <= 0 ? 0 : (vocab_major ? tc_vocab_topk_parts(V, dev) : tc_topk_parts(B, dev));
   const size_t need = std::max<size_t>(static_cast<size_t>(B) * parts * K * sizeof(Partial), 256);
   Partial* partials = nullptr;
   {
@@ -605,10 +608,10 @@ fs_status fs_sample_topk(const void* h, const void* W, int64_t B, int64_t d, int
   if (V > 0) {
     int* err = nullptr;
     FS_TRY(error_word(&err));
-    e = launch_tc_topk(p, K, partials, err, stream);
+    e = vocab_major ? launch_tc_vocab_topk(p, K, partials, err, stream) : launch_tc_topk(p, K, partials, err, stream);
     if (e != cudaSuccess) return cuda_fail(e, "top-k kernel launch");
   }
-  e = launch_topk_merge(partials, parts * K, B, k, out_ids, out_z, stream);
+  e = launch_topk_merge(partials, parts, K, B, k, out_ids, out_z, stream);
   if (e != cudaSuccess) return cuda_fail(e, "top-k merge launch");
   return FS_OK;
 }

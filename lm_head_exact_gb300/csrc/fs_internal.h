@@ -126,11 +126,16 @@ cudaError_t launch_row_norms(const void* X, int64_t n, int64_t d, float* out, un
 // Gumbel-top-k: the batch-major kernel in top-K mode (K in {4, 8, 16}, one
 // launch, B <= one launch's rows) writes per-(row, CTA group) lists to
 // partials [B, tc_topk_parts(B), K]; launch_topk_merge then merges each row's
-// lists into its k <= K best (out_ids / out_z [B, k]; -1 / -inf padded).
+// lists (n_lists <= 256 per row, each sorted) into its k <= K best
+// (out_ids / out_z [B, k]; -1 / -inf padded).
 int tc_topk_parts(int64_t B, int device);
 cudaError_t launch_tc_topk(const Problem& p, int K, Partial* partials, int* err, cudaStream_t stream);
-cudaError_t launch_topk_merge(const Partial* partials, int n_cand, int64_t B, int k, int64_t* out_ids, float* out_z,
-                              cudaStream_t stream);
+// The vocabulary-major kernel in top-K mode, for B <= 32: partials [B,
+// tc_vocab_topk_parts(V), K] (one list per (row, CTA)).
+int tc_vocab_topk_parts(int64_t V, int device);
+cudaError_t launch_tc_vocab_topk(const Problem& p, int K, Partial* partials, int* err, cudaStream_t stream);
+cudaError_t launch_topk_merge(const Partial* partials, int n_lists, int K, int64_t B, int k, int64_t* out_ids,
+                              float* out_z, cudaStream_t stream);
 
 // Tensor-parallel combine: out[b] = best over r of (shard_max[r, b], shard_ids[r, b]).
 cudaError_t launch_combine_shards(const float* shard_max, const int64_t* shard_ids, int64_t R, int64_t B,

@@ -54,88 +54,79 @@ combine_shards_kernel(const float* __restrict__ shard_max, const int64_t* __rest
   out_max[b] = best.id == kNoId ? -INFINITY : best.z;
 }
 
-// Gumbel-top-k merge, one 256-thread block per row over the row's n_cand
-// candidates (the per-CTA-group lists; ids unique, empty entries kNoId).
-// Each lane holds at most kMergePerLane candidates in registers.  Round j of
-// a selection picks the best candidate that ranks after the one picked in
-// round j - 1 (warp shuffles only), so k rounds give the k best in order.
-// Level 1: each warp selects the k best of its slice of the candidates into
-// shared memory; level 2: warp 0 selects the k best of those 8 k.
+// Gumbel-top-k merge, one 256-thread block per row over the row's n_lists
+// lists of K candidates each (one per CTA, each already sorted best first;
+// ids unique across lists, empty entries kNoId).  Lane l of warp w holds list
+// 32 w + l in registers.  Level 1: each warp merges its 32 lists -- k rounds
+// of a warp argmax over the list heads, the owner of the winning head drops
+// it -- into a sorted list of k in shared memory.  Level 2: warp 0 merges the
+// 8 warps' lists the same way.  The output is the row's k best in order.
 constexpr int kMergeThreads = 256;
 constexpr int kMergeWarps = kMergeThreads / 32;
-constexpr int kMergePerLane = 12;
-constexpr int kTopKMaxList = 16;
 
-__device__ __forceinline__ Best select_after(const float (&cz)[kMergePerLane], const int32_t (&ci)[kMergePerLane],
-                                             float pz, int32_t pid) {
-  Best best = best_none();
+template <int K>
+__device__ __forceinline__ void drop_head(float (&lz)[K], int32_t (&li)[K]) {
 #pragma unroll
-  for (int i = 0; i < kMergePerLane; ++i)
-    if (ci[i] != kNoId && beats(pz, pid, cz[i], ci[i]) && beats(cz[i], ci[i], best.z, best.id)) {
-      best.z = cz[i];
-      best.id = ci[i];
-    }
-  return warp_combine(best);
+  for (int i = 0; i + 1 < K; ++i) {
+    lz[i] = lz[i + 1];
+    li[i] = li[i + 1];
+  }
+  lz[K - 1] = -INFINITY;
+  li[K - 1] = kNoId;
 }
 
+// k rounds of a warp-wide merge of the lanes' sorted lists; calls
+// emit(j, winner) on every lane.
+template <int K, class Emit>
+__device__ __forceinline__ void warp_merge(float (&lz)[K], int32_t (&li)[K], int k, Emit emit) {
+  for (int j = 0; j < k; ++j) {
+    Best h;
+    h.z = lz[0];
+    h.id = li[0];
+    if (h.id == kNoId) h = best_none();
+    const Best w = warp_combine(h);
+    emit(j, w);
+    if (w.id != kNoId && li[0] == w.id) drop_head(lz, li);
+  }
+}
+
+template <int K>
 __global__ void __launch_bounds__(kMergeThreads)
-topk_merge_kernel(const Partial* __restrict__ partials, int n_cand, int k, int64_t* __restrict__ out_ids,
+topk_merge_kernel(const Partial* __restrict__ partials, int n_lists, int k, int64_t* __restrict__ out_ids,
                   float* __restrict__ out_z) {
-  __shared__ Best level1[kMergeWarps][kTopKMaxList];
+  __shared__ Best level1[kMergeWarps][K];
   pdl_launch_dependents();      // the next call's kernel may start its W prefetch
   pdl_wait();                   // launched as a dependent of the kernel that wrote the partials
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   const int64_t b = blockIdx.x;
-  const Partial* row = partials + b * n_cand;
-  // this warp's slice of the candidates, strided over its lanes
-  const int per_warp = (n_cand + kMergeWarps - 1) / kMergeWarps;
-  const int lo = warp * per_warp;
-  const int hi = min(n_cand, lo + per_warp);
-  float cz[kMergePerLane];
-  int32_t ci[kMergePerLane];
+  float lz[K];
+  int32_t li[K];
+  const bool has_list = static_cast<int>(threadIdx.x) < n_lists;
+  const Partial* mine = partials + (b * n_lists + threadIdx.x) * K;
 #pragma unroll
-  for (int i = 0; i < kMergePerLane; ++i) {
-    const int j = lo + lane + 32 * i;
-    if (j < hi) {
-      const Partial c = row[j];
-      cz[i] = c.z;
-      ci[i] = c.id;
-    } else {
-      cz[i] = -INFINITY;
-      ci[i] = kNoId;
-    }
+  for (int j = 0; j < K; ++j) {
+    const Partial c = has_list ? mine[j] : Partial{-INFINITY, kNoId};
+    lz[j] = c.z;
+    li[j] = c.id;
   }
-  float pz = INFINITY;          // (+inf, -1) ranks before every candidate
-  int32_t pid = -1;
-  for (int j = 0; j < k; ++j) {
-    const Best w = select_after(cz, ci, pz, pid);
+  warp_merge(lz, li, k, [&](int j, Best w) {
     if (lane == 0) level1[warp][j] = w;
-    pz = w.z;
-    pid = w.id;
-  }
+  });
   __syncthreads();
   if (warp == 0) {
-    // level 2: the 8 k level-1 entries, at most 4 per lane
 #pragma unroll
-    for (int i = 0; i < kMergePerLane; ++i) {
-      const int j = lane + 32 * i;
-      const bool ok = i < 4 && j < kMergeWarps * k;
-      const Best c = ok ? level1[j / k][j % k] : best_none();
-      cz[i] = c.z;
-      ci[i] = c.id;
+    for (int j = 0; j < K; ++j) {
+      const Best c = (lane < kMergeWarps && j < k) ? level1[lane][j] : best_none();
+      lz[j] = c.z;
+      li[j] = c.id;
     }
-    pz = INFINITY;
-    pid = -1;
-    for (int j = 0; j < k; ++j) {
-      const Best w = select_after(cz, ci, pz, pid);
+    warp_merge(lz, li, k, [&](int j, Best w) {
       if (lane == 0) {
         out_ids[b * k + j] = w.id == kNoId ? -1 : static_cast<int64_t>(w.id);
         out_z[b * k + j] = w.id == kNoId ? -INFINITY : w.z;
       }
-      pz = w.z;
-      pid = w.id;
-    }
+    });
   }
 }
 
@@ -195,13 +186,17 @@ cudaError_t launch_combine_shards(const float* shard_max, const int64_t* shard_i
   return cudaGetLastError();
 }
 
-cudaError_t launch_topk_merge(const Partial* partials, int n_cand, int64_t B, int k, int64_t* out_ids, float* out_z,
-                              cudaStream_t stream) {
+cudaError_t launch_topk_merge(const Partial* partials, int n_lists, int K, int64_t B, int k, int64_t* out_ids,
+                              float* out_z, cudaStream_t stream) {
   if (B == 0) return cudaSuccess;
-  if (k < 1 || k > kTopKMaxList || n_cand > kMergeThreads * kMergePerLane || B > 2147483647)
-    return cudaErrorInvalidValue;
-  return launch_kernel(topk_merge_kernel, dim3(static_cast<unsigned>(B)), dim3(kMergeThreads), 0, stream, true,
-                       partials, n_cand, k, out_ids, out_z);
+  if (k < 1 || k > K || n_lists > kMergeThreads || B > 2147483647) return cudaErrorInvalidValue;
+  const dim3 grid(static_cast<unsigned>(B));
+  switch (K) {
+    case 4: return launch_kernel(topk_merge_kernel<4>, grid, dim3(kMergeThreads), 0, stream, true, partials, n_lists, k, out_ids, out_z);
+    case 8: return launch_kernel(topk_merge_kernel<8>, grid, dim3(kMergeThreads), 0, stream, true, partials, n_lists, k, out_ids, out_z);
+    case 16: return launch_kernel(topk_merge_kernel<16>, grid, dim3(kMergeThreads), 0, stream, true, partials, n_lists, k, out_ids, out_z);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 cudaError_t launch_debug_noise(uint64_t seed, uint64_t step, int64_t row0, int64_t n_rows,

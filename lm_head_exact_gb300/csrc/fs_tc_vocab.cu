@@ -49,7 +49,9 @@ constexpr int kBM = 128;          // vocabulary rows per tile (MMA M)
 constexpr int kBK = 64;           // K per stage: one 128-byte swizzle row of bf16
 constexpr int kATileBytes = kBM * kBK * 2;
 
-template <int BN>
+// kTopK > 0: Gumbel-top-k mode (BN <= 32): per-lane K-lists, one list per
+// (row, CTA) written to partials, no in-kernel finish.
+template <int BN, int kTopK = 0>
 struct VocabCfg {
   static constexpr int kBTileBytes = BN * kBK * 2;
   static constexpr int kStageBytes = kATileBytes + kBTileBytes;
@@ -58,10 +60,13 @@ struct VocabCfg {
   static constexpr int kTmemCols = (2 * BN < 32) ? 32 : 2 * BN;     // two accumulators
   // everything but the stage ring: barriers (<= 29), tmem base / flags,
   // per-column 1/T and mode, per-warp bests, transpose tiles, alignment slack
-  static constexpr int kFixedBytes = 29 * 8 + 16 + BN * 8 + kEpiWarps * BN * 8 + kEpiWarps * 32 * 33 * 4 + 1024;
+  static constexpr int kTopKBytes = kTopK > 0 ? kEpiWarps * BN * kTopK * 8 : 0;   // per-warp lists
+  static constexpr int kFixedBytes =
+      29 * 8 + 16 + BN * 8 + kEpiWarps * BN * 8 + kEpiWarps * 32 * 33 * 4 + kTopKBytes + 1024;
   // Resident CTAs per SM: two for narrow batches (measured ~2% faster on
   // GB300 for B <= 32: two independent TMA streams per SM), one otherwise.
-  static constexpr int kCtasPerSm = BN <= 32 ? 2 : 1;
+  // (Top-k lists need the registers: one CTA per SM there.)
+  static constexpr int kCtasPerSm = (BN <= 32 && kTopK == 0) ? 2 : 1;
   static constexpr int kStages = std::min(12, (225 * 1024 / kCtasPerSm - kFixedBytes) / kStageBytes);
   // shared memory carve-up (offsets from a 1024-byte aligned base)
   static constexpr int kOffA = 0;
@@ -73,7 +78,8 @@ struct VocabCfg {
   static constexpr int kOffMode = kOffInvT + BN * 4;
   static constexpr int kOffBest = kOffMode + BN * 4;
   static constexpr int kOffTr = kOffBest + kEpiWarps * BN * 8;     // per-warp 32 x 33 transpose tiles
-  static constexpr int kSmemBytes = kOffTr + kEpiWarps * 32 * 33 * 4 + 1024;   // + alignment slack
+  static constexpr int kOffTopK = kOffTr + kEpiWarps * 32 * 33 * 4;
+  static constexpr int kSmemBytes = kOffTopK + kTopKBytes + 1024;   // + alignment slack
 };
 
 struct VocabArgs {
@@ -83,11 +89,12 @@ struct VocabArgs {
   int* err;
 };
 
-template <int BN>
-__global__ void __launch_bounds__(kThreads, VocabCfg<BN>::kCtasPerSm)
+template <int BN, int kTopK = 0>
+__global__ void __launch_bounds__(kThreads, VocabCfg<BN, kTopK>::kCtasPerSm)
 tc_vocab_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_h,
                 const VocabArgs args) {
-  using C = VocabCfg<BN>;
+  using C = VocabCfg<BN, kTopK>;
+  static_assert(kTopK == 0 || C::kChunks == 1, "top-k lists: one accumulator chunk per lane");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + C::kOffBars);
@@ -98,7 +105,7 @@ tc_vocab_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
   uint32_t* tmem_base_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
   int* last_flag = reinterpret_cast<int*>(smem + C::kOffMisc + 8);
-  if (early_done_cta(args.f, last_flag)) {
+  if (kTopK == 0 && early_done_cta(args.f, last_flag)) {
     early_skip_cta(args.f, args.p.B, args.p.pdl, last_flag);
     return;
   }
@@ -258,6 +265,8 @@ tc_vocab_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
     float* tr = tr_all + warp * 32 * 33;
     float best_z[C::kChunks];
     int32_t best_id[C::kChunks];
+    TopList<(kTopK > 0 ? kTopK : 1)> list;       // top-k mode: this lane's column (kChunks == 1)
+    topk_init(list);
 #pragma unroll
     for (int c = 0; c < C::kChunks; ++c) {
       best_z[c] = -INFINITY;
@@ -300,43 +309,75 @@ tc_vocab_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
             const float* col = tr + lane * 33;
 #pragma unroll
             for (int i = 0; i < 32; ++i) vals[i] = __float_as_uint(col[i]);
-            Best bb;
-            bb.z = best_z[c];
-            bb.id = best_id[c];
             const int64_t row_end = row0 + n_rows;
-            if (scan.bias_row != nullptr)
-              scan32<true>(vals, row0, row_end, p.v_offset, scan, bb);
-            else
-              scan32<false>(vals, row0, row_end, p.v_offset, scan, bb);
-            best_z[c] = bb.z;
-            best_id[c] = bb.id;
+            if constexpr (kTopK > 0) {
+              if (scan.bias_row != nullptr)
+                scan32_topk<true>(vals, row0, row_end, p.v_offset, scan, list);
+              else
+                scan32_topk<false>(vals, row0, row_end, p.v_offset, scan, list);
+            } else {
+              Best bb;
+              bb.z = best_z[c];
+              bb.id = best_id[c];
+              if (scan.bias_row != nullptr)
+                scan32<true>(vals, row0, row_end, p.v_offset, scan, bb);
+              else
+                scan32<false>(vals, row0, row_end, p.v_offset, scan, bb);
+              best_z[c] = bb.z;
+              best_id[c] = bb.id;
+            }
           }
         }
       }
       tc_fence_before();
       mbar_arrive(&tempty_bar[acc]);
     }
-    pdl_wait();                   // the finish area is shared with the previous launch
+    if constexpr (kTopK > 0) {
+      // merge the 4 epilogue warps' lists of each column, one list per (row, CTA)
+      Partial* lists = reinterpret_cast<Partial*>(smem + C::kOffTopK);   // [kEpiWarps][BN][kTopK]
+      if (lane < C::kChunk && lane < B) {
 #pragma unroll
-    for (int c = 0; c < C::kChunks; ++c) {
-      const int b = c * C::kChunk + lane;
-      if (lane < C::kChunk && b < B) {
-        Best bb;
-        bb.z = best_z[c];
-        bb.id = best_id[c];
-        warp_best[warp * BN + b] = bb;
+        for (int j = 0; j < kTopK; ++j) lists[(warp * BN + lane) * kTopK + j] = Partial{list.z[j], list.id[j]};
       }
-    }
-    // combine the 4 epilogue warps, push one candidate per (batch row, CTA)
-    asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
-    for (int b = threadIdx.x; b < B; b += kEpiWarps * 32) {
-      Best r = warp_best[b];
+      asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
+      pdl_wait();                 // the previous call's merge kernel may still read the partials
+      for (int b = threadIdx.x; b < B; b += kEpiWarps * 32) {
+        TopList<(kTopK > 0 ? kTopK : 1)> m;
 #pragma unroll
-      for (int w = 1; w < kEpiWarps; ++w) r = combine(r, warp_best[w * BN + b]);
-      push_candidate(args.f, b, r);
+        for (int j = 0; j < kTopK; ++j) {
+          m.z[j] = lists[b * kTopK + j].z;
+          m.id[j] = lists[b * kTopK + j].id;
+        }
+        for (int w = 1; w < kEpiWarps; ++w) {
+#pragma unroll
+          for (int j = 0; j < kTopK; ++j) topk_offer(m, lists[(w * BN + b) * kTopK + j].z, lists[(w * BN + b) * kTopK + j].id);
+        }
+        Partial* dst = args.f.partials + (static_cast<int64_t>(b) * args.f.n_parts + blockIdx.x) * kTopK;
+#pragma unroll
+        for (int j = 0; j < kTopK; ++j) dst[j] = Partial{m.z[j], m.id[j]};
+      }
+    } else {
+      pdl_wait();                 // the finish area is shared with the previous launch
+#pragma unroll
+      for (int c = 0; c < C::kChunks; ++c) {
+        const int b = c * C::kChunk + lane;
+        if (lane < C::kChunk && b < B) {
+          Best bb;
+          bb.z = best_z[c];
+          bb.id = best_id[c];
+          warp_best[warp * BN + b] = bb;
+        }
+      }
+      // combine the 4 epilogue warps, push one candidate per (batch row, CTA)
+      asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
+      for (int b = threadIdx.x; b < B; b += kEpiWarps * 32) {
+        Best r = warp_best[b];
+#pragma unroll
+        for (int w = 1; w < kEpiWarps; ++w) r = combine(r, warp_best[w * BN + b]);
+        push_candidate(args.f, b, r);
+      }
+      finish_grid(args.f, B, threadIdx.x, kEpiWarps * 32, last_flag, named_bar1_and<kEpiWarps * 32>);
     }
-    finish_grid(args.f, B, threadIdx.x, kEpiWarps * 32, last_flag,
-                named_bar1_and<kEpiWarps * 32>);
   }
 
   // ---- teardown
@@ -347,15 +388,15 @@ tc_vocab_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
 }
 
 // ------------------------------------------------------------------ host side
-template <int BN>
+template <int BN, int kTopK = 0>
 cudaError_t launch_bn(const Problem& p, const Finish& f, int* err, cudaStream_t stream) {
-  using C = VocabCfg<BN>;
+  using C = VocabCfg<BN, kTopK>;
   static_assert(C::kStages >= 2, "pipeline needs at least two stages");
   static_assert(C::kSmemBytes * C::kCtasPerSm <= 228 * 1024, "shared memory budget");
   CUtensorMap tw, th;
   if (!encode_kmajor_bf16(&tw, p.W, p.V_local, p.d, kBK, kBM)) return cudaErrorInvalidValue;
   if (!encode_kmajor_bf16(&th, p.h, p.B, p.d, kBK, BN)) return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(tc_vocab_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(tc_vocab_kernel<BN, kTopK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::kSmemBytes);
   if (e != cudaSuccess) return e;
   int dev = 0, sms = 0;
@@ -365,7 +406,7 @@ cudaError_t launch_bn(const Problem& p, const Finish& f, int* err, cudaStream_t 
   const int64_t n_vt = (p.V_local + kBM - 1) / kBM;
   const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(C::kCtasPerSm * sms, n_vt)));
   VocabArgs a{p, f, n_vt, err};
-  return launch_kernel(tc_vocab_kernel<BN>, dim3(grid), dim3(kThreads), C::kSmemBytes, stream, p.pdl, tw, th, a);
+  return launch_kernel(tc_vocab_kernel<BN, kTopK>, dim3(grid), dim3(kThreads), C::kSmemBytes, stream, p.pdl, tw, th, a);
 }
 
 }  // namespace
@@ -383,6 +424,34 @@ cudaError_t launch_tc_vocab(const Problem& p, const Finish& f, int* err, cudaStr
     case 128: return launch_bn<128>(p, f, err, stream);
     default: return launch_bn<256>(p, f, err, stream);
   }
+}
+
+int tc_vocab_topk_parts(int64_t V, int device) {
+  int sms = 0;
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
+  if (sms <= 0) sms = 148;
+  const int64_t n_vt = (V + kBM - 1) / kBM;
+  return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(sms, n_vt)));
+}
+
+template <int BN>
+static cudaError_t launch_topk_bn(const Problem& p, int K, const Finish& f, int* err, cudaStream_t stream) {
+  switch (K) {
+    case 4: return launch_bn<BN, 4>(p, f, err, stream);
+    case 8: return launch_bn<BN, 8>(p, f, err, stream);
+    case 16: return launch_bn<BN, 16>(p, f, err, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_tc_vocab_topk(const Problem& p, int K, Partial* partials, int* err, cudaStream_t stream) {
+  if (p.B > 32 || p.d < kBK || p.V_local <= 0) return cudaErrorNotSupported;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  Finish f{};
+  f.partials = partials;
+  f.n_parts = tc_vocab_topk_parts(p.V_local, dev);
+  return p.B <= 16 ? launch_topk_bn<16>(p, K, f, err, stream) : launch_topk_bn<32>(p, K, f, err, stream);
 }
 
 }  // namespace fs

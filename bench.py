@@ -288,6 +288,14 @@ def run_ours(args):
     fs.workspace_reserve(bmax, V, stream=stream)
 
     hd, td = hd_all[:B], temp_all[:B]
+
+    def want(section):
+        """Extra measurements after the headline: all unless --no-sweep, or
+        only those named by --only."""
+        if args.only:
+            return section in args.only.split(",")
+        return not args.no_sweep
+
     # warm-up (untimed)
     time_steps(fs, torch, hd, Wd, td, seed, 0, args.warmup, stream, events=False)
     clocks = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
@@ -330,8 +338,18 @@ def run_ours(args):
     # batch sweeps of the metric (same kernels, fewer steps per point): the
     # Llama-3-8B head over the decode range and the large-batch tensor-core
     # range, and the Qwen3-8B head's large batches
+    big = max(SWEEP_LARGE)
+    big_inputs = {}
+
+    def big_batch():
+        """h rows and temperatures for the large-batch points (made once)."""
+        if not big_inputs:
+            big_inputs["h"] = _to_dev(synthetic.normal_rows_bf16(synthetic.SEED_H, big, d, 1.0), torch)
+            big_inputs["t"] = torch.ones(big, dtype=torch.float32, device="cuda")
+        return big_inputs["h"], big_inputs["t"]
+
     sweep = []
-    if not args.no_sweep:
+    if want("sweep"):
         def point(kind, b, hdev, Wdev, tdev, Vk, dk):
             time_steps(fs, torch, hdev[:b], Wdev, tdev[:b], seed, 0, 3, stream, events=False)
             tot, _ = time_steps(fs, torch, hdev[:b], Wdev, tdev[:b], seed, 3, 20, stream, events=False)
@@ -342,9 +360,7 @@ def run_ours(args):
                     "fused_kernel_us_isolated": round(km * 1e3, 2), "roofline_us": rf["roofline_us"],
                     "frac": rf["frac"], "bound": rf["bound"], "path": fs.path_for_batch(b)}
 
-        big = max(SWEEP_LARGE)
-        h_big = _to_dev(synthetic.normal_rows_bf16(synthetic.SEED_H, big, d, 1.0), torch)
-        t_big = torch.ones(big, dtype=torch.float32, device="cuda")
+        h_big, t_big = big_batch()
         for b in SWEEP:
             sweep.append(point(kind, b, hd_all, Wd, temp_all, V, d))
         for b in SWEEP_LARGE:
@@ -381,7 +397,7 @@ def run_ours(args):
         return e0.elapsed_time(e1) / reps * 1e3
 
     chunked = []
-    if not args.no_sweep:
+    if want("chunked"):
         for b in synthetic.SHAPES["chunked"]["batches"]:
             for n in (8, 32):
                 bounds = synthetic.chunk_bounds(V, n)
@@ -407,7 +423,7 @@ def run_ours(args):
     # chunk ("spiked", the later chunks skip their work); the plain chunked
     # step on the same inputs beside it.  The step includes the h row norms.
     early = []
-    if not args.no_sweep:
+    if want("early"):
         n = 8
         bounds = synthetic.chunk_bounds(V, n)
         rest = fs.chunk_rest_norms(Wd, bounds, stream=stream)
@@ -449,13 +465,12 @@ def run_ours(args):
                               "launches_per_step": n + 1, "cuda_graph": True})
                 del chunks, bias
 
-    # Gumbel-top-k (k ids per row without replacement) on the same head:
-    # the batch-major kernel with a per-row list epilogue + a merge launch
+    # Gumbel-top-k (k ids per row without replacement) on the same head: a
+    # tensor-core kernel with a per-row list epilogue + a merge launch
     topk = []
-    if not args.no_sweep:
+    if want("topk"):
         for b, k in ((1, 8), (16, 8), (16, 16), (64, 8), (256, 8), (1024, 4)):
-            hsrc = hd_all if b <= bmax else h_big
-            tsrc = temp_all if b <= bmax else t_big
+            hsrc, tsrc = (hd_all, temp_all) if b <= bmax else big_batch()
             ids_k = torch.empty((b, k), dtype=torch.int64, device="cuda")
             z_k = torch.empty((b, k), dtype=torch.float32, device="cuda")
             with torch.cuda.stream(stream):
@@ -476,7 +491,7 @@ def run_ours(args):
     # the unfused comparison pipeline on the same workload: GEMM -> fp32
     # logits in HBM -> softmax -> sample (the traffic fusion removes)
     unfused = None
-    if not args.no_sweep:
+    if want("unfused"):
         with torch.cuda.stream(stream):
             for i in range(3):
                 fs.sample_unfused(hd, Wd, td, seed, i, stream=stream)
@@ -616,6 +631,7 @@ def parse_args(argv=None):
     ap.add_argument("--batch", type=int, default=16)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--only", default="", help="comma list of extra sections: sweep,chunked,early,topk,unfused")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
     args = ap.parse_args(argv)

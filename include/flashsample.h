@@ -220,7 +220,7 @@ FS_API fs_status fs_combine_shards(const float* shard_max, const int64_t* shard_
  * id -1 and z -inf.  k = 1 gives fs_sample_ex's ids.
  *   1 <= k <= 16 (else FS_ERR_INVALID_ARG); B <= 4096 and d >= 64 (else
  *   FS_ERR_UNSUPPORTED).  Two launches: a tensor-core kernel with a K-list
- *   epilogue (K = 4, 8 or 16 >= k; the vocabulary-major kernel for B <= 32,
+ *   epilogue (K = 4, 8 or 16 >= k; the vocabulary-major kernel for B <= 64,
  *   the batch-major one above), writing one list per (row, CTA) to library
  *   workspace, then a block-per-row merge.  The
  *   workspace grows on the first call of a size; capture in a CUDA graph only

@@ -592,9 +592,9 @@ fs_status fs_sample_topk(const void* h, const void* W, int64_t B, int64_t d, int
   // wait, h / temp / bias read and the shared partials written after it
   p.pdl = g_launch_overlap.load() != 0;
   p.defer_inputs = p.pdl;
-  // B <= 32: the vocabulary-major kernel (one lane per batch column keeps the
+  // B <= 64: the vocabulary-major kernel (one lane per batch column keeps the
   // lists); larger B: the batch-major kernel (one thread per batch row).
-  const bool vocab_major = B <= 32;
+  const bool vocab_major = B <= 64;
   const int parts = V <= 0 ? 0 : (vocab_major ? tc_vocab_topk_parts(V, dev) : tc_topk_parts(B, dev));
   const size_t need = std::max<size_t>(static_cast<size_t>(B) * parts * K * sizeof(Partial), 256);
   Partial* partials = nullptr;

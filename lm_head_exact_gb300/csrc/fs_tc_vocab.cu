@@ -49,8 +49,9 @@ constexpr int kBM = 128;          // vocabulary rows per tile (MMA M)
 constexpr int kBK = 64;           // K per stage: one 128-byte swizzle row of bf16
 constexpr int kATileBytes = kBM * kBK * 2;
 
-// kTopK > 0: Gumbel-top-k mode (BN <= 32): per-lane K-lists, one list per
-// (row, CTA) written to partials, no in-kernel finish.
+// kTopK > 0: Gumbel-top-k mode (BN <= 64): per-lane K-lists (one per
+// accumulator chunk), one list per (row, CTA) written to partials, no
+// in-kernel finish.
 template <int BN, int kTopK = 0>
 struct VocabCfg {
   static constexpr int kBTileBytes = BN * kBK * 2;
@@ -94,7 +95,7 @@ __global__ void __launch_bounds__(kThreads, VocabCfg<BN, kTopK>::kCtasPerSm)
 tc_vocab_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_h,
                 const VocabArgs args) {
   using C = VocabCfg<BN, kTopK>;
-  static_assert(kTopK == 0 || C::kChunks == 1, "top-k lists: one accumulator chunk per lane");
+  static_assert(kTopK == 0 || C::kChunks <= 2, "top-k lists: at most two accumulator chunks per lane");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + C::kOffBars);
@@ -265,8 +266,9 @@ tc_vocab_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
     float* tr = tr_all + warp * 32 * 33;
     float best_z[C::kChunks];
     int32_t best_id[C::kChunks];
-    TopList<(kTopK > 0 ? kTopK : 1)> list;       // top-k mode: this lane's column (kChunks == 1)
-    topk_init(list);
+    TopList<(kTopK > 0 ? kTopK : 1)> list[C::kChunks];   // top-k mode: this lane's column of each chunk
+#pragma unroll
+    for (int c = 0; c < C::kChunks; ++c) topk_init(list[c]);
 #pragma unroll
     for (int c = 0; c < C::kChunks; ++c) {
       best_z[c] = -INFINITY;
@@ -312,9 +314,9 @@ tc_vocab_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
             const int64_t row_end = row0 + n_rows;
             if constexpr (kTopK > 0) {
               if (scan.bias_row != nullptr)
-                scan32_topk<true>(vals, row0, row_end, p.v_offset, scan, list);
+                scan32_topk<true>(vals, row0, row_end, p.v_offset, scan, list[c]);
               else
-                scan32_topk<false>(vals, row0, row_end, p.v_offset, scan, list);
+                scan32_topk<false>(vals, row0, row_end, p.v_offset, scan, list[c]);
             } else {
               Best bb;
               bb.z = best_z[c];
@@ -335,9 +337,13 @@ tc_vocab_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
     if constexpr (kTopK > 0) {
       // merge the 4 epilogue warps' lists of each column, one list per (row, CTA)
       Partial* lists = reinterpret_cast<Partial*>(smem + C::kOffTopK);   // [kEpiWarps][BN][kTopK]
-      if (lane < C::kChunk && lane < B) {
 #pragma unroll
-        for (int j = 0; j < kTopK; ++j) lists[(warp * BN + lane) * kTopK + j] = Partial{list.z[j], list.id[j]};
+      for (int c = 0; c < C::kChunks; ++c) {
+        const int b = c * C::kChunk + lane;
+        if (lane < C::kChunk && b < B) {
+#pragma unroll
+          for (int j = 0; j < kTopK; ++j) lists[(warp * BN + b) * kTopK + j] = Partial{list[c].z[j], list[c].id[j]};
+        }
       }
       asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
       pdl_wait();                 // the previous call's merge kernel may still read the partials
@@ -445,13 +451,17 @@ static cudaError_t launch_topk_bn(const Problem& p, int K, const Finish& f, int*
 }
 
 cudaError_t launch_tc_vocab_topk(const Problem& p, int K, Partial* partials, int* err, cudaStream_t stream) {
-  if (p.B > 32 || p.d < kBK || p.V_local <= 0) return cudaErrorNotSupported;
+  if (p.B > 64 || p.d < kBK || p.V_local <= 0) return cudaErrorNotSupported;
   int dev = 0;
   cudaGetDevice(&dev);
   Finish f{};
   f.partials = partials;
   f.n_parts = tc_vocab_topk_parts(p.V_local, dev);
-  return p.B <= 16 ? launch_topk_bn<16>(p, K, f, err, stream) : launch_topk_bn<32>(p, K, f, err, stream);
+  switch (tc_vocab_bn(p.B)) {
+    case 16: return launch_topk_bn<16>(p, K, f, err, stream);
+    case 32: return launch_topk_bn<32>(p, K, f, err, stream);
+    default: return launch_topk_bn<64>(p, K, f, err, stream);
+  }
 }
 
 }  // namespace fs

@@ -232,7 +232,7 @@ def _to_dev(a, torch):
     return torch.from_numpy(a).cuda()
 
 
-def time_steps(fs, torch, hd, Wd, td, seed, first_step, n, stream, events=True):
+def time_steps(fs, torch, hd, Wd, td, seed, first_step, n, stream, events=True, bias=None):
     """Run n steps on ``stream``; return (total ms by events around all steps,
     mean fused-kernel ms from per-step profile events)."""
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(n)] if events else []
@@ -248,7 +248,7 @@ def time_steps(fs, torch, hd, Wd, td, seed, first_step, n, stream, events=True):
         for i in range(n):
             if events:
                 fs.profile_events(starts[i], stops[i])
-            fs.sample(hd, Wd, td, seed, first_step + i, out=(ids, mx), stream=stream)
+            fs.sample(hd, Wd, td, seed, first_step + i, bias=bias, out=(ids, mx), stream=stream)
         t1.record(stream)
     fs.profile_events(None, None)
     torch.cuda.synchronize()
@@ -350,12 +350,13 @@ def run_ours(args):
 
     sweep = []
     if want("sweep"):
-        def point(kind, b, hdev, Wdev, tdev, Vk, dk):
-            time_steps(fs, torch, hdev[:b], Wdev, tdev[:b], seed, 0, 3, stream, events=False)
-            tot, _ = time_steps(fs, torch, hdev[:b], Wdev, tdev[:b], seed, 3, 20, stream, events=False)
-            _, km = time_steps(fs, torch, hdev[:b], Wdev, tdev[:b], seed, 23, 5, stream)
+        def point(kind, b, hdev, Wdev, tdev, Vk, dk, bias=None):
+            bb = None if bias is None else bias[:b]
+            time_steps(fs, torch, hdev[:b], Wdev, tdev[:b], seed, 0, 3, stream, events=False, bias=bb)
+            tot, _ = time_steps(fs, torch, hdev[:b], Wdev, tdev[:b], seed, 3, 20, stream, events=False, bias=bb)
+            _, km = time_steps(fs, torch, hdev[:b], Wdev, tdev[:b], seed, 23, 5, stream, bias=bb)
             us = tot / 20 * 1e3
-            rf = roofline(b, dk, Vk, us, peaks)
+            rf = roofline(b, dk, Vk, us, peaks, bias=bias is not None)
             return {"workload": kind, "B": b, "us_per_step": round(us, 2),
                     "fused_kernel_us_isolated": round(km * 1e3, 2), "roofline_us": rf["roofline_us"],
                     "frac": rf["frac"], "bound": rf["bound"], "path": fs.path_for_batch(b)}
@@ -371,6 +372,16 @@ def run_ours(args):
         for b in qshape["batches"]:
             sweep.append(point("qwen3_8b", b, h_big, Wq, tq, qshape["V"], qshape["d"]))
         del Wq
+        # the Llama-3-70B-shaped head (d 8192) with its dense per-row spike bias
+        lshape = synthetic.SHAPES["llama3_70b"]
+        bmax70 = max(lshape["batches"])
+        W70 = _to_dev(synthetic.weights("llama3_70b"), torch)
+        h70 = _to_dev(synthetic.normal_rows_bf16(synthetic.SEED_H, bmax70, lshape["d"], 1.0), torch)
+        t70 = torch.ones(bmax70, dtype=torch.float32, device="cuda")
+        bias70 = _to_dev(synthetic.spike_bias(bmax70, lshape["V"]), torch)
+        for b in lshape["batches"]:
+            sweep.append(point("llama3_70b", b, h70, W70, t70, lshape["V"], lshape["d"], bias=bias70))
+        del W70, h70, bias70
 
     # the grouped online (chunked) variant: 8 and 32 contiguous vocabulary
     # chunks per decode step, each chunk one launch; the step is captured in a

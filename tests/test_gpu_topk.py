@@ -154,3 +154,67 @@ def test_topk_llama3_8b_head(fs, torch_cuda, B, k):
     rows = np.unique(np.r_[0, B - 1, np.random.default_rng(B).choice(B, size=min(B, 4), replace=False)])
     ref = otopk.sample_topk(wl.h, wl.W, wl.temp, wl.seed, 7, k, rows=rows)
     compare_topk(ids, z, ref, rows=rows, what=f"8B head B={B} k={k}")
+
+
+@pytest.mark.parametrize("rows", [16, 200])
+def test_topk_law_on_gpu(fs, torch_cuda, rows):
+    """3 x 10^5 ordered pairs (k = 2) drawn on the GPU from one repeated row
+    (every (row, step) has its own noise): chi-square against the
+    Plackett-Luce law of drawing without replacement from softmax(logits / T),
+    computed from scipy's softmax of the oracle's logits.  rows = 16 runs the
+    vocabulary-major kernel, 200 the batch-major one."""
+    from scipy import special, stats
+    from oracle import sampler
+    torch = torch_cuda
+    V, d, k, T = 6, 64, 2, 0.9
+    rng = np.random.default_rng(8)
+    h1 = synthetic.bf16_bits(rng.standard_normal((1, d)).astype(np.float32))
+    W = synthetic.bf16_bits((rng.standard_normal((V, d)) * 0.12).astype(np.float32))
+    steps = 300_000 // rows
+    hd = to_device(np.repeat(h1, rows, axis=0), torch)
+    Wd = to_device(W, torch)
+    td = torch.full((rows,), T, device="cuda")
+    ids = torch.empty((steps, rows, k), dtype=torch.int64, device="cuda")
+    z = torch.empty((steps, rows, k), dtype=torch.float32, device="cuda")
+    for s_ in range(steps):
+        fs.sample_topk(hd, Wd, td, 99, s_, k, out=(ids[s_], z[s_]))
+    got = ids.cpu().numpy().reshape(-1, k)
+    assert np.all(got[:, 0] != got[:, 1]) and np.all(got >= 0)
+    counts = np.bincount(got[:, 0] * V + got[:, 1], minlength=V * V)
+    p = special.softmax(sampler.logits(h1, W)[0] / T)
+    probs = np.zeros(V * V)
+    for i in range(V):
+        for j in range(V):
+            if i != j:
+                probs[i * V + j] = p[i] * p[j] / (1.0 - p[i])
+    keep = probs > 0
+    assert stats.chisquare(counts[keep], probs[keep] * counts.sum()).pvalue > 0.01
+
+
+def test_topk_captured_in_cuda_graph(fs, torch_cuda):
+    """After one eager call of the same size, a top-k call can be captured
+    into a CUDA graph; replays with a changed step buffer are not possible
+    (the step is baked in), so the replay must reproduce the eager result."""
+    torch = torch_cuda
+    B, V, d, k = 24, 5003, 128, 8
+    h, W, temp = _problem(B, V, d, seed=31)
+    hd, Wd, td = to_device(h, torch), to_device(W, torch), to_device(temp, torch)
+    stream = torch.cuda.Stream()
+    ids = torch.empty((B, k), dtype=torch.int64, device="cuda")
+    z = torch.empty((B, k), dtype=torch.float32, device="cuda")
+    fs.workspace_reserve(B, V, stream=stream)
+    with torch.cuda.stream(stream):
+        fs.sample_topk(hd, Wd, td, 4, 4, k, out=(ids, z), stream=stream)
+    torch.cuda.synchronize()
+    want = (ids.cpu().numpy().copy(), z.cpu().numpy().copy())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        fs.sample_topk(hd, Wd, td, 4, 4, k, out=(ids, z), stream=stream)
+    ids.fill_(-5)
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(ids.cpu().numpy(), want[0])
+    np.testing.assert_array_equal(z.cpu().numpy(), want[1])
+    compare_topk(want[0], want[1], otopk.sample_topk(h, W, temp, 4, 4, k), what="graph")
+    del graph

@@ -69,3 +69,13 @@ def test_early_stops_after_a_dominant_first_chunk():
     np.testing.assert_array_equal(zmax, ref.zmax)
     assert read == 1
     assert ids[4] == -1
+
+
+def test_row_norms_is_numpy_norm_of_the_decoded_rows():
+    import torch
+    from lm_head_exact_gb300.synthetic import bf16_bits
+    rng = np.random.default_rng(12)
+    X = bf16_bits((rng.standard_normal((7, 300)) * 3).astype(np.float32))
+    # decode through torch's own bf16 (not the oracle's decoder), norm through numpy
+    dec = torch.from_numpy(X.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    np.testing.assert_allclose(sampler.row_norms(X), np.linalg.norm(dec, axis=1), rtol=1e-15)

@@ -595,7 +595,7 @@ fs_status fs_sample_topk(const void* h, const void* W, int64_t B, int64_t d, int
   // B <= 64: the vocabulary-major kernel (one lane per batch column keeps the
   // lists); larger B: the batch-major kernel (one thread per batch row).
   const bool vocab_major = B <= 64;
-  const int parts = V <= 0 ? 0 : (vocab_major ? tc_vocab_topk_parts(V, dev) : tc_topk_parts(B, dev));
+  const int parts = V <= 0 ? 0 : (vocab_major ? tc_vocab_topk_parts(V, dev) : tc_topk_parts(B, V, dev));
   const size_t need = std::max<size_t>(static_cast<size_t>(B) * parts * K * sizeof(Partial), 256);
   Partial* partials = nullptr;
   {

@@ -128,7 +128,7 @@ cudaError_t launch_row_norms(const void* X, int64_t n, int64_t d, float* out, un
 // partials [B, tc_topk_parts(B), K]; launch_topk_merge then merges each row's
 // lists (n_lists <= 256 per row, each sorted) into its k <= K best
 // (out_ids / out_z [B, k]; -1 / -inf padded).
-int tc_topk_parts(int64_t B, int device);
+int tc_topk_parts(int64_t B, int64_t V, int device);
 cudaError_t launch_tc_topk(const Problem& p, int K, Partial* partials, int* err, cudaStream_t stream);
 // The vocabulary-major kernel in top-K mode, for B <= 64: partials [B,
 // tc_vocab_topk_parts(V), K] (one list per (row, CTA)).

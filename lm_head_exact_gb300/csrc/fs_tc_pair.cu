@@ -330,7 +330,12 @@ cudaError_t launch_tc_pair(const Problem& p, const Finish& f, int* err, cudaStre
       fs_slice.out_max = f.out_max + b0;
     }
     const int npt = static_cast<int>((ps.B + 2 * kRowsPerCta - 1) / (2 * kRowsPerCta));
-    const int n_groups = std::max(1, pairs / npt);
+    int n_groups = std::max(1, pairs / npt);
+    {   // as few groups as give every group the same number of vocabulary tiles
+      const int64_t n_vt = (p.V_local + kBN - 1) / kBN;
+      const int64_t per = (n_vt + n_groups - 1) / n_groups;
+      n_groups = static_cast<int>(std::max<int64_t>(1, (n_vt + per - 1) / per));
+    }
     CUtensorMap th;
     if (!encode_kmajor_bf16(&th, ps.h, ps.B, p.d, kBK, kRowsPerCta)) return cudaErrorInvalidValue;
     PairArgs a{ps, fs_slice, npt, n_groups, static_cast<int>((p.V_local + kBN - 1) / kBN), err};

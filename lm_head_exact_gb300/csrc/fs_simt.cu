@@ -156,7 +156,8 @@ int pick_group(int64_t B, int64_t d) {
 
 // One wave of CTAs: the SMs times the CTAs of this instantiation that fit on
 // one SM (registers and shared memory), never more than the 8-row vocabulary
-// groups.
+// groups, then as few as give every warp the same number of rows (B = 1 on
+// the 8B head: 160.0 -> 158.5 us).
 template <int BG, bool kEarly>
 cudaError_t launch_variant(const Problem& p, const Finish& f, cudaStream_t stream) {
   const size_t smem = static_cast<size_t>(BG) * p.d * 2;
@@ -169,9 +170,12 @@ cudaError_t launch_variant(const Problem& p, const Finish& f, cudaStream_t strea
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, simt_fused_kernel<BG, kEarly>, kSimtThreads, smem);
   if (e != cudaSuccess) return e;
-  const int64_t parts = std::min<int64_t>(static_cast<int64_t>(std::max(sms, 1)) * std::max(per_sm, 1),
-                                          std::max<int64_t>(1, (p.V_local + kSimtWarps - 1) / kSimtWarps));
-  const int n_parts = static_cast<int>(parts);
+  const int64_t max_parts = std::min<int64_t>(static_cast<int64_t>(std::max(sms, 1)) * std::max(per_sm, 1),
+                                              std::max<int64_t>(1, (p.V_local + kSimtWarps - 1) / kSimtWarps));
+  // then as few CTAs as give every warp the same number of vocabulary rows
+  const int64_t rows_per_warp = (p.V_local + max_parts * kSimtWarps - 1) / (max_parts * kSimtWarps);
+  const int64_t warps = (p.V_local + rows_per_warp - 1) / rows_per_warp;
+  const int n_parts = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(max_parts, (warps + kSimtWarps - 1) / kSimtWarps)));
   const int64_t groups = (p.B + BG - 1) / BG;
   dim3 grid(n_parts, static_cast<unsigned>(std::min<int64_t>(groups, 65535)));
   return launch_kernel(simt_fused_kernel<BG, kEarly>, grid, dim3(kSimtThreads), smem, stream, p.pdl, p, f);

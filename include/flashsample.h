@@ -306,8 +306,7 @@ FS_API fs_status fs_set_path(int path);
 
 /*
  * Launch overlap of fs_sample / fs_sample_ex (1, the default, or 0;
- * process-wide).  With 1, the tensor-core kernels (B >= 2, except the CTA-pair
- * kernel at B <= 256, where it measured slower) are launched
+ * process-wide).  With 1, the tensor-core kernels (B >= 2) are launched
  * as programmatic dependents of the preceding kernel on the stream: their
  * prologues and first rings of W loads may run while that kernel finishes
  * (for example the previous decode step's sampling kernel, or the model's

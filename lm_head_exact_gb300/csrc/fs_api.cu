@@ -252,10 +252,10 @@ fs_status run(Problem p, Finish f, cudaStream_t stream) {
   }
   FS_TRY(get_finish(stream, p.B, &f));
   const int path = resolve_path(p.B, p.d);
-  // The tensor-core kernels defer their input reads; the overlap was measured
-  // to cost 2-4 us for the CTA-pair kernel at B <= 256 on GB300 (and to save
-  // 4-6 us everywhere else), so those calls launch plainly.
-  if (p.defer_inputs && (path == kPathSimt || (path == kPathTcPair && p.B <= 256))) {
+  // The tensor-core kernels defer their input reads (interleaved A/B runs on
+  // GB300: the overlap saves 4-8 us per back-to-back step at every B from 2
+  // to 512); the CUDA-core kernel launches plainly.
+  if (p.defer_inputs && path == kPathSimt) {
     p.defer_inputs = false;
     p.pdl = false;
   }

@@ -270,6 +270,8 @@ def run_ours(args):
     else:
         torch.cuda.set_device(0)
     fs.library()
+    fs.set_path({"auto": fs.FS_PATH_AUTO, "simt": fs.FS_PATH_SIMT, "vocab": fs.FS_PATH_TC_VOCAB,
+                 "batch": fs.FS_PATH_TC_BATCH, "pair": fs.FS_PATH_TC_PAIR}[args.path])
     peaks = load_peaks()
     kind = "llama3_8b"
     shape = synthetic.SHAPES[kind]
@@ -642,6 +644,8 @@ def parse_args(argv=None):
     ap.add_argument("--batch", type=int, default=16)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--path", choices=["auto", "simt", "vocab", "batch", "pair"], default="auto",
+                    help="force a kernel family (profiling)")
     ap.add_argument("--only", default="", help="comma list of extra sections: sweep,chunked,early,topk,unfused")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=20.0)

@@ -225,6 +225,11 @@ constexpr int64_t kVocabMajorMaxBatch = 96;
 //   larger B: the CTA-pair kernel when padding B to 256-row pair tiles wastes
 //   fewer than 128 rows (B = 256: 205 vs 217, B = 1024: 701 vs 729), otherwise
 //   the single-CTA batch-major kernel (B = 128: 185 vs 193, B = 384: 307 vs 344).
+// B = 1 stays on the CUDA-core kernel: measured on GB300 (8B head), the
+// vocabulary-major kernel is 1.8% faster for a one-shot B = 1 step (154.3 vs
+// 157.8 us) but slower on chunks, whose few 128-row tiles leave most SMs idle
+// (8 chunks 195.5 vs 188.7 us, 32 chunks 234 vs 212, early stop 121 vs 91);
+// chunked and one-shot calls must use the same family to agree bit for bit.
 int auto_path(int64_t B) {
   if (B == 1) return kPathSimt;
   if (B <= kVocabMajorMaxBatch) return kPathTcVocab;

@@ -253,9 +253,13 @@ FS_API fs_status fs_sample_unfused(const void* h, const void* W, int64_t B, int6
  * temp_host [B] fp32 to the device, samples against the device-resident
  * W [V, d] (and optional device bias), copies out_ids_host [B] int64 and
  * out_max_host [B] fp32 back, and synchronizes `stream` before returning.
- * Host buffers should be pinned (cudaHostAlloc / cudaHostRegister) for the
- * copies to be asynchronous; pageable memory works but is slower.  Device
- * staging lives in the library workspace of (device, stream).
+ * When h_host and temp_host are mapped page-locked memory (cudaHostAlloc,
+ * cudaHostRegister with mapping, torch's pin_memory), a small kernel reads
+ * them directly and the fused kernel starts as its programmatic dependent
+ * (see fs_set_launch_overlap), writing the results straight into a mapped
+ * landing area: no copy-engine transfers.  Other host memory is copied with
+ * cudaMemcpyAsync (pageable memory works but is slower).  Device staging
+ * lives in the library workspace of (device, stream).
  */
 FS_API fs_status fs_sample_host(const void* h_host, const void* W, int64_t B, int64_t d, int64_t V,
                          const float* temp_host, const float* bias, int64_t bias_row_stride,

@@ -137,6 +137,12 @@ cudaError_t launch_tc_vocab_topk(const Problem& p, int K, Partial* partials, int
 cudaError_t launch_topk_merge(const Partial* partials, int n_lists, int K, int64_t B, int k, int64_t* out_ids,
                               float* out_z, cudaStream_t stream);
 
+// Host-buffer entry point: h (h_bytes, a multiple of 16) and temperatures
+// [B] from mapped pinned host memory into device staging; the next kernel on
+// the stream may start as its programmatic dependent.
+cudaError_t launch_copy_in(const void* h_src, void* h_dst, int64_t h_bytes, const float* t_src, float* t_dst, int64_t B,
+                           cudaStream_t stream);
+
 // Tensor-parallel combine: out[b] = best over r of (shard_max[r, b], shard_ids[r, b]).
 cudaError_t launch_combine_shards(const float* shard_max, const int64_t* shard_ids, int64_t R, int64_t B,
                                   int64_t* out_ids, float* out_max, cudaStream_t stream);

@@ -6,6 +6,8 @@
 //
 // Also holds the noise-inspection kernel that exposes the exact Philox words
 // and Gumbel values every sampling kernel uses, for parity tests.
+#include <algorithm>
+
 #include "fs_finish.cuh"
 #include "fs_internal.h"
 #include "fs_sm100.cuh"
@@ -32,6 +34,19 @@ reduce_kernel(Finish f, int64_t B) {
   }
   best = warp_combine(best);
   if (lane == 0) write_row(f, b, best);
+}
+
+// Host-buffer entry point: copy h (bf16x8 packets) and the temperatures from
+// mapped pinned host memory into device staging.  Launched before the fused
+// kernel, which starts as its programmatic dependent: the fused kernel's
+// prologue and first W loads overlap this copy.
+__global__ void __launch_bounds__(256)
+copy_in_kernel(const uint4* __restrict__ h_src, uint4* __restrict__ h_dst, int64_t n16, const float* __restrict__ t_src,
+               float* __restrict__ t_dst, int64_t B) {
+  pdl_launch_dependents();
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n16; i += stride) h_dst[i] = h_src[i];
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < B; i += stride) t_dst[i] = t_src[i];
 }
 
 // Cross-shard combine of the tensor-parallel variant: row b's result is the
@@ -197,6 +212,15 @@ cudaError_t launch_topk_merge(const Partial* partials, int n_lists, int K, int64
     case 16: return launch_kernel(topk_merge_kernel<16>, grid, dim3(kMergeThreads), 0, stream, true, partials, n_lists, k, out_ids, out_z);
     default: return cudaErrorInvalidValue;
   }
+}
+
+cudaError_t launch_copy_in(const void* h_src, void* h_dst, int64_t h_bytes, const float* t_src, float* t_dst, int64_t B,
+                           cudaStream_t stream) {
+  const int64_t n16 = h_bytes / 16;
+  const int64_t blocks = std::min<int64_t>(128, std::max<int64_t>(1, (std::max(n16, B) + 255) / 256));
+  copy_in_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(static_cast<const uint4*>(h_src),
+                                                                     static_cast<uint4*>(h_dst), n16, t_src, t_dst, B);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_debug_noise(uint64_t seed, uint64_t step, int64_t row0, int64_t n_rows,

@@ -429,3 +429,22 @@ def test_launch_overlap_gives_identical_results(fs, torch_cuda, B):
         np.testing.assert_array_equal(i1, i0)
         np.testing.assert_array_equal(m1, m0)
     compare(on[3][0], on[3][1], sampler.sample(h2, W, temp2, 5, 3), what=f"overlap B={B}")
+
+
+def test_sample_host_pinned_and_pageable_agree(fs, torch_cuda):
+    """fs_sample_host reads mapped pinned buffers directly (copy kernel +
+    overlapped launch + mapped results) and copies pageable ones: both give
+    the device-buffer sample, for every kernel family's batch sizes."""
+    torch = torch_cuda
+    for B in (1, 16, 130, 300):
+        h, W, temp = _problem(B, 3001, 128, seed=70 + B)
+        Wd = to_device(W, torch)
+        ids_d, mx_d = _run(fs, torch, h, W, temp, 12, 5)
+        h_pin = torch.from_numpy(h.view(np.int16)).pin_memory()
+        t_pin = torch.from_numpy(temp).pin_memory()
+        ids_p, mx_p = fs.sample_host(h_pin, Wd, t_pin, 12, 5)
+        ids_q, mx_q = fs.sample_host(h, Wd, temp, 12, 5)
+        np.testing.assert_array_equal(ids_p, ids_d)
+        np.testing.assert_array_equal(mx_p, mx_d)
+        np.testing.assert_array_equal(ids_q, ids_d)
+        np.testing.assert_array_equal(mx_q, mx_d)

@@ -218,3 +218,18 @@ def test_topk_captured_in_cuda_graph(fs, torch_cuda):
     np.testing.assert_array_equal(z.cpu().numpy(), want[1])
     compare_topk(want[0], want[1], otopk.sample_topk(h, W, temp, 4, 4, k), what="graph")
     del graph
+
+
+def test_topk_llama3_70b_head_with_bias(fs, torch_cuda):
+    """d 8192 and the dense spike bias (16 ids per row at +8): the top 16
+    carry the spikes; sampled rows against the oracle."""
+    torch = torch_cuda
+    B, k = 8, 16
+    wl = synthetic.workload("llama3_70b", B)
+    hd, Wd, td = to_device(wl.h, torch), to_device(wl.W, torch), to_device(wl.temp, torch)
+    bd = to_device(wl.bias, torch)
+    ids, z = fs.sample_topk(hd, Wd, td, wl.seed, 3, k, bias=bd)
+    torch.cuda.synchronize()
+    rows = np.array([0, 3, 7])
+    ref = otopk.sample_topk(wl.h, wl.W, wl.temp, wl.seed, 3, k, bias=wl.bias, rows=rows)
+    compare_topk(ids.cpu().numpy(), z.cpu().numpy(), ref, rows=rows, what="70B head, bias")

@@ -7,6 +7,8 @@ compared on sampled rows (the oracle computes each row over the whole
 vocabulary).  Comparison rule: tests/_helpers.py.
 """
 
+import os
+
 import numpy as np
 import pytest
 
@@ -448,3 +450,31 @@ def test_sample_host_pinned_and_pageable_agree(fs, torch_cuda):
         np.testing.assert_array_equal(mx_p, mx_d)
         np.testing.assert_array_equal(ids_q, ids_d)
         np.testing.assert_array_equal(mx_q, mx_d)
+
+
+def test_noise_words_match_curand_philox(fs, torch_cuda, tmp_path):
+    """The library's noise words equal cuRAND's device-API Philox-4x32-10
+    (curandStatePhilox4_32_10_t, curand4) run as a library, with the
+    sampler's key / counter layout reached through curand_init(seed,
+    subsequence = step, offset = (row << 34) + 4 (id >> 2))."""
+    import shutil
+    import subprocess
+    nvcc = shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
+    src = os.path.join(os.path.dirname(__file__), "gpu_helpers", "curand_philox_words.cu")
+    exe = str(tmp_path / "curand_words")
+    r = subprocess.run([nvcc, "-gencode", "arch=compute_103a,code=sm_103a", "-O2", "-o", exe, src],
+                       capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    seed = 0x1234ABCD5678EF01
+    cases = [(row0, v0, step) for row0, v0, step in ((0, 0, 0), (5, 3, 99), (1000, 151900, (3 << 32) + 17))]
+    for row0, v0, step in cases:
+        n_rows, n_vocab = 7, 13
+        words, _ = fs.debug_noise(seed, step, row0, n_rows, v0, n_vocab)
+        torch_cuda.cuda.synchronize()
+        ours = words.cpu().numpy().view(np.uint32).reshape(n_rows, n_vocab)
+        triples = [(row0 + r_, v0 + j, step) for r_ in range(n_rows) for j in range(n_vocab)]
+        stdin = f"{seed} {len(triples)}\n" + "\n".join(f"{a} {b} {c}" for a, b, c in triples) + "\n"
+        out = subprocess.run([exe], input=stdin, capture_output=True, text=True, timeout=60)
+        assert out.returncode == 0, out.stderr
+        theirs = np.array([int(x) for x in out.stdout.split()], dtype=np.uint64).astype(np.uint32)
+        np.testing.assert_array_equal(ours.ravel(), theirs)

@@ -346,6 +346,20 @@ FS_API fs_status fs_device_error(int* code);
  */
 FS_API fs_status fs_debug_wait_timeout(uint64_t timeout_ns, void* stream);
 
+/*
+ * Host-side fault injection for failure-detection tests (process-wide):
+ * FS_FAULT_ALLOC makes every workspace allocation that would happen fail with
+ * FS_ERR_WORKSPACE, FS_FAULT_LAUNCH makes every fused sampling launch fail
+ * with FS_ERR_CUDA -- before any CUDA call is made, so the GPU and the
+ * context are untouched and later calls work once FS_FAULT_NONE is set.  The
+ * initial value comes from the FS_FAULT environment variable ("alloc",
+ * "launch"; anything else: none).
+ */
+#define FS_FAULT_NONE 0
+#define FS_FAULT_ALLOC 1
+#define FS_FAULT_LAUNCH 2
+FS_API fs_status fs_debug_set_fault(int kind);
+
 /* Static name of a status code. */
 FS_API const char* fs_status_string(fs_status s);
 

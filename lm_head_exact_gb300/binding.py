@@ -19,6 +19,7 @@ FS_CHUNK_FIRST = 1
 FS_CHUNK_LAST = 2
 FS_CHUNK_SERIAL = 4
 FS_PATH_AUTO, FS_PATH_SIMT, FS_PATH_TC_VOCAB, FS_PATH_TC_BATCH, FS_PATH_TC_PAIR = 0, 1, 2, 3, 4
+FS_FAULT_NONE, FS_FAULT_ALLOC, FS_FAULT_LAUNCH = 0, 1, 2
 
 _c_void_p = ctypes.c_void_p
 _i64 = ctypes.c_int64
@@ -58,6 +59,7 @@ SIGNATURES = {
     "fs_profile_events": (_int, [_c_void_p, _c_void_p]),
     "fs_device_error": (_int, [ctypes.POINTER(_int)]),
     "fs_debug_wait_timeout": (_int, [_u64, _c_void_p]),
+    "fs_debug_set_fault": (_int, [_int]),
     "fs_status_string": (ctypes.c_char_p, [_int]),
     "fs_last_error": (ctypes.c_char_p, []),
     "fs_debug_noise": (_int, [_u64, _u64, _i64, _i64, _i64, _i64, _c_void_p, _c_void_p, _c_void_p]),
@@ -365,6 +367,11 @@ def debug_noise(seed, step, row0, n_rows, v0, n_vocab, stream=None):
 
 def set_path(path):
     check(library().fs_set_path(path))
+
+
+def debug_set_fault(kind):
+    """Host-side fault injection (FS_FAULT_NONE / _ALLOC / _LAUNCH)."""
+    check(library().fs_debug_set_fault(int(kind)))
 
 
 def set_launch_overlap(enable):

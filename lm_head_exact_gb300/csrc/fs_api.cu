@@ -6,6 +6,7 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <map>
 #include <mutex>
@@ -23,6 +24,23 @@ thread_local cudaEvent_t g_prof_start = nullptr;
 thread_local cudaEvent_t g_prof_stop = nullptr;
 std::atomic<int> g_forced_path{kPathAuto};
 std::atomic<int> g_launch_overlap{1};
+
+// Host-side fault injection (FS_FAULT_*): read from the FS_FAULT environment
+// variable ("alloc" or "launch") on first use, or set by fs_debug_set_fault.
+// An injected fault makes the library return the error of the failing call
+// without touching the GPU.
+std::atomic<int> g_fault{-1};
+
+int injected_fault() {
+  int f = g_fault.load();
+  if (f < 0) {
+    const char* env = getenv("FS_FAULT");
+    f = env == nullptr ? FS_FAULT_NONE
+                       : (strcmp(env, "alloc") == 0 ? FS_FAULT_ALLOC : strcmp(env, "launch") == 0 ? FS_FAULT_LAUNCH : FS_FAULT_NONE);
+    g_fault.store(f);
+  }
+  return f;
+}
 
 fs_status fail(fs_status s, const char* fmt, ...) {
   va_list ap;
@@ -76,6 +94,8 @@ bool capturing(cudaStream_t stream) {
 // that no in-flight kernel still uses the old buffer.
 fs_status grow(void** buf, size_t* have, size_t need, cudaStream_t stream) {
   if (*have >= need) return FS_OK;
+  if (injected_fault() == FS_FAULT_ALLOC)
+    return fail(FS_ERR_WORKSPACE, "cudaMalloc(%zu) for the workspace failed: injected (FS_FAULT=alloc)", need);
   if (capturing(stream))
     return fail(FS_ERR_WORKSPACE, "workspace must grow to %zu bytes during stream capture; "
                 "call fs_workspace_reserve() before capturing", need);
@@ -283,6 +303,8 @@ fs_status run(Problem p, Finish f, cudaStream_t stream) {
     e = cudaEventRecord(g_prof_start, stream);
     if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord(start)");
   }
+  if (injected_fault() == FS_FAULT_LAUNCH)
+    return fail(FS_ERR_CUDA, "fused sampling kernel launch failed: injected (FS_FAULT=launch)");
   switch (path) {
     case kPathTcVocab:
       e = launch_tc_vocab(p, f, err, stream);
@@ -744,6 +766,13 @@ fs_status fs_workspace_release(void) {
 fs_status fs_set_path(int path) {
   if (path < FS_PATH_AUTO || path > FS_PATH_TC_PAIR) return fail(FS_ERR_INVALID_ARG, "unknown path %d", path);
   g_forced_path.store(path);
+  return FS_OK;
+}
+
+fs_status fs_debug_set_fault(int kind) {
+  g_last_error[0] = '\0';
+  if (kind < FS_FAULT_NONE || kind > FS_FAULT_LAUNCH) return fail(FS_ERR_INVALID_ARG, "unknown fault kind %d", kind);
+  g_fault.store(kind);
   return FS_OK;
 }
 

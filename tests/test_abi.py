@@ -66,6 +66,8 @@ def test_host_side_argument_checks(built_library):
     assert lib.fs_sample_chunked(z, z, 4, 64, 0, 5, z, z, 0, 0, 0, z, z, 8, z, z, z) == 1
     assert lib.fs_set_path(7) == 1
     assert lib.fs_set_launch_overlap(2) == 1
+    assert lib.fs_debug_set_fault(7) == 1
+    assert lib.fs_debug_set_fault(0) == 0
     # top-k: k outside [1, 16] is refused before anything else
     assert lib.fs_sample_topk(z, z, 4, 64, 10, z, z, 0, 0, 0, 0, z, z, z) == 1
     assert lib.fs_sample_topk(z, z, 4, 64, 10, z, z, 0, 0, 0, 17, z, z, z) == 1

@@ -100,3 +100,20 @@ def test_product_path_refuses_cpu_tensors(built_library):
     t = torch.ones(2)
     with pytest.raises(binding.FlashSampleError, match="CUDA tensor"):
         binding.sample(h, W, t, 0, 0)
+
+
+def test_binding_constants_match_the_header():
+    """Every FS_* integer constant of the header (flags, paths, fault kinds,
+    status codes) has the same value in the Python binding."""
+    from lm_head_exact_gb300 import binding
+    text = open(HEADER).read()
+    defines = {m.group(1): int(m.group(2)) for m in re.finditer(r"^#define\s+(FS_\w+)\s+(\d+)", text, flags=re.M)}
+    enum_body = re.search(r"typedef enum fs_status \{(.*?)\} fs_status;", text, flags=re.S).group(1)
+    status = {m.group(1): int(m.group(2)) for m in re.finditer(r"(FS_\w+)\s*=\s*(\d+)", enum_body)}
+    assert defines, "no #define constants found"
+    for name, value in defines.items():
+        assert getattr(binding, name) == value, name
+    assert status["FS_OK"] == binding.FS_OK
+    lib = binding.library()
+    for name, value in status.items():
+        assert lib.fs_status_string(value).decode() == name

@@ -662,9 +662,14 @@ fs_status fs_sample_topk(const void* h, const void* W, int64_t B, int64_t d, int
   p.pdl = g_launch_overlap.load() != 0;
   p.defer_inputs = p.pdl;
   // B <= 64: the vocabulary-major kernel (one lane per batch column keeps the
-  // lists); larger B: the batch-major kernel (one thread per batch row).
-  const bool vocab_major = B <= 64;
-  const int parts = V <= 0 ? 0 : (vocab_major ? tc_vocab_topk_parts(V, dev) : tc_topk_parts(B, V, dev));
+  // lists); larger B: the kernel the sampler runs at that B, CTA pairs or the
+  // batch-major one (one thread per batch row in both).
+  const int family = B <= 64 ? kPathTcVocab
+                     : (auto_path(B) == kPathTcPair && B <= tc_pair_topk_max_rows(dev) ? kPathTcPair : kPathTcBatch);
+  const int parts = V <= 0 ? 0
+                    : family == kPathTcVocab ? tc_vocab_topk_parts(V, dev)
+                    : family == kPathTcPair  ? tc_pair_topk_parts(B, V, dev)
+                                             : tc_topk_parts(B, V, dev);
   const size_t need = std::max<size_t>(static_cast<size_t>(B) * parts * K * sizeof(Partial), 256);
   Partial* partials = nullptr;
   {
@@ -677,7 +682,9 @@ fs_status fs_sample_topk(const void* h, const void* W, int64_t B, int64_t d, int
   if (V > 0) {
     int* err = nullptr;
     FS_TRY(error_word(&err));
-    e = vocab_major ? launch_tc_vocab_topk(p, K, partials, err, stream) : launch_tc_topk(p, K, partials, err, stream);
+    e = family == kPathTcVocab ? launch_tc_vocab_topk(p, K, partials, err, stream)
+        : family == kPathTcPair ? launch_tc_pair_topk(p, K, partials, err, stream)
+                                : launch_tc_topk(p, K, partials, err, stream);
     if (e != cudaSuccess) return cuda_fail(e, "top-k kernel launch");
   }
   e = launch_topk_merge(partials, parts, K, B, k, out_ids, out_z, stream);

@@ -134,6 +134,12 @@ cudaError_t launch_tc_topk(const Problem& p, int K, Partial* partials, int* err,
 // tc_vocab_topk_parts(V), K] (one list per (row, CTA)).
 int tc_vocab_topk_parts(int64_t V, int device);
 cudaError_t launch_tc_vocab_topk(const Problem& p, int K, Partial* partials, int* err, cudaStream_t stream);
+// The CTA-pair kernel in top-K mode, for the batches the sampler runs on CTA
+// pairs: partials [B, tc_pair_topk_parts(B, V), K] (one list per (row, pair
+// group)); B <= tc_pair_topk_max_rows (one launch).
+int64_t tc_pair_topk_max_rows(int device);
+int tc_pair_topk_parts(int64_t B, int64_t V, int device);
+cudaError_t launch_tc_pair_topk(const Problem& p, int K, Partial* partials, int* err, cudaStream_t stream);
 cudaError_t launch_topk_merge(const Partial* partials, int n_lists, int K, int64_t B, int k, int64_t* out_ids,
                               float* out_z, cudaStream_t stream);
 

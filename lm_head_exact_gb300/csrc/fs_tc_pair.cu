@@ -21,6 +21,11 @@
 // CTA grouping as in the single-CTA kernel: with npt = ceil(B / 256) pair
 // tiles, groups of npt pairs walk the vocabulary tiles q, q + n_groups, ...
 // in lockstep, so W comes from HBM once per group.
+//
+// Gumbel-top-k mode (kTopK > 0): every epilogue thread keeps its batch row's
+// K best perturbed scores instead of the best one; the two column halves
+// merge through shared memory and each CTA writes one list per (row, group)
+// for the merge kernel, with no in-kernel finish.
 #include <cuda.h>
 
 #include <algorithm>
@@ -53,19 +58,23 @@ constexpr int kOffB = kOffA + kStages * kATileBytes;
 constexpr int kOffBars = kOffB + kStages * kBTileBytes;
 constexpr int kNumBars = 2 * kStages + 5;
 constexpr int kOffMisc = kOffBars + kNumBars * 8;
-constexpr int kOffHalf = kOffMisc + 16;
-constexpr int kSmemBytes = kOffHalf + kRowsPerCta * 8 + 1024;
+constexpr int kOffHalf = kOffMisc + 16;                        // Best[128]: second-half results
+constexpr int kOffTopK = kOffHalf + kRowsPerCta * 8;           // top-k mode: Partial[128][K] of the second half
+constexpr int kSmemBytes = kOffTopK + 1024;
+constexpr int smem_bytes(int top_k) { return kSmemBytes + kRowsPerCta * top_k * 8; }
 constexpr uint16_t kPairMask = 0x3;
 
 struct PairArgs {
   Problem p;            // rows [0, p.B) of this launch's batch slice
-  Finish f;
+  Finish f;             // sampling mode: cross-CTA finish of this slice's rows;
+                        // top-k mode: f.partials [B, f.n_parts, K], part = pair group
   int npt;              // pair tiles (256 batch rows each) of this launch
   int n_groups;         // groups of npt pairs
   int n_vt;             // vocabulary tiles = ceil(V_local / 256)
   int* err;
 };
 
+template <int kTopK = 0>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_constant__ CUtensorMap tmap_w,
                const PairArgs args) {
@@ -80,7 +89,7 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_constant
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
   int* last_flag = reinterpret_cast<int*>(smem + kOffMisc + 8);
   Best* half_best = reinterpret_cast<Best*>(smem + kOffHalf);
-  if (args.f.done != nullptr && args.f.carry_in) {
+  if (kTopK == 0 && args.f.done != nullptr && args.f.carry_in) {
     // Early finalization: the two CTAs of a pair must take the same decision
     // (the running one would otherwise signal a peer that has left), so the
     // even CTA reads the flag once and stores it into both CTAs.
@@ -234,6 +243,8 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_constant
     scan.greedy = greedy;
     scan.bias_row = p.bias != nullptr ? p.bias + b * p.bias_stride : nullptr;
     Best best = best_none();
+    TopList<(kTopK > 0 ? kTopK : 1)> list;
+    topk_init(list);
     for (int t = 0; t < n_tiles; ++t) {
       const int acc = t & 1;
       const uint32_t acc_phase = (t >> 1) & 1;
@@ -248,22 +259,48 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_constant
         tmem_ld_wait();
         const int64_t v0 = col0 + c;
         if (active && v0 < p.V_local) {
-          if (scan.bias_row != nullptr)
-            scan32<true>(r, v0, p.V_local, p.v_offset, scan, best);
-          else
-            scan32<false>(r, v0, p.V_local, p.v_offset, scan, best);
+          if constexpr (kTopK > 0) {
+            if (scan.bias_row != nullptr)
+              scan32_topk<true>(r, v0, p.V_local, p.v_offset, scan, list);
+            else
+              scan32_topk<false>(r, v0, p.V_local, p.v_offset, scan, list);
+          } else {
+            if (scan.bias_row != nullptr)
+              scan32<true>(r, v0, p.V_local, p.v_offset, scan, best);
+            else
+              scan32<false>(r, v0, p.V_local, p.v_offset, scan, best);
+          }
         }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&tempty_bar[acc]), 0));
     }
-    if (half == 1) half_best[row_in_tile] = best;
-    asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
-    pdl_wait();                   // the finish area is shared with the previous launch
-    if (half == 0 && row_ok) push_candidate(args.f, b, combine(best, half_best[row_in_tile]));
-    finish_grid(args.f, p.B, threadIdx.x, kEpiWarps * 32, last_flag,
-                named_bar1_and<kEpiWarps * 32>);
+    if constexpr (kTopK > 0) {
+      // merge the two column halves' lists, then one list per (row, group)
+      Partial* other = reinterpret_cast<Partial*>(smem + kOffTopK) + row_in_tile * kTopK;
+      if (half == 1) {
+#pragma unroll
+        for (int j = 0; j < kTopK; ++j) other[j] = Partial{list.z[j], list.id[j]};
+      }
+      asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
+      if (p.pdl) pdl_wait();      // the previous call's merge kernel may still read the partials
+      if (half == 0 && row_ok) {
+#pragma unroll
+        for (int j = 0; j < kTopK; ++j) topk_offer(list, other[j].z, other[j].id);
+        Partial* dst = args.f.partials + (b * args.f.n_parts + q) * kTopK;
+#pragma unroll
+        for (int j = 0; j < kTopK; ++j) dst[j] = Partial{list.z[j], list.id[j]};
+      }
+    } else {
+      // combine the two column halves of each row, then one candidate per (row, group)
+      if (half == 1) half_best[row_in_tile] = best;
+      asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
+      pdl_wait();                 // the finish area is shared with the previous launch
+      if (half == 0 && row_ok) push_candidate(args.f, b, combine(best, half_best[row_in_tile]));
+      finish_grid(args.f, p.B, threadIdx.x, kEpiWarps * 32, last_flag,
+                  named_bar1_and<kEpiWarps * 32>);
+    }
   }
 
   // ---- teardown: neither CTA leaves (or frees TMEM) while the pair's MMAs or
@@ -291,7 +328,7 @@ static int resident_pairs(int dev, int sms) {
   cfg.gridDim = dim3(static_cast<unsigned>(2 * (sms / 2)));
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = kSmemBytes;
-  if (cudaOccupancyMaxActiveClusters(&n, tc_pair_kernel, &cfg) != cudaSuccess || n <= 0) {
+  if (cudaOccupancyMaxActiveClusters(&n, tc_pair_kernel<0>, &cfg) != cudaSuccess || n <= 0) {
     cudaGetLastError();
     n = sms / 2;
   }
@@ -300,13 +337,35 @@ static int resident_pairs(int dev, int sms) {
   return n;
 }
 
+// Geometry of one launch over a batch slice of B rows: npt pair tiles, then
+// at most pairs / npt groups, as few as give every group the same number of
+// vocabulary tiles.
+struct PairGeometry {
+  int npt, n_groups;
+};
+
+static PairGeometry pair_geometry(int64_t B, int pairs, int64_t n_vt) {
+  PairGeometry g;
+  g.npt = static_cast<int>((B + 2 * kRowsPerCta - 1) / (2 * kRowsPerCta));
+  g.n_groups = std::max(1, pairs / g.npt);
+  const int64_t tiles = std::max<int64_t>(n_vt, 1);
+  const int64_t per = (tiles + g.n_groups - 1) / g.n_groups;
+  g.n_groups = static_cast<int>(std::max<int64_t>(1, (tiles + per - 1) / per));
+  return g;
+}
+
+static int device_sms(int* dev) {
+  int sms = 0;
+  cudaGetDevice(dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, *dev);
+  return sms > 0 ? sms : 148;
+}
+
 cudaError_t launch_tc_pair(const Problem& p, const Finish& f, int* err, cudaStream_t stream) {
   if (p.d < kBK || p.V_local <= 0) return cudaErrorNotSupported;
-  int dev = 0, sms = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (sms <= 0) sms = 148;
-  cudaError_t e = cudaFuncSetAttribute(tc_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  int dev = 0;
+  const int sms = device_sms(&dev);
+  cudaError_t e = cudaFuncSetAttribute(tc_pair_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   const int pairs = resident_pairs(dev, sms);
   CUtensorMap tw;
@@ -329,20 +388,60 @@ cudaError_t launch_tc_pair(const Problem& p, const Finish& f, int* err, cudaStre
       fs_slice.out_ids = f.out_ids + b0;
       fs_slice.out_max = f.out_max + b0;
     }
-    const int npt = static_cast<int>((ps.B + 2 * kRowsPerCta - 1) / (2 * kRowsPerCta));
-    int n_groups = std::max(1, pairs / npt);
-    {   // as few groups as give every group the same number of vocabulary tiles
-      const int64_t n_vt = (p.V_local + kBN - 1) / kBN;
-      const int64_t per = (n_vt + n_groups - 1) / n_groups;
-      n_groups = static_cast<int>(std::max<int64_t>(1, (n_vt + per - 1) / per));
-    }
+    const int n_vt = static_cast<int>((p.V_local + kBN - 1) / kBN);
+    const PairGeometry g = pair_geometry(ps.B, pairs, n_vt);
     CUtensorMap th;
     if (!encode_kmajor_bf16(&th, ps.h, ps.B, p.d, kBK, kRowsPerCta)) return cudaErrorInvalidValue;
-    PairArgs a{ps, fs_slice, npt, n_groups, static_cast<int>((p.V_local + kBN - 1) / kBN), err};
-    e = launch_kernel(tc_pair_kernel, dim3(2 * npt * n_groups), dim3(kThreads), kSmemBytes, stream, ps.pdl, th, tw, a);
+    PairArgs a{ps, fs_slice, g.npt, g.n_groups, n_vt, err};
+    e = launch_kernel(tc_pair_kernel<0>, dim3(2 * g.npt * g.n_groups), dim3(kThreads), kSmemBytes, stream, ps.pdl,
+                      th, tw, a);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
+}
+
+int64_t tc_pair_topk_max_rows(int device) {
+  int sms = 0;
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
+  return static_cast<int64_t>(resident_pairs(device, sms > 0 ? sms : 148)) * 2 * kRowsPerCta;
+}
+
+int tc_pair_topk_parts(int64_t B, int64_t V, int device) {
+  int sms = 0;
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
+  const int pairs = resident_pairs(device, sms > 0 ? sms : 148);
+  return pair_geometry(B, pairs, (V + kBN - 1) / kBN).n_groups;
+}
+
+template <int K>
+static cudaError_t launch_pair_topk_k(const Problem& p, Partial* partials, int* err, cudaStream_t stream) {
+  int dev = 0;
+  const int sms = device_sms(&dev);
+  const int pairs = resident_pairs(dev, sms);
+  if (p.B > static_cast<int64_t>(pairs) * 2 * kRowsPerCta) return cudaErrorNotSupported;   // one launch
+  cudaError_t e = cudaFuncSetAttribute(tc_pair_kernel<K>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes(K));
+  if (e != cudaSuccess) return e;
+  CUtensorMap tw, th;
+  if (!encode_kmajor_bf16(&tw, p.W, p.V_local, p.d, kBK, kBN / 2)) return cudaErrorInvalidValue;
+  if (!encode_kmajor_bf16(&th, p.h, p.B, p.d, kBK, kRowsPerCta)) return cudaErrorInvalidValue;
+  const int n_vt = static_cast<int>((p.V_local + kBN - 1) / kBN);
+  const PairGeometry g = pair_geometry(p.B, pairs, n_vt);
+  Finish f{};
+  f.partials = partials;
+  f.n_parts = g.n_groups;
+  PairArgs a{p, f, g.npt, g.n_groups, n_vt, err};
+  return launch_kernel(tc_pair_kernel<K>, dim3(2 * g.npt * g.n_groups), dim3(kThreads), smem_bytes(K), stream, p.pdl,
+                       th, tw, a);
+}
+
+cudaError_t launch_tc_pair_topk(const Problem& p, int K, Partial* partials, int* err, cudaStream_t stream) {
+  if (p.d < kBK || p.V_local <= 0) return cudaErrorNotSupported;
+  switch (K) {
+    case 4: return launch_pair_topk_k<4>(p, partials, err, stream);
+    case 8: return launch_pair_topk_k<8>(p, partials, err, stream);
+    case 16: return launch_pair_topk_k<16>(p, partials, err, stream);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace fs

@@ -55,7 +55,7 @@ def _run(fs, torch, h, W, temp, seed, step, k, bias=None):
 
 
 @pytest.mark.parametrize("k", [1, 3, 8, 16])
-@pytest.mark.parametrize("B,V,d", [(1, 50, 64), (5, 4097, 256), (37, 3001, 128), (130, 4097, 64)])
+@pytest.mark.parametrize("B,V,d", [(1, 50, 64), (5, 4097, 256), (37, 3001, 128), (100, 2500, 128), (130, 4097, 64)])
 def test_topk_matches_oracle(fs, torch_cuda, B, V, d, k):
     h, W, temp = _problem(B, V, d, seed=B + V + k)
     ids, z = _run(fs, torch_cuda, h, W, temp, 21, 4, k)
@@ -64,10 +64,13 @@ def test_topk_matches_oracle(fs, torch_cuda, B, V, d, k):
         assert np.all(ids[3] == -1)                       # invalid temperature
 
 
-def test_topk_masks_padding_and_ties(fs, torch_cuda):
-    B, V, d, k = 4, 300, 64, 8
+@pytest.mark.parametrize("B", [4, 200])
+def test_topk_masks_padding_and_ties(fs, torch_cuda, B):
+    """Rows 0-3 carry the special cases; B = 200 runs them through the CTA-pair
+    kernel, B = 4 through the vocabulary-major one."""
+    V, d, k = 300, 64, 8
     h, W, temp = _problem(B, V, d, seed=5)
-    temp[:] = [0.0, 1.0, 1.0, 0.7]
+    temp[:4] = [0.0, 1.0, 1.0, 0.7]
     W[40] = W[17]
     W[250] = W[17]                                        # equal logits at ids 17, 40, 250
     bias = np.zeros((B, V), np.float32)
@@ -82,16 +85,18 @@ def test_topk_masks_padding_and_ties(fs, torch_cuda):
     compare_topk(ids, z, otopk.sample_topk(h, W, temp, 3, 9, k, bias=bias), what="masks")
 
 
-@pytest.mark.parametrize("B", [20, 64, 100])
-def test_top1_equals_the_sampler_on_the_same_kernel(fs, torch_cuda, B):
+@pytest.mark.parametrize("B,path", [(20, "TC_VOCAB"), (64, "TC_VOCAB"), (100, "TC_BATCH"), (200, "TC_PAIR"),
+                                    (256, "TC_PAIR"), (300, "TC_BATCH"), (520, "TC_PAIR")])
+def test_top1_equals_the_sampler_on_the_same_kernel(fs, torch_cuda, B, path):
     """k = 1 through the top-k epilogue and the sample through the same kernel
-    (vocabulary-major for B <= 64, batch-major above) compute identical
+    (vocabulary-major for B <= 64, above that CTA pairs where 256-row pair
+    tiles waste fewer than 128 rows, else batch-major) compute identical
     scores: identical ids and maxima."""
     torch = torch_cuda
     V, d = 20011, 256
     h, W, temp = _problem(B, V, d, seed=77)
     hd, Wd, td = to_device(h, torch), to_device(W, torch), to_device(temp, torch)
-    fs.set_path(fs.FS_PATH_TC_VOCAB if B <= 64 else fs.FS_PATH_TC_BATCH)
+    fs.set_path(getattr(fs, "FS_PATH_" + path))
     try:
         s_ids, s_max = fs.sample(hd, Wd, td, 8, 1)
     finally:
@@ -146,7 +151,7 @@ def test_topk_empty_vocabulary(fs, torch_cuda):
     assert np.all(ids.cpu().numpy() == -1) and np.all(z.cpu().numpy() == -np.inf)
 
 
-@pytest.mark.parametrize("B,k", [(16, 8), (256, 4)])
+@pytest.mark.parametrize("B,k", [(16, 8), (100, 8), (256, 4)])
 def test_topk_llama3_8b_head(fs, torch_cuda, B, k):
     torch = torch_cuda
     wl = synthetic.workload("llama3_8b", B)
@@ -156,13 +161,13 @@ def test_topk_llama3_8b_head(fs, torch_cuda, B, k):
     compare_topk(ids, z, ref, rows=rows, what=f"8B head B={B} k={k}")
 
 
-@pytest.mark.parametrize("rows", [16, 200])
+@pytest.mark.parametrize("rows", [16, 100, 200])
 def test_topk_law_on_gpu(fs, torch_cuda, rows):
     """3 x 10^5 ordered pairs (k = 2) drawn on the GPU from one repeated row
     (every (row, step) has its own noise): chi-square against the
     Plackett-Luce law of drawing without replacement from softmax(logits / T),
     computed from scipy's softmax of the oracle's logits.  rows = 16 runs the
-    vocabulary-major kernel, 200 the batch-major one."""
+    vocabulary-major kernel, 100 the batch-major one, 200 the CTA-pair one."""
     from scipy import special, stats
     from oracle import sampler
     torch = torch_cuda
@@ -191,12 +196,13 @@ def test_topk_law_on_gpu(fs, torch_cuda, rows):
     assert stats.chisquare(counts[keep], probs[keep] * counts.sum()).pvalue > 0.01
 
 
-def test_topk_captured_in_cuda_graph(fs, torch_cuda):
+@pytest.mark.parametrize("B", [24, 256])
+def test_topk_captured_in_cuda_graph(fs, torch_cuda, B):
     """After one eager call of the same size, a top-k call can be captured
     into a CUDA graph; replays with a changed step buffer are not possible
     (the step is baked in), so the replay must reproduce the eager result."""
     torch = torch_cuda
-    B, V, d, k = 24, 5003, 128, 8
+    V, d, k = 5003, 128, 8
     h, W, temp = _problem(B, V, d, seed=31)
     hd, Wd, td = to_device(h, torch), to_device(W, torch), to_device(temp, torch)
     stream = torch.cuda.Stream()

@@ -23,7 +23,7 @@
 // in lockstep, so W comes from HBM once per group.
 //
 // Gumbel-top-k mode (kTopK > 0): every epilogue thread keeps its batch row's
-// K best perturbed scores instead of the best one; the two column halves
+// K best perturbed scores instead of the best one; the column parts
 // merge through shared memory and each CTA writes one list per (row, group)
 // for the merge kernel, with no in-kernel finish.
 #include <cuda.h>
@@ -42,10 +42,22 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kThreads = 320;
-constexpr int kEpiWarps = 8;
-constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
+// Warp roles: kEpi epilogue warps (kEpi / 4 per TMEM lane quarter, each
+// scanning that share of the tile's columns), then the TMA producer and the
+// MMA issuer.  The sampler runs 16 epilogue warps, four per scheduler (2.4%
+// faster than 8 at B = 512, 1% at 1024 and 256, in interleaved runs); 18
+// warps leave 96 registers a thread (the register file is split between the
+// four schedulers), which made the top-k lists spill and the B = 256, k = 8
+// call 2.5% slower, so the top-k variants keep 8.
+template <int kTopK>
+struct PairWarps {
+  static constexpr int kEpi = kTopK > 0 ? 8 : 16;
+  static constexpr int kParts = kEpi / 4;
+  static constexpr int kProducer = kEpi;
+  static constexpr int kMma = kEpi + 1;
+  static constexpr int kThreads = (kEpi + 2) * 32;
+};
+constexpr int kMaxColParts = 4;
 constexpr int kRowsPerCta = 128;    // batch rows of one CTA (half of the MMA M = 256)
 constexpr int kBN = 256;            // vocabulary rows per tile (MMA N); each CTA loads 128
 constexpr int kBK = 64;
@@ -58,8 +70,8 @@ constexpr int kOffB = kOffA + kStages * kATileBytes;
 constexpr int kOffBars = kOffB + kStages * kBTileBytes;
 constexpr int kNumBars = 2 * kStages + 5;
 constexpr int kOffMisc = kOffBars + kNumBars * 8;
-constexpr int kOffHalf = kOffMisc + 16;                        // Best[128]: second-half results
-constexpr int kOffTopK = kOffHalf + kRowsPerCta * 8;           // top-k mode: Partial[128][K] of the second half
+constexpr int kOffHalf = kOffMisc + 16;                        // Best[parts - 1][128]: other parts' results
+constexpr int kOffTopK = kOffHalf + (kMaxColParts - 1) * kRowsPerCta * 8;   // top-k mode: Partial[128][K] of one part
 constexpr int kSmemBytes = kOffTopK + 1024;
 constexpr int smem_bytes(int top_k) { return kSmemBytes + kRowsPerCta * top_k * 8; }
 constexpr uint16_t kPairMask = 0x3;
@@ -75,9 +87,13 @@ struct PairArgs {
 };
 
 template <int kTopK = 0>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairWarps<kTopK>::kThreads, 1)
 tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_constant__ CUtensorMap tmap_w,
                const PairArgs args) {
+  constexpr int kEpiWarps = PairWarps<kTopK>::kEpi;
+  constexpr int kColParts = PairWarps<kTopK>::kParts;
+  constexpr int kProducerWarp = PairWarps<kTopK>::kProducer;
+  constexpr int kMmaWarp = PairWarps<kTopK>::kMma;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + kOffBars);   // used in the even CTA
@@ -88,7 +104,7 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_constant
   uint32_t* tmem_base_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
   int* last_flag = reinterpret_cast<int*>(smem + kOffMisc + 8);
-  Best* half_best = reinterpret_cast<Best*>(smem + kOffHalf);
+  Best* part_best = reinterpret_cast<Best*>(smem + kOffHalf);
   if (kTopK == 0 && args.f.done != nullptr && args.f.carry_in) {
     // Early finalization: the two CTAs of a pair must take the same decision
     // (the running one would otherwise signal a peer that has left), so the
@@ -220,9 +236,9 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_constant
       }
     }
   } else {
-    // ---------------------------------------------------------------- epilogue (warps 0-7, both CTAs)
+    // ---------------------------------------------------------------- epilogue (warps 0-15, both CTAs)
     const int quad = warp & 3;
-    const int half = warp >> 2;
+    const int part = warp >> 2;                         // column part of the tile
     const int row_in_tile = quad * 32 + lane;
     const int64_t b = static_cast<int64_t>(pt) * 2 * kRowsPerCta + static_cast<int64_t>(rank) * kRowsPerCta + row_in_tile;
     const bool row_ok = b < p.B;
@@ -251,11 +267,11 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_constant
       if (!mbar_wait(&tfull_bar[acc], acc_phase, args.err, abort_flag)) break;
       tc_fence_after();
       const int vt = q + t * args.n_groups;
-      const int64_t col0 = static_cast<int64_t>(vt) * kBN + half * (kBN / 2);
+      const int64_t col0 = static_cast<int64_t>(vt) * kBN + part * (kBN / kColParts);
 #pragma unroll 1
-      for (int c = 0; c < kBN / 2; c += 32) {
+      for (int c = 0; c < kBN / kColParts; c += 32) {
         uint32_t r[32];
-        tmem_ld_32(tmem_base + lane_addr + acc * kBN + half * (kBN / 2) + c, r);
+        tmem_ld_32(tmem_base + lane_addr + acc * kBN + part * (kBN / kColParts) + c, r);
         tmem_ld_wait();
         const int64_t v0 = col0 + c;
         if (active && v0 < p.V_local) {
@@ -277,27 +293,38 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_constant
       if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&tempty_bar[acc]), 0));
     }
     if constexpr (kTopK > 0) {
-      // merge the two column halves' lists, then one list per (row, group)
+      // merge the column parts' lists into part 0's (one buffer, one part
+      // at a time), then one list per (row, group)
       Partial* other = reinterpret_cast<Partial*>(smem + kOffTopK) + row_in_tile * kTopK;
-      if (half == 1) {
+#pragma unroll 1
+      for (int src = 1; src < kColParts; ++src) {
+        if (part == src) {
 #pragma unroll
-        for (int j = 0; j < kTopK; ++j) other[j] = Partial{list.z[j], list.id[j]};
+          for (int j = 0; j < kTopK; ++j) other[j] = Partial{list.z[j], list.id[j]};
+        }
+        asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
+        if (part == 0) {
+#pragma unroll
+          for (int j = 0; j < kTopK; ++j) topk_offer(list, other[j].z, other[j].id);
+        }
+        asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
       }
-      asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
       if (p.pdl) pdl_wait();      // the previous call's merge kernel may still read the partials
-      if (half == 0 && row_ok) {
-#pragma unroll
-        for (int j = 0; j < kTopK; ++j) topk_offer(list, other[j].z, other[j].id);
+      if (part == 0 && row_ok) {
         Partial* dst = args.f.partials + (b * args.f.n_parts + q) * kTopK;
 #pragma unroll
         for (int j = 0; j < kTopK; ++j) dst[j] = Partial{list.z[j], list.id[j]};
       }
     } else {
-      // combine the two column halves of each row, then one candidate per (row, group)
-      if (half == 1) half_best[row_in_tile] = best;
+      // combine the column parts of each row, then one candidate per (row, group)
+      if (part != 0) part_best[(part - 1) * kRowsPerCta + row_in_tile] = best;
       asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
+      if (part == 0) {
+#pragma unroll
+        for (int src = 1; src < kColParts; ++src) best = combine(best, part_best[(src - 1) * kRowsPerCta + row_in_tile]);
+      }
       pdl_wait();                 // the finish area is shared with the previous launch
-      if (half == 0 && row_ok) push_candidate(args.f, b, combine(best, half_best[row_in_tile]));
+      if (part == 0 && row_ok) push_candidate(args.f, b, best);
       finish_grid(args.f, p.B, threadIdx.x, kEpiWarps * 32, last_flag,
                   named_bar1_and<kEpiWarps * 32>);
     }
@@ -326,7 +353,7 @@ static int resident_pairs(int dev, int sms) {
   int n = 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(2 * (sms / 2)));
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(PairWarps<0>::kThreads);
   cfg.dynamicSmemBytes = kSmemBytes;
   if (cudaOccupancyMaxActiveClusters(&n, tc_pair_kernel<0>, &cfg) != cudaSuccess || n <= 0) {
     cudaGetLastError();
@@ -393,7 +420,8 @@ cudaError_t launch_tc_pair(const Problem& p, const Finish& f, int* err, cudaStre
     CUtensorMap th;
     if (!encode_kmajor_bf16(&th, ps.h, ps.B, p.d, kBK, kRowsPerCta)) return cudaErrorInvalidValue;
     PairArgs a{ps, fs_slice, g.npt, g.n_groups, n_vt, err};
-    e = launch_kernel(tc_pair_kernel<0>, dim3(2 * g.npt * g.n_groups), dim3(kThreads), kSmemBytes, stream, ps.pdl,
+    e = launch_kernel(tc_pair_kernel<0>, dim3(2 * g.npt * g.n_groups), dim3(PairWarps<0>::kThreads), kSmemBytes,
+                      stream, ps.pdl,
                       th, tw, a);
     if (e != cudaSuccess) return e;
   }
@@ -430,7 +458,8 @@ static cudaError_t launch_pair_topk_k(const Problem& p, Partial* partials, int* 
   f.partials = partials;
   f.n_parts = g.n_groups;
   PairArgs a{p, f, g.npt, g.n_groups, n_vt, err};
-  return launch_kernel(tc_pair_kernel<K>, dim3(2 * g.npt * g.n_groups), dim3(kThreads), smem_bytes(K), stream, p.pdl,
+  return launch_kernel(tc_pair_kernel<K>, dim3(2 * g.npt * g.n_groups), dim3(PairWarps<K>::kThreads), smem_bytes(K),
+                       stream, p.pdl,
                        th, tw, a);
 }
 

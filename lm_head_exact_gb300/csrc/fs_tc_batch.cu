@@ -23,9 +23,14 @@
 //     thread keeps ITS batch row's running (max, argmax) in registers across
 //     all of the CTA's tiles and pushes one candidate per (row, CTA) at the
 //     end; the last CTA to finish writes the sample (fs_finish.cuh).
-//   * Warp roles (320 threads): warps 0-7 epilogue (TMEM lane = batch row;
-//     warps w and w + 4 share lanes and split the 256 columns in halves),
-//     warp 8 TMA producer, warp 9 TMEM allocator + MMA issuer.
+//   * Warp roles: kEpi epilogue warps (TMEM lane = batch row; warps w, w + 4,
+//     ... share lanes and split the 256 columns into kEpi / 4 parts), then
+//     the TMA producer and the TMEM allocator + MMA issuer.  The sampler runs
+//     16 epilogue warps when one batch tile covers the batch (B <= 128: the
+//     last tile's epilogue is exposed there; 172 -> 167 us at B = 128 in
+//     interleaved runs) and 8 above (B = 600: 471 vs 481 us with 16); the
+//     top-k variants run 8 (at 18 warps a thread gets 96 registers, too few
+//     for the lists).
 //   * Epilogue per element: z = logit * (1/T) + Gumbel(Philox); one Philox
 //     call serves the four consecutive vocabulary ids that share a counter.
 #include <cuda.h>
@@ -43,10 +48,15 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kThreads = 320;
-constexpr int kEpiWarps = 8;
-constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
+template <int kEpiWarps>
+struct BatchWarps {
+  static constexpr int kEpi = kEpiWarps;
+  static constexpr int kParts = kEpi / 4;
+  static constexpr int kProducer = kEpi;
+  static constexpr int kMma = kEpi + 1;
+  static constexpr int kThreads = (kEpi + 2) * 32;
+};
+constexpr int kMaxColParts = 4;
 constexpr int kBM = 128;            // batch rows per tile (MMA M)
 constexpr int kBN = 256;            // vocabulary rows per tile (MMA N)
 constexpr int kBK = 64;             // K per stage
@@ -59,8 +69,8 @@ constexpr int kOffB = kOffA + kStages * kATileBytes;
 constexpr int kOffBars = kOffB + kStages * kBTileBytes;
 constexpr int kNumBars = 2 * kStages + 5;
 constexpr int kOffMisc = kOffBars + kNumBars * 8;
-constexpr int kOffHalf = kOffMisc + 16;                            // Best[128]: second-half results
-constexpr int kOffTopK = kOffHalf + kBM * 8;                       // top-k mode: Partial[128][K] of the second half
+constexpr int kOffHalf = kOffMisc + 16;                            // Best[parts - 1][128]: other parts' results
+constexpr int kOffTopK = kOffHalf + (kMaxColParts - 1) * kBM * 8;  // top-k mode: Partial[128][K] of one part
 constexpr int kSmemBytes = kOffTopK + 1024;
 constexpr int smem_bytes(int top_k) { return kSmemBytes + kBM * top_k * 8; }
 
@@ -80,10 +90,14 @@ struct BatchArgs {
 // kTopK > 0 (with kStoreLogits = false): Gumbel-top-k epilogue -- every
 // thread keeps its batch row's K best perturbed scores, and each CTA writes
 // its per-row list to f.partials for the merge kernel (no in-kernel finish).
-template <bool kStoreLogits, int kTopK = 0>
-__global__ void __launch_bounds__(kThreads, 1)
+template <bool kStoreLogits, int kTopK, int kEpi>
+__global__ void __launch_bounds__(BatchWarps<kEpi>::kThreads, 1)
 tc_batch_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_constant__ CUtensorMap tmap_w,
                 const BatchArgs args) {
+  constexpr int kEpiWarps = BatchWarps<kEpi>::kEpi;
+  constexpr int kColParts = BatchWarps<kEpi>::kParts;
+  constexpr int kProducerWarp = BatchWarps<kEpi>::kProducer;
+  constexpr int kMmaWarp = BatchWarps<kEpi>::kMma;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + kOffBars);
@@ -98,7 +112,7 @@ tc_batch_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_constan
     early_skip_cta(args.f, args.p.B, args.p.pdl, last_flag);
     return;
   }
-  Best* half_best = reinterpret_cast<Best*>(smem + kOffHalf);
+  Best* part_best = reinterpret_cast<Best*>(smem + kOffHalf);
 
   const Problem& p = args.p;
   const int warp = threadIdx.x >> 5;
@@ -210,9 +224,9 @@ tc_batch_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_constan
       }
     }
   } else {
-    // ---------------------------------------------------------------- epilogue (warps 0-7)
+    // ---------------------------------------------------------------- epilogue (warps 0 .. kEpi - 1)
     const int quad = warp & 3;                 // TMEM lane quadrant
-    const int half = warp >> 2;                // column half of the 256-wide tile
+    const int part = warp >> 2;                // column part of the 256-wide tile
     const int row_in_tile = quad * 32 + lane;
     const int64_t b = static_cast<int64_t>(bt) * kBM + row_in_tile;
     const bool row_ok = b < p.B;
@@ -242,11 +256,11 @@ tc_batch_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_constan
       if (!mbar_wait(&tfull_bar[acc], acc_phase, args.err, abort_flag)) break;
       tc_fence_after();
       const int vt = q + t * args.n_groups;
-      const int64_t col0 = static_cast<int64_t>(vt) * kBN + half * (kBN / 2);   // local vocabulary row
+      const int64_t col0 = static_cast<int64_t>(vt) * kBN + part * (kBN / kColParts);   // local vocabulary row
 #pragma unroll 1
-      for (int c = 0; c < kBN / 2; c += 32) {
+      for (int c = 0; c < kBN / kColParts; c += 32) {
         uint32_t r[32];
-        tmem_ld_32(tmem_base + lane_addr + acc * kBN + half * (kBN / 2) + c, r);
+        tmem_ld_32(tmem_base + lane_addr + acc * kBN + part * (kBN / kColParts) + c, r);
         tmem_ld_wait();
         const int64_t v0 = col0 + c;                       // local id of r[0]
         if constexpr (kStoreLogits) {
@@ -279,30 +293,39 @@ tc_batch_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_constan
       mbar_arrive(&tempty_bar[acc]);
     }
     if constexpr (kTopK > 0) {
-      // merge the two column halves' lists, then one list per (row, group)
+      // merge the column parts' lists into part 0's (one buffer, one part
+      // at a time), then one list per (row, group)
       Partial* other = reinterpret_cast<Partial*>(smem + kOffTopK) + row_in_tile * kTopK;
-      if (half == 1) {
+#pragma unroll 1
+      for (int src = 1; src < kColParts; ++src) {
+        if (part == src) {
 #pragma unroll
-        for (int j = 0; j < kTopK; ++j) other[j] = Partial{list.z[j], list.id[j]};
+          for (int j = 0; j < kTopK; ++j) other[j] = Partial{list.z[j], list.id[j]};
+        }
+        asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
+        if (part == 0) {
+#pragma unroll
+          for (int j = 0; j < kTopK; ++j) topk_offer(list, other[j].z, other[j].id);
+        }
+        asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
       }
-      asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
       if (p.pdl) pdl_wait();      // the previous call's merge kernel may still read the partials
-      if (half == 0 && row_ok) {
-#pragma unroll
-        for (int j = 0; j < kTopK; ++j) topk_offer(list, other[j].z, other[j].id);
+      if (part == 0 && row_ok) {
         Partial* dst = args.f.partials + (b * args.f.n_parts + q) * kTopK;
 #pragma unroll
         for (int j = 0; j < kTopK; ++j) dst[j] = Partial{list.z[j], list.id[j]};
       }
     }
-    // combine the two column halves of each row, then one candidate per (row, group)
-    if constexpr (kTopK == 0) {
-      if (half == 1) half_best[row_in_tile] = best;
-      asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
-    }
+    // combine the column parts of each row, then one candidate per (row, group)
     if constexpr (!kStoreLogits && kTopK == 0) {
+      if (part != 0) part_best[(part - 1) * kBM + row_in_tile] = best;
+      asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
+      if (part == 0) {
+#pragma unroll
+        for (int src = 1; src < kColParts; ++src) best = combine(best, part_best[(src - 1) * kBM + row_in_tile]);
+      }
       pdl_wait();                 // the finish area is shared with the previous launch
-      if (half == 0 && row_ok) push_candidate(args.f, b, combine(best, half_best[row_in_tile]));
+      if (part == 0 && row_ok) push_candidate(args.f, b, best);
       finish_grid(args.f, p.B, threadIdx.x, kEpiWarps * 32, last_flag,
                   named_bar1_and<kEpiWarps * 32>);
     }
@@ -349,8 +372,14 @@ static cudaError_t launch_batch_impl(const Problem& p, const Finish* f, float* l
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (sms <= 0) sms = 148;
   const bool store = logits != nullptr;
-  cudaError_t e = store ? cudaFuncSetAttribute(tc_batch_kernel<true, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes)
-                        : cudaFuncSetAttribute(tc_batch_kernel<false, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  cudaError_t e = cudaSuccess;
+  if (store) {
+    e = cudaFuncSetAttribute(tc_batch_kernel<true, 0, 16>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  } else {
+    e = cudaFuncSetAttribute(tc_batch_kernel<false, 0, 16>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(tc_batch_kernel<false, 0, 8>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  }
   if (e != cudaSuccess) return e;
   CUtensorMap tw;
   if (!encode_kmajor_bf16(&tw, p.W, p.V_local, p.d, kBK, kBN)) return cudaErrorInvalidValue;
@@ -381,10 +410,14 @@ static cudaError_t launch_batch_impl(const Problem& p, const Finish* f, float* l
     BatchArgs a{ps, store ? logits + b0 * p.V_local : nullptr, fs_slice, g.nbt, g.n_groups,
                 static_cast<int>((p.V_local + kBN - 1) / kBN), err};
     if (store) {
-      tc_batch_kernel<true, 0><<<g.grid, kThreads, kSmemBytes, stream>>>(th, tw, a);
+      tc_batch_kernel<true, 0, 16><<<g.grid, BatchWarps<16>::kThreads, kSmemBytes, stream>>>(th, tw, a);
       e = cudaGetLastError();
+    } else if (g.nbt == 1) {
+      e = launch_kernel(tc_batch_kernel<false, 0, 16>, dim3(g.grid), dim3(BatchWarps<16>::kThreads), kSmemBytes,
+                        stream, ps.pdl, th, tw, a);
     } else {
-      e = launch_kernel(tc_batch_kernel<false, 0>, dim3(g.grid), dim3(kThreads), kSmemBytes, stream, ps.pdl, th, tw, a);
+      e = launch_kernel(tc_batch_kernel<false, 0, 8>, dim3(g.grid), dim3(BatchWarps<8>::kThreads), kSmemBytes,
+                        stream, ps.pdl, th, tw, a);
     }
     if (e != cudaSuccess) return e;
   }
@@ -413,7 +446,7 @@ static cudaError_t launch_topk_k(const Problem& p, Partial* partials, int* err, 
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (sms <= 0) sms = 148;
   if (p.B > static_cast<int64_t>(sms) * kBM) return cudaErrorNotSupported;   // one launch
-  cudaError_t e = cudaFuncSetAttribute(tc_batch_kernel<false, K>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(tc_batch_kernel<false, K, 8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        smem_bytes(K));
   if (e != cudaSuccess) return e;
   CUtensorMap tw, th;
@@ -425,7 +458,8 @@ static cudaError_t launch_topk_k(const Problem& p, Partial* partials, int* err, 
   f.partials = partials;
   f.n_parts = g.n_groups;
   BatchArgs a{ps, nullptr, f, g.nbt, g.n_groups, static_cast<int>((p.V_local + kBN - 1) / kBN), err};
-  return launch_kernel(tc_batch_kernel<false, K>, dim3(g.grid), dim3(kThreads), smem_bytes(K), stream, ps.pdl, th,
+  return launch_kernel(tc_batch_kernel<false, K, 8>, dim3(g.grid), dim3(BatchWarps<8>::kThreads), smem_bytes(K), stream,
+                       ps.pdl, th,
                        tw, a);
 }
 

@@ -359,9 +359,30 @@ def run_ours(args):
             _, km = time_steps(fs, torch, hdev[:b], Wdev, tdev[:b], seed, 23, 5, stream, bias=bb)
             us = tot / 20 * 1e3
             rf = roofline(b, dk, Vk, us, peaks, bias=bias is not None)
-            return {"workload": kind, "B": b, "us_per_step": round(us, 2),
-                    "fused_kernel_us_isolated": round(km * 1e3, 2), "roofline_us": rf["roofline_us"],
-                    "frac": rf["frac"], "bound": rf["bound"], "path": fs.path_for_batch(b)}
+            out = {"workload": kind, "B": b, "us_per_step": round(us, 2),
+                   "fused_kernel_us_isolated": round(km * 1e3, 2), "roofline_us": rf["roofline_us"],
+                   "frac": rf["frac"], "bound": rf["bound"], "path": fs.path_for_batch(b)}
+            if b >= 128:
+                out["library_gemm_us"] = library_gemm_us(hdev[:b], Wdev)
+            return out
+
+        def library_gemm_us(hdev, Wdev, n=20):
+            """Context for the contraction regime: the vendor library's plain
+            bf16 GEMM (torch.mm -> cuBLAS) on the same shape, logits only (bf16
+            out, no bias, no sampling), back to back, µs per call."""
+            logits = torch.empty((hdev.shape[0], Wdev.shape[0]), dtype=torch.bfloat16, device="cuda")
+            with torch.cuda.stream(stream):
+                for _ in range(3):
+                    torch.mm(hdev, Wdev.t(), out=logits)
+                g0 = torch.cuda.Event(enable_timing=True)
+                g1 = torch.cuda.Event(enable_timing=True)
+                g0.record(stream)
+                for _ in range(n):
+                    torch.mm(hdev, Wdev.t(), out=logits)
+                g1.record(stream)
+            torch.cuda.synchronize()
+            del logits
+            return round(g0.elapsed_time(g1) / n * 1e3, 2)
 
         h_big, t_big = big_batch()
         for b in SWEEP:

@@ -11,7 +11,7 @@
 // spans a cluster of two CTAs (tcgen05 cta_group::2): M = 256 batch rows
 // (128 per CTA, each CTA loads its own h rows) by N = 256 vocabulary rows
 // (each CTA loads HALF of the W tile, 128 rows), K = 64 per stage.  Per CTA a
-// stage is 32 KB instead of 48 KB, so six stages fit and each CTA moves a
+// stage is 32 KB instead of 48 KB, so seven stages fit and each CTA moves a
 // third fewer bytes from L2 for the same MMA work.  The even CTA of the pair
 // issues the MMAs and commits them to both CTAs' barriers; each CTA's TMEM
 // holds the accumulators of its own 128 batch rows x 256 vocabulary rows, and
@@ -61,7 +61,7 @@ constexpr int kMaxColParts = 4;
 constexpr int kRowsPerCta = 128;    // batch rows of one CTA (half of the MMA M = 256)
 constexpr int kBN = 256;            // vocabulary rows per tile (MMA N); each CTA loads 128
 constexpr int kBK = 64;
-constexpr int kStages = 6;
+constexpr int kStages = 7;
 constexpr int kATileBytes = kRowsPerCta * kBK * 2;     // 16 KB: this CTA's h rows
 constexpr int kBTileBytes = (kBN / 2) * kBK * 2;       // 16 KB: this CTA's half of the W tile
 constexpr int kTmemCols = 512;
@@ -70,10 +70,16 @@ constexpr int kOffB = kOffA + kStages * kATileBytes;
 constexpr int kOffBars = kOffB + kStages * kBTileBytes;
 constexpr int kNumBars = 2 * kStages + 5;
 constexpr int kOffMisc = kOffBars + kNumBars * 8;
-constexpr int kOffHalf = kOffMisc + 16;                        // Best[parts - 1][128]: other parts' results
-constexpr int kOffTopK = kOffHalf + (kMaxColParts - 1) * kRowsPerCta * 8;   // top-k mode: Partial[128][K] of one part
-constexpr int kSmemBytes = kOffTopK + 1024;
-constexpr int smem_bytes(int top_k) { return kSmemBytes + kRowsPerCta * top_k * 8; }
+// The epilogue's merge buffers are used only after the CTA's last tile has
+// been waited for, when every MMA has completed and every TMA load has
+// landed, so they alias the first stages; that leaves room for a seventh
+// stage (230.6 KB of the 232 KB a CTA may use).
+constexpr int kOffHalf = kOffA;                                              // Best[parts - 1][128]
+constexpr int kOffTopK = kOffHalf + (kMaxColParts - 1) * kRowsPerCta * 8;   // top-k mode: Partial[128][K]
+constexpr int kSmemBytes = kOffMisc + 16 + 1024;
+static_assert(kOffTopK + kRowsPerCta * 16 * 8 <= kOffBars, "merge buffers must fit in the stage memory");
+static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+constexpr int smem_bytes(int) { return kSmemBytes; }
 constexpr uint16_t kPairMask = 0x3;
 
 struct PairArgs {

@@ -398,6 +398,36 @@ def test_batch_larger_than_one_launch(fs, torch_cuda, forced):
     compare(ids, mx, sampler.sample(h, W, temp, 8, 2), what=f"B=20000 {forced}")
 
 
+def test_epilogue_warp_splits_agree(fs, torch_cuda):
+    """The batch-major kernel scans a tile with 16 epilogue warps when one
+    batch tile covers the batch (B <= 128) and with 8 above; the CTA-pair
+    kernel samples with 16 and keeps its top-k lists with 8.  How the columns
+    are split between warps must not change any score or decision: the same
+    rows agree bit for bit across the splits."""
+    torch = torch_cuda
+    V, d = 7001, 256
+    h, W, temp = _problem(300, V, d, seed=93)
+    hd, Wd, td = to_device(h, torch), to_device(W, torch), to_device(temp, torch)
+    fs.set_path(fs.FS_PATH_TC_BATCH)
+    try:
+        ids16, mx16 = fs.sample(hd[:128], Wd, td[:128], 6, 11)      # one batch tile: 16 warps
+        ids8, mx8 = fs.sample(hd, Wd, td, 6, 11)                    # three batch tiles: 8 warps
+    finally:
+        fs.set_path(fs.FS_PATH_AUTO)
+    fs.set_path(fs.FS_PATH_TC_PAIR)
+    try:
+        p_ids, p_mx = fs.sample(hd[:256], Wd, td[:256], 6, 11)      # pair sampler: 16 warps
+    finally:
+        fs.set_path(fs.FS_PATH_AUTO)
+    t_ids, t_z = fs.sample_topk(hd[:256], Wd, td[:256], 6, 11, 1)   # pair top-k: 8 warps
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(ids16.cpu().numpy(), ids8[:128].cpu().numpy())
+    np.testing.assert_array_equal(mx16.cpu().numpy(), mx8[:128].cpu().numpy())
+    np.testing.assert_array_equal(t_ids[:, 0].cpu().numpy(), p_ids.cpu().numpy())
+    np.testing.assert_array_equal(t_z[:, 0].cpu().numpy(), p_mx.cpu().numpy())
+    compare(ids8.cpu().numpy(), mx8.cpu().numpy(), sampler.sample(h, W, temp, 6, 11), what="8-warp batch")
+
+
 # ------------------------------------------------------------------ launch overlap
 @pytest.mark.parametrize("B", [2, 16, 96, 128, 256, 300])
 def test_launch_overlap_gives_identical_results(fs, torch_cuda, B):

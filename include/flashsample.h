@@ -221,8 +221,9 @@ FS_API fs_status fs_combine_shards(const float* shard_max, const int64_t* shard_
  *   1 <= k <= 16 (else FS_ERR_INVALID_ARG); B <= 4096 and d >= 64 (else
  *   FS_ERR_UNSUPPORTED).  Two launches: a tensor-core kernel with a K-list
  *   epilogue (K = 4, 8 or 16 >= k; the vocabulary-major kernel for B <= 64,
- *   above that the kernel fs_sample_ex runs at that B: CTA pairs or the
- *   batch-major one), writing one list per (row, CTA or CTA group) to library
+ *   above that the kernel fs_sample_ex runs at that B, fs_set_path included:
+ *   CTA pairs or the batch-major one, which also stands in for the other
+ *   families), writing one list per (row, CTA or CTA group) to library
  *   workspace, then a block-per-row merge.  The
  *   workspace grows on the first call of a size; capture in a CUDA graph only
  *   after an eager call of the same B.

@@ -662,10 +662,13 @@ fs_status fs_sample_topk(const void* h, const void* W, int64_t B, int64_t d, int
   p.pdl = g_launch_overlap.load() != 0;
   p.defer_inputs = p.pdl;
   // B <= 64: the vocabulary-major kernel (one lane per batch column keeps the
-  // lists); larger B: the kernel the sampler runs at that B, CTA pairs or the
-  // batch-major one (one thread per batch row in both).
+  // lists); larger B: the kernel the sampler runs at that B (fs_set_path
+  // included), CTA pairs or the batch-major one (one thread per batch row in
+  // both); the vocabulary-major and CUDA-core families have no list epilogue
+  // there, so those B take the batch-major one.
   const int family = B <= 64 ? kPathTcVocab
-                     : (auto_path(B) == kPathTcPair && B <= tc_pair_topk_max_rows(dev) ? kPathTcPair : kPathTcBatch);
+                     : (resolve_path(B, d) == kPathTcPair && B <= tc_pair_topk_max_rows(dev) ? kPathTcPair
+                                                                                             : kPathTcBatch);
   const int parts = V <= 0 ? 0
                     : family == kPathTcVocab ? tc_vocab_topk_parts(V, dev)
                     : family == kPathTcPair  ? tc_pair_topk_parts(B, V, dev)

@@ -85,12 +85,14 @@ def test_topk_masks_padding_and_ties(fs, torch_cuda, B):
     compare_topk(ids, z, otopk.sample_topk(h, W, temp, 3, 9, k, bias=bias), what="masks")
 
 
-@pytest.mark.parametrize("B,path", [(20, "TC_VOCAB"), (64, "TC_VOCAB"), (100, "TC_BATCH"), (200, "TC_PAIR"),
-                                    (256, "TC_PAIR"), (300, "TC_BATCH"), (520, "TC_PAIR")])
+@pytest.mark.parametrize("B,path", [(20, "AUTO"), (64, "AUTO"), (100, "AUTO"), (200, "AUTO"), (256, "AUTO"),
+                                    (300, "AUTO"), (520, "AUTO"), (256, "TC_BATCH"), (100, "TC_PAIR"),
+                                    (20, "TC_VOCAB")])
 def test_top1_equals_the_sampler_on_the_same_kernel(fs, torch_cuda, B, path):
     """k = 1 through the top-k epilogue and the sample through the same kernel
-    (vocabulary-major for B <= 64, above that CTA pairs where 256-row pair
-    tiles waste fewer than 128 rows, else batch-major) compute identical
+    (vocabulary-major for B <= 64; above that the sampler's own choice, CTA
+    pairs where 256-row pair tiles waste fewer than 128 rows, else
+    batch-major, or the family forced with set_path) compute identical
     scores: identical ids and maxima."""
     torch = torch_cuda
     V, d = 20011, 256
@@ -99,9 +101,9 @@ def test_top1_equals_the_sampler_on_the_same_kernel(fs, torch_cuda, B, path):
     fs.set_path(getattr(fs, "FS_PATH_" + path))
     try:
         s_ids, s_max = fs.sample(hd, Wd, td, 8, 1)
+        t_ids, t_z = fs.sample_topk(hd, Wd, td, 8, 1, 1)
     finally:
         fs.set_path(fs.FS_PATH_AUTO)
-    t_ids, t_z = fs.sample_topk(hd, Wd, td, 8, 1, 1)
     torch.cuda.synchronize()
     np.testing.assert_array_equal(t_ids[:, 0].cpu().numpy(), s_ids.cpu().numpy())
     np.testing.assert_array_equal(t_z[:, 0].cpu().numpy(), s_max.cpu().numpy())

@@ -50,15 +50,18 @@ def algorithmic_flops(B, d, V):
     return 2 * B * d * V
 
 
-# Sources that determine each fused kernel's code; the recorded ncu traffic of
-# a kernel (profiles/traffic.json) is only reported while their hash matches.
+# Sources that determine each fused kernel's code (and the compiler flags, in
+# build.py); the recorded ncu traffic of a kernel (profiles/traffic.json) is
+# only reported while their hash matches.
 _CSRC = os.path.join(ROOT, "lm_head_exact_gb300", "csrc")
-_SHARED = ["fs_device.cuh", "fs_sm100.cuh", "fs_finish.cuh", "fs_internal.h", "fs_tmap.cu", "fs_tmap.h"]
+_SHARED = ["fs_device.cuh", "fs_sm100.cuh", "fs_finish.cuh", "fs_internal.h", "fs_tmap.cu", "fs_tmap.h",
+           os.path.join("..", "build.py")]
+_TC = ["fs_epilogue.cuh"] + _SHARED
 KERNEL_SOURCES = {
-    "tc_vocab_kernel": ["fs_tc_vocab.cu"] + _SHARED,
-    "tc_batch_kernel": ["fs_tc_batch.cu"] + _SHARED,
+    "tc_vocab_kernel": ["fs_tc_vocab.cu"] + _TC,
+    "tc_batch_kernel": ["fs_tc_batch.cu"] + _TC,
     "simt_fused_kernel": ["fs_simt.cu"] + _SHARED,
-    "tc_pair_kernel": ["fs_tc_pair.cu"] + _SHARED,
+    "tc_pair_kernel": ["fs_tc_pair.cu"] + _TC,
 }
 PATH_KERNEL = {1: "simt_fused_kernel", 2: "tc_vocab_kernel", 3: "tc_batch_kernel", 4: "tc_pair_kernel"}
 

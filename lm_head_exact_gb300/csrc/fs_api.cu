@@ -249,11 +249,13 @@ fs_status check_problem(const Problem& p, bool need_out, const void* out_ids, co
 // model width, identical for every chunk of a chunked run) only -- never from
 // V or the chunk range -- so one-shot and chunked runs compute every logit
 // with the same kernel and agree bit for bit.
-constexpr int64_t kVocabMajorMaxBatch = 96;
+constexpr int64_t kVocabMajorMaxBatch = 64;
 
 // Auto rule, measured on GB300 (Llama-3-8B head, fused kernel µs):
 //   B = 1: CUDA-core kernel (161 vs 168 vocabulary-major);
-//   B <= 96: vocabulary-major (W streaming, 166-181);
+//   B <= 64: vocabulary-major (W streaming; back to back at B = 64: 161.2 vs
+//   167.3 for the batch-major kernel, while at every B from 72 to 96 the
+//   batch-major kernel wins, 167.3 vs 170.7, in alternating runs);
 //   larger B: the CTA-pair kernel when padding B to 256-row pair tiles wastes
 //   fewer than 128 rows (B = 256: 205 vs 217, B = 1024: 701 vs 729), otherwise
 //   the single-CTA batch-major kernel (B = 128: 185 vs 193, B = 384: 307 vs 344).

@@ -1,5 +1,5 @@
 // Tensor-core fused LM-head sampler, batch-major, one CTA per MMA: used for
-// 96 < B <= 128 and for batches that do not fill 256-row CTA-pair tiles (the
+// 64 < B <= 128 and for batches that do not fill 256-row CTA-pair tiles (the
 // pair kernel, fs_tc_pair.cu, takes the rest).  W tiles are shared by the
 // batch tiles of a CTA group through L2; from B ~ 300 on the contraction
 // bounds the step.

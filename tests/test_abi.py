@@ -117,3 +117,27 @@ def test_binding_constants_match_the_header():
     lib = binding.library()
     for name, value in status.items():
         assert lib.fs_status_string(value).decode() == name
+
+
+def test_auto_dispatch_rule(built_library):
+    """The batch-size rule (host logic, no GPU): B = 1 the CUDA-core kernel,
+    B <= 64 vocabulary-major, larger B CTA pairs where padding to 256-row pair
+    tiles wastes fewer than 128 rows, else batch-major; a forced family is
+    honoured (vocabulary-major only up to B = 256) and AUTO restores the rule."""
+    from lm_head_exact_gb300 import binding as fs
+    expect = {1: fs.FS_PATH_SIMT, 2: fs.FS_PATH_TC_VOCAB, 64: fs.FS_PATH_TC_VOCAB, 65: fs.FS_PATH_TC_BATCH,
+              96: fs.FS_PATH_TC_BATCH, 128: fs.FS_PATH_TC_BATCH, 129: fs.FS_PATH_TC_PAIR,
+              256: fs.FS_PATH_TC_PAIR, 300: fs.FS_PATH_TC_BATCH, 384: fs.FS_PATH_TC_BATCH,
+              385: fs.FS_PATH_TC_PAIR, 512: fs.FS_PATH_TC_PAIR, 600: fs.FS_PATH_TC_BATCH,
+              1024: fs.FS_PATH_TC_PAIR}
+    for B, path in expect.items():
+        assert fs.path_for_batch(B) == path, B
+    try:
+        fs.set_path(fs.FS_PATH_TC_VOCAB)
+        assert fs.path_for_batch(200) == fs.FS_PATH_TC_VOCAB
+        assert fs.path_for_batch(300) == fs.FS_PATH_TC_BATCH
+        fs.set_path(fs.FS_PATH_TC_PAIR)
+        assert fs.path_for_batch(16) == fs.FS_PATH_TC_PAIR
+    finally:
+        fs.set_path(fs.FS_PATH_AUTO)
+    assert fs.path_for_batch(16) == fs.FS_PATH_TC_VOCAB

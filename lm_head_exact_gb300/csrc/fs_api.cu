@@ -133,7 +133,10 @@ fs_status get_finish(cudaStream_t stream, int64_t B, Finish* f) {
   if (ws.finish_bytes < need) {
     s = grow(&ws.finish, &ws.finish_bytes, need, stream);
     if (s != FS_OK) return s;
-    cudaError_t e = cudaMemset(ws.finish, 0, ws.finish_bytes);
+    // on the call's stream: the kernels that use the area follow on it (a
+    // plain cudaMemset would run on the legacy default stream, which a
+    // non-blocking stream is not ordered after)
+    cudaError_t e = cudaMemsetAsync(ws.finish, 0, ws.finish_bytes, stream);
     if (e != cudaSuccess) {
       cudaGetLastError();
       return fail(FS_ERR_WORKSPACE, "zeroing the workspace failed: %s", cudaGetErrorString(e));

@@ -59,8 +59,9 @@ fs_status noalloc_fail(fs_status s, const char* msg) {
 }
 
 // Device address of the static scratch on the current device; the first
-// call per device resolves it and zeroes the whole array.
-fs_status scratch_for_current_device(unsigned char** out) {
+// call per device resolves it and zeroes the whole array on `stream`, the
+// stream of the call's kernel, so the kernel is ordered after the zeroing.
+fs_status scratch_for_current_device(cudaStream_t stream, unsigned char** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
     return noalloc_fail(FS_ERR_CUDA, "cannot query the current device");
@@ -72,7 +73,7 @@ fs_status scratch_for_current_device(unsigned char** out) {
       cudaGetLastError();
       return noalloc_fail(FS_ERR_CUDA, "cudaGetSymbolAddress of the static scratch failed");
     }
-    e = cudaMemset(ptr, 0, kScratchBytes);
+    e = cudaMemsetAsync(ptr, 0, kScratchBytes, stream);
     if (e != cudaSuccess) {
       cudaGetLastError();
       return noalloc_fail(FS_ERR_CUDA, "clearing the static scratch failed");
@@ -117,11 +118,11 @@ extern "C" FS_API fs_status fs_sample_noalloc(const void* h, const void* W, int6
       (V > 0 && !is_device_ptr(W)))
     return noalloc_fail(FS_ERR_INVALID_ARG, "h, W, temp, out_ids and out_max must be device memory");
 
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
   unsigned char* scratch = nullptr;
-  fs_status s = scratch_for_current_device(&scratch);
+  fs_status s = scratch_for_current_device(stream, &scratch);
   if (s != FS_OK) return s;
   int* status_word = reinterpret_cast<int*>(scratch);
-  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
   Finish f{};
   f.counter = reinterpret_cast<unsigned int*>(scratch + kCounterOffset);
   f.keys = reinterpret_cast<unsigned long long*>(scratch + kHeaderBytes);

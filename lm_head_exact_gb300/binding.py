@@ -234,7 +234,8 @@ def sample_tp(h, W_shard, v_begin, temp, seed, step, group=None, bias_shard=None
 def sample_topk(h, W, temp, seed, step, k, bias=None, out=None, stream=None):
     """Gumbel-top-k: k ids per row without replacement, best first.
     Returns (ids int64 [B, k], z fp32 [B, k]); -1 / -inf where a row has
-    fewer than k choosable ids."""
+    fewer than k choosable ids.  1 <= k <= 16, B <= 4096; k = 1 gives
+    sample()'s ids and maxima."""
     torch = _torch()
     B, d = h.shape
     V = W.shape[0]
@@ -277,8 +278,9 @@ def sample_chunked_early(h, W_chunk, v_begin, temp, seed, step, carry_max, carry
                          serial=False):
     """sample_chunked with online early finalization: ``h_norms`` fp32 [B]
     (row_norms(h)), ``rest_w_norm`` / ``rest_bias_max`` host floats bounding
-    the later chunks, ``done`` a device int32 [1] flag that the first call
-    writes and later calls read (set: they skip their work).  ``serial``
+    the later chunks, ``done`` a device int32 [1] flag: the first call
+    resets it, a chunk sets it once every row's carried best can no longer be
+    overtaken, and later calls that see it set skip their work.  ``serial``
     launches the call without overlapping the previous one."""
     torch = _torch()
     B, d = h.shape

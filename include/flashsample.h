@@ -270,8 +270,14 @@ FS_API fs_status fs_sample_host(const void* h_host, const void* W, int64_t B, in
 
 /*
  * fs_sample without any device-memory allocation.  (An engineering variant:
- * the FlashSampling paper has no counterpart.)  Same arguments, results and
- * noise as fs_sample, computed by the same tensor-core kernel, but the
+ * the FlashSampling paper has no counterpart.)  Same arguments, noise and
+ * sampled distribution as fs_sample, but it always runs the vocabulary-major
+ * tensor-core kernel, whatever B and fs_set_path say (fs_sample picks the
+ * kernel family from B: the CUDA-core kernel at B = 1, the batch-major or
+ * CTA-pair kernels above B = 64).  Its results therefore equal fs_sample's
+ * bit for bit for 2 <= B <= 64 under FS_PATH_AUTO, and otherwise agree with
+ * them within the parity tolerance (ids may differ only on rows whose two
+ * best perturbed scores are within rounding of each other).  The
  * cross-tile finish area (ticket counter + one candidate key per row) lives
  * in a fixed static device array inside the library (2.3 KB per GPU, held
  * until the process exits) instead of a workspace the library cudaMalloc's
@@ -280,7 +286,12 @@ FS_API fs_status fs_sample_host(const void* h_host, const void* W, int64_t B, in
  * the GPU's memory budget, or code that cannot afford the device-wide
  * synchronization of cudaFree.
  *   Limits: 1 <= B <= 256 (larger B returns FS_ERR_UNSUPPORTED with a
- *   message), d >= 64 and a multiple of 8; no bias.
+ *   message), d >= 64 and a multiple of 8; no bias.  Alignment: h and W
+ *   16 bytes, out_ids 8, temp and out_max 4 (else FS_ERR_UNSUPPORTED,
+ *   before anything is enqueued).
+ *   Errors on the device: a bounded wait that runs out sets a status word
+ *   in the same static array; fs_device_error() reports and clears it and
+ *   allocates nothing.
  *   Set-up: the first call on each device looks up the array's device
  *   address (cudaGetSymbolAddress) and zeroes it; make that first call
  *   before any stream capture starts.
@@ -335,8 +346,9 @@ FS_API int fs_path_for_batch(int64_t B);
  */
 FS_API fs_status fs_profile_events(void* start, void* stop);
 
-/* Read and clear the device error word of the current device (synchronizes
- * the device).  *code receives 0 when no kernel reported a problem. */
+/* Read and clear the device error words of the current device -- the
+ * library's own and fs_sample_noalloc's -- after synchronizing the device.
+ * *code receives 0 when no kernel reported a problem.  Allocates nothing. */
 FS_API fs_status fs_device_error(int* code);
 
 /*
@@ -377,6 +389,23 @@ FS_API const char* fs_last_error(void);
 FS_API fs_status fs_debug_noise(uint64_t seed, uint64_t step, int64_t row0, int64_t n_rows,
                          int64_t v0, int64_t n_vocab, uint32_t* words, float* gumbel,
                          void* stream);
+
+/*
+ * Logit inspection of the FUSED kernels, for parity tests (the fused path
+ * never writes logits, so this is how its accumulators are checked; summary
+ * page, "Method": the logit tile is computed on chip).  Runs exactly the
+ * launch fs_sample_ex would run for these arguments -- the same kernel
+ * family (from B and fs_set_path), instantiation and grid, same outputs --
+ * with the kernel's inspection store switched on: every logit it forms, the
+ * fp32 accumulator plus the bias (before the division by T and the noise),
+ * is also written to logits_out[b * V + v] (device, fp32 [B, V], 4-byte
+ * aligned; every element is written, rows with an invalid T included).
+ * Slow (the store is uncoalesced in the vocabulary-major kernel): for tests.
+ */
+FS_API fs_status fs_debug_fused_logits(const void* h, const void* W, int64_t B, int64_t d, int64_t V,
+                                       const float* temp, const float* bias, int64_t bias_row_stride,
+                                       uint64_t seed, uint64_t step, int64_t* out_ids, float* out_max,
+                                       float* logits_out, void* stream);
 
 #ifdef __cplusplus
 }

@@ -63,6 +63,8 @@ SIGNATURES = {
     "fs_status_string": (ctypes.c_char_p, [_int]),
     "fs_last_error": (ctypes.c_char_p, []),
     "fs_debug_noise": (_int, [_u64, _u64, _i64, _i64, _i64, _i64, _c_void_p, _c_void_p, _c_void_p]),
+    "fs_debug_fused_logits": (_int, [_c_void_p, _c_void_p, _i64, _i64, _i64, _c_void_p, _c_void_p, _i64,
+                                     _u64, _u64, _c_void_p, _c_void_p, _c_void_p, _c_void_p]),
 }
 
 
@@ -161,6 +163,25 @@ def sample(h, W, temp, seed, step, bias=None, out=None, stream=None):
                                  seed, step, _dev(ids, "out_ids", torch.int64),
                                  _dev(mx, "out_max", torch.float32), _stream_ptr(stream)))
     return ids, mx
+
+
+def debug_fused_logits(h, W, temp, seed, step, bias=None, stream=None):
+    """``sample`` with the fused kernel's logit inspection store switched on:
+    returns (ids, max, logits fp32 [B, V]), the logits being the values the
+    fused kernel's epilogue read (accumulator + bias, before temperature and
+    noise).  Same kernel family, instantiation and launch as ``sample``."""
+    torch = _torch()
+    B, d = h.shape
+    V = W.shape[0]
+    ids, mx = _outs(B, h.device, None)
+    logits = torch.full((B, V), float("nan"), dtype=torch.float32, device=h.device)
+    bptr, bstride = _bias_args(bias, B, V)
+    check(library().fs_debug_fused_logits(_dev(h, "h", torch.bfloat16, 2), _dev(W, "W", torch.bfloat16, 2),
+                                          B, d, V, _dev(temp, "temp", torch.float32, 1), bptr, bstride,
+                                          seed, step, _dev(ids, "out_ids", torch.int64),
+                                          _dev(mx, "out_max", torch.float32), _dev(logits, "logits_out"),
+                                          _stream_ptr(stream)))
+    return ids, mx, logits
 
 
 def sample_unfused(h, W, temp, seed, step, bias=None, logits_out=None, out=None, stream=None):

@@ -147,10 +147,13 @@ fs_status get_finish(cudaStream_t stream, int64_t B, Finish* f) {
   return FS_OK;
 }
 
-// The device error word of the current device (allocated zeroed on first use).
-fs_status error_word(int** out) {
+// The device error word of the current device, allocated on first use and
+// zeroed on `stream` -- the stream of the kernels that will report to it, so
+// they are ordered after the zeroing even on a non-blocking stream.  Not
+// allowed during stream capture (fs_workspace_reserve creates it first).
+fs_status error_word(int** out, cudaStream_t stream) {
   int dev;
-    {
+  {
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
   }
@@ -160,13 +163,33 @@ fs_status error_word(int** out) {
     *out = it->second;
     return FS_OK;
   }
+  if (capturing(stream))
+    return fail(FS_ERR_WORKSPACE, "the device error word must be created during stream capture; "
+                "call fs_workspace_reserve() before capturing");
   int* w = nullptr;
   cudaError_t e = cudaMalloc(&w, sizeof(int));
-  if (e == cudaSuccess) e = cudaMemset(w, 0, sizeof(int));
-  if (e != cudaSuccess) return fail(FS_ERR_WORKSPACE, "device error word: %s", cudaGetErrorString(e));
+  if (e == cudaSuccess) e = cudaMemsetAsync(w, 0, sizeof(int), stream);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    if (w != nullptr) cudaFree(w);
+    return fail(FS_ERR_WORKSPACE, "device error word: %s", cudaGetErrorString(e));
+  }
   g_error_words[dev] = w;
   *out = w;
   return FS_OK;
+}
+
+// The error word of the current device if one exists (nullptr otherwise);
+// never allocates.
+int* existing_error_word() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(g_ws_mutex);
+  auto it = g_error_words.find(dev);
+  return it == g_error_words.end() ? nullptr : it->second;
 }
 
 // ---------------------------------------------------------------- checks
@@ -302,7 +325,7 @@ fs_status run(Problem p, Finish f, cudaStream_t stream) {
     p.pdl = false;
   }
   int* err = nullptr;
-  if (path != kPathSimt) FS_TRY(error_word(&err));
+  if (path != kPathSimt) FS_TRY(error_word(&err, stream));
   cudaError_t e = cudaSuccess;
   if (g_prof_start != nullptr) {
     e = cudaEventRecord(g_prof_start, stream);
@@ -415,6 +438,28 @@ fs_status fs_sample_ex(const void* h, const void* W, int64_t B, int64_t d, int64
   // bias are read only after its dependency wait.
   p.pdl = g_launch_overlap.load() != 0;
   p.defer_inputs = p.pdl;
+  Finish f{};
+  f.write_out = true;
+  f.out_ids = out_ids;
+  f.out_max = out_max;
+  return run(p, f, static_cast<cudaStream_t>(stream));
+}
+
+fs_status fs_debug_fused_logits(const void* h, const void* W, int64_t B, int64_t d, int64_t V,
+                                const float* temp, const float* bias, int64_t bias_row_stride,
+                                uint64_t seed, uint64_t step, int64_t* out_ids, float* out_max,
+                                float* logits_out, void* stream) {
+  g_last_error[0] = '\0';
+  Problem p{h, W, B, d, V, 0, temp, bias, bias_row_stride, seed, step};
+  FS_TRY(check_problem(p, true, out_ids, out_max));
+  if (B > 0 && V > 0) {
+    FS_TRY(check_device_ptr(logits_out, "logits_out"));
+    FS_TRY(check_aligned(logits_out, 4, "logits_out"));
+  }
+  // exactly fs_sample_ex's launch, with the kernel's logit store switched on
+  p.pdl = g_launch_overlap.load() != 0;
+  p.defer_inputs = p.pdl;
+  p.dbg_logits = logits_out;
   Finish f{};
   f.write_out = true;
   f.out_ids = out_ids;
@@ -689,7 +734,7 @@ fs_status fs_sample_topk(const void* h, const void* W, int64_t B, int64_t d, int
   cudaError_t e = cudaSuccess;
   if (V > 0) {
     int* err = nullptr;
-    FS_TRY(error_word(&err));
+    FS_TRY(error_word(&err, stream));
     e = family == kPathTcVocab ? launch_tc_vocab_topk(p, K, partials, err, stream)
         : family == kPathTcPair ? launch_tc_pair_topk(p, K, partials, err, stream)
                                 : launch_tc_topk(p, K, partials, err, stream);
@@ -736,7 +781,7 @@ fs_status fs_sample_unfused(const void* h, const void* W, int64_t B, int64_t d, 
   float* logits = logits_out ? logits_out : reinterpret_cast<float*>(buf);
   float* probs = reinterpret_cast<float*>(logits_out ? buf : buf + plane);
   int* err = nullptr;
-  FS_TRY(error_word(&err));
+  FS_TRY(error_word(&err, stream));
   cudaError_t e = launch_tc_logits(p, logits, err, stream);
   if (e != cudaSuccess) return cuda_fail(e, "logits GEMM launch");
   e = launch_unfused_tail(p, logits, probs, out_ids, out_max, stream);
@@ -753,7 +798,7 @@ fs_status fs_workspace_reserve(int64_t B, int64_t V, void* stream) {
   g_last_error[0] = '\0';
   if (B < 0 || V < 0) return fail(FS_ERR_INVALID_ARG, "need B >= 0 and V >= 0");
   int* err = nullptr;
-  FS_TRY(error_word(&err));           // allocated once per device, never during capture
+  FS_TRY(error_word(&err, static_cast<cudaStream_t>(stream)));   // once per device, never during capture
   Finish f{};
   return get_finish(static_cast<cudaStream_t>(stream), B, &f);
 }
@@ -813,11 +858,19 @@ fs_status fs_device_error(int* code) {
   *code = 0;
   cudaError_t e = cudaDeviceSynchronize();
   if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
-  int* w = nullptr;
-  FS_TRY(error_word(&w));
-  e = cudaMemcpy(code, w, sizeof(int), cudaMemcpyDeviceToHost);
-  if (e == cudaSuccess) e = cudaMemset(w, 0, sizeof(int));
-  if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
+  // the library's word, if any call on this device created it (reading
+  // allocates nothing, so callers of fs_sample_noalloc may call this too)
+  int* w = existing_error_word();
+  if (w != nullptr) {
+    e = cudaMemcpy(code, w, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess) e = cudaMemset(w, 0, sizeof(int));
+    if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
+  }
+  // fs_sample_noalloc's word, in its static scratch
+  int na = 0;
+  e = noalloc_take_status(&na);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the allocation-free entry point's status word");
+  if (*code == 0) *code = na;
   return FS_OK;
 }
 
@@ -826,7 +879,7 @@ fs_status fs_debug_wait_timeout(uint64_t timeout_ns, void* stream) {
   if (timeout_ns == 0 || timeout_ns > 1000000000ull)
     return fail(FS_ERR_INVALID_ARG, "timeout_ns must be in (0, 1e9]");
   int* err = nullptr;
-  FS_TRY(error_word(&err));
+  FS_TRY(error_word(&err, static_cast<cudaStream_t>(stream)));
   cudaError_t e = launch_debug_wait(err, timeout_ns, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "wait kernel launch");
   return FS_OK;

@@ -154,11 +154,14 @@ struct __align__(8) Partial {
 // total order above, so atomicMax over all CTAs' candidates is the cross-tile
 // reduction (order-independent, hence deterministic).  High 32 bits: z mapped
 // to an order-preserving unsigned; low 32 bits: 0xFFFFFFFF - id (a smaller id
-// is larger).  0 means "no candidate" and is below every real key.
+// is larger).  0 means "no candidate" and is below every real key.  -0.0 is
+// keyed as +0.0: the two scores are equal under the total order, so between
+// them the smaller id must win, as it does in beats() and in the oracle.
 // -------------------------------------------------------------------------
 __device__ __forceinline__ unsigned long long pack_key(float z, int32_t id) {
   if (id == kNoId) return 0ull;
   uint32_t u = __float_as_uint(z);
+  if (u == 0x80000000u) u = 0u;
   u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
   return (static_cast<unsigned long long>(u) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(id));
 }

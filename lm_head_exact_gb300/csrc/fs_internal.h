@@ -39,6 +39,12 @@ struct Problem {
   // Global index of row 0 of h in this launch (a batch split over several
   // launches); the noise counter always uses the global row.
   int64_t row_offset = 0;
+  // Parity inspection (fs_debug_fused_logits), normally nullptr: when set,
+  // the fused kernel also stores every logit it forms -- the fp32
+  // accumulator plus the bias, before the temperature and the noise -- at
+  // dbg_logits[b * V_local + v] for rows b < B of this launch, from the same
+  // accumulator values its epilogue scans.
+  float* dbg_logits = nullptr;
 };
 
 // Launch `kernel` on `stream`, as a programmatic dependent launch when `pdl`.
@@ -154,6 +160,12 @@ cudaError_t launch_combine_shards(const float* shard_max, const int64_t* shard_i
                                   int64_t* out_ids, float* out_max, cudaStream_t stream);
 
 cudaError_t launch_reduce(const Finish& f, int64_t B, cudaStream_t stream);
+
+// Status word of fs_sample_noalloc on the current device (the bounded-wait
+// error word inside its static scratch): read into *code and cleared, with
+// no allocation; 0 when that entry point has not run on the device.  The
+// caller has synchronized the device.
+cudaError_t noalloc_take_status(int* code);
 
 // Set the calling thread's fs_last_error() text.
 void record_error(const char* msg);

@@ -1,6 +1,9 @@
 // fs_sample_noalloc: the tensor-core sampling path with its scratch memory in
 // a fixed, statically allocated device array instead of the library's
-// cudaMalloc'ed workspace.
+// cudaMalloc'ed workspace.  It always runs the vocabulary-major tensor-core
+// kernel, whatever the batch size (fs_sample picks the family from B), so
+// its results agree with fs_sample's within the parity tolerance, and bit
+// for bit where fs_sample runs that kernel too (2 <= B <= 64).
 //
 // Why it exists: fs_sample finishes the sample through a small workspace (a
 // ticket counter and one packed candidate key per batch row) that the
@@ -28,6 +31,10 @@
 // zero for the next call.  Calls whose kernels overlap on the GPU (for
 // example on two streams without ordering between them) race on the array
 // and may return wrong samples: order them on one stream.
+//
+// The kernel's bounded waits report a timeout to the status word at the
+// start of the array; fs_device_error() reads and clears it (together with
+// the library's own error word) without allocating anything.
 #include <cstdio>
 #include <cstdint>
 #include <mutex>
@@ -94,6 +101,24 @@ bool is_device_ptr(const void* p) {
 }
 
 }  // namespace
+
+cudaError_t noalloc_take_status(int* code) {
+  *code = 0;
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaSuccess;
+  int* word = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_setup_mutex);
+    word = static_cast<int*>(g_scratch_ptr[dev]);
+  }
+  if (word == nullptr) return cudaSuccess;          // the entry point never ran on this device
+  e = cudaMemcpy(code, word, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess) e = cudaMemset(word, 0, sizeof(int));
+  return e;
+}
+
 }  // namespace fs
 
 using namespace fs;
@@ -114,6 +139,14 @@ extern "C" FS_API fs_status fs_sample_noalloc(const void* h, const void* W, int6
     return noalloc_fail(FS_ERR_INVALID_ARG, "NULL pointer");
   if (reinterpret_cast<uintptr_t>(h) % 16 || reinterpret_cast<uintptr_t>(W) % 16)
     return noalloc_fail(FS_ERR_UNSUPPORTED, "h and W must be 16-byte aligned");
+  // the kernel stores int64 ids and fp32 maxima and loads fp32 temperatures:
+  // a misaligned pointer is rejected here rather than faulting on the device
+  if (reinterpret_cast<uintptr_t>(temp) % 4)
+    return noalloc_fail(FS_ERR_UNSUPPORTED, "temp must be 4-byte aligned");
+  if (reinterpret_cast<uintptr_t>(out_ids) % 8)
+    return noalloc_fail(FS_ERR_UNSUPPORTED, "out_ids must be 8-byte aligned");
+  if (reinterpret_cast<uintptr_t>(out_max) % 4)
+    return noalloc_fail(FS_ERR_UNSUPPORTED, "out_max must be 4-byte aligned");
   if (!is_device_ptr(h) || !is_device_ptr(temp) || !is_device_ptr(out_ids) || !is_device_ptr(out_max) ||
       (V > 0 && !is_device_ptr(W)))
     return noalloc_fail(FS_ERR_INVALID_ARG, "h, W, temp, out_ids and out_max must be device memory");

@@ -115,22 +115,25 @@ simt_fused_kernel(Problem p, Finish f) {
         for (int off = 16; off > 0; off >>= 1) acc[b] += __shfl_xor_sync(0xffffffffu, acc[b], off);
       }
 
-      if (owns_row && rt.mode != kRowInvalid) {
+      if (owns_row) {
         float logit = 0.0f;
 #pragma unroll
         for (int b = 0; b < BG; ++b)
           if (lane == b) logit = acc[b];
         if (p.bias != nullptr) logit += p.bias[my_b * p.bias_stride + v];
-        const int64_t vg = p.v_offset + v;
-        float z = logit;
-        if (rt.mode == kRowSample) {
-          const uint4 words = noise_words(key, static_cast<uint32_t>(vg >> 2),
-                                          static_cast<uint32_t>(my_b), step_lo, step_hi);
-          z = fmaf(logit, rt.inv_t, gumbel_from_word(word_of(words, static_cast<uint32_t>(vg & 3))));
-        }
-        if (z > best.z) {  // ids rise within a warp, so strict > keeps the smaller id on ties
-          best.z = z;
-          best.id = static_cast<int32_t>(vg);
+        if (p.dbg_logits != nullptr) p.dbg_logits[my_b * p.V_local + v] = logit;   // parity inspection only
+        if (rt.mode != kRowInvalid) {
+          const int64_t vg = p.v_offset + v;
+          float z = logit;
+          if (rt.mode == kRowSample) {
+            const uint4 words = noise_words(key, static_cast<uint32_t>(vg >> 2),
+                                            static_cast<uint32_t>(my_b), step_lo, step_hi);
+            z = fmaf(logit, rt.inv_t, gumbel_from_word(word_of(words, static_cast<uint32_t>(vg & 3))));
+          }
+          if (z > best.z) {  // ids rise within a warp, so strict > keeps the smaller id on ties
+            best.z = z;
+            best.id = static_cast<int32_t>(vg);
+          }
         }
       }
     }

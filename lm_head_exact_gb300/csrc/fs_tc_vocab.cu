@@ -83,6 +83,18 @@ struct VocabCfg {
   static constexpr int kSmemBytes = kOffTopK + kTopKBytes + 1024;   // + alignment slack
 };
 
+// Parity inspection (Problem::dbg_logits): the logits of batch column b at
+// vocabulary rows row0 .. row0 + n - 1, from this lane's transposed column.
+// Kept out of line so the sampling epilogue's register allocation is the
+// same whether or not the store is compiled in.
+__device__ __noinline__ void dump_column(const Problem& p, const float* col, int b, int64_t row0, int n) {
+  for (int i = 0; i < n; ++i) {
+    float logit = col[i];
+    if (p.bias != nullptr) logit += p.bias[static_cast<int64_t>(b) * p.bias_stride + row0 + i];
+    p.dbg_logits[static_cast<int64_t>(b) * p.V_local + row0 + i] = logit;
+  }
+}
+
 struct VocabArgs {
   Problem p;
   Finish f;           // cross-CTA finish: packed keys, ticket, carry, outputs
@@ -297,6 +309,8 @@ tc_vocab_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
           for (int j = 0; j < C::kChunk; ++j) tr[j * 33 + lane] = __uint_as_float(r[j]);
           __syncwarp();
           const int b = c0 + lane;
+          if (p.dbg_logits != nullptr && lane < C::kChunk && b < B)   // parity inspection only
+            dump_column(p, tr + lane * 33, b, row0, n_rows);
           const int mode = (lane < C::kChunk && b < B) ? col_mode[b] : kRowInvalid;
           if (mode != kRowInvalid) {
             RowScan scan;

@@ -222,8 +222,16 @@ def sample(h_bits, W_bits, temp, seed, step, bias=None, rows=None, vocab_offset=
     rows, h_r, t_r, bias_r = _row_select(h_bits, temp, bias, rows)
     V = W_bits.shape[0]
     vocab_ids = np.arange(vocab_offset, vocab_offset + V, dtype=np.int64)
-    ell = logits(h_r, W_bits, bias_r)
-    z = scores(ell, t_r, seed, step, rows, vocab_ids)
+    return sample_from_logits(logits(h_r, W_bits, bias_r), t_r, seed, step, rows, vocab_ids)
+
+
+def sample_from_logits(ell, temp, seed, step, rows, vocab_ids):
+    """The sample given the fp64 logits (bias included) of ``rows``: scores,
+    then the total-order argmax and the top-two gap.  ``temp`` holds the
+    temperatures of ``rows``; ``vocab_ids`` labels the columns of ``ell``.
+    ``sample`` is logits followed by this; a caller that already holds the
+    logits of many rows (they do not depend on the step) can reuse them."""
+    z = scores(ell, temp, seed, step, rows, vocab_ids)
     ids, zmax = argmax_total_order(z, vocab_ids)
     return Sample(ids, zmax, top2_gap(z))
 

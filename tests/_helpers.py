@@ -1,17 +1,50 @@
-"""Helpers shared by the parity tests: moving seeded workloads to the device
-and the oracle comparison rule.
+"""Helpers shared by the parity tests: moving seeded workloads to the device,
+the oracle over many rows, and the oracle comparison rule.
 
-Comparison rule (the tolerance the benchmark spec states, see the
-design notes): sampled ids are bit-exact except on rows whose oracle top-two
-perturbed scores differ by less than ``BAND`` (= 2e-3); such rows are counted
-and must stay below 0.1% of the rows compared.  Winning scores agree within
-``MAX_TOL`` (= 2e-3).  Rows without a sample (-1) must agree exactly.
+Comparison rule: sampled ids are bit-exact except on rows whose oracle
+top-two perturbed scores differ by less than ``BAND`` (= 2e-3) -- there fp32
+accumulation (error ~1e-5 at d = 8192) and the fp32 Gumbel transform (error
+< 1e-5) may legitimately flip the winner -- and such mismatching rows must
+stay below 0.1% of the rows compared.  Winning scores agree within
+``MAX_TOL`` (= 2e-3), the same bound as the logits.  Rows without a sample
+(-1) must agree exactly.  Every comparison is logged in ``BAND_LOG`` (rows
+compared, rows inside the band, id mismatches) for the run's summary.
 """
+
+from concurrent.futures import ThreadPoolExecutor
 
 import numpy as np
 
 BAND = 2e-3
 MAX_TOL = 2e-3
+
+# (what, rows compared, rows whose oracle gap is inside the band, id mismatches)
+BAND_LOG = []
+
+
+def oracle_rows(ell, temp, seed, step, rows=None, block=64, threads=None):
+    """Oracle sample of many rows from their precomputed fp64 logits ``ell``
+    [R, V] (``sampler.logits``, bias included), in row blocks on a thread
+    pool: rows are independent, and numpy releases the GIL in the
+    elementwise work.  ``rows`` are the global batch rows of ``ell``'s rows
+    (their noise counters), default 0..R-1; ``temp`` holds their
+    temperatures."""
+    from oracle import sampler
+    R, V = ell.shape
+    rows = np.arange(R) if rows is None else np.asarray(rows, dtype=np.int64)
+    temp = np.asarray(temp, dtype=np.float32)
+    vocab = np.arange(V, dtype=np.int64)
+    starts = list(range(0, R, block))
+
+    def one(s):
+        e = min(R, s + block)
+        return sampler.sample_from_logits(ell[s:e], temp[s:e], seed, step, rows[s:e], vocab)
+
+    import os
+    with ThreadPoolExecutor(threads or max(1, min(16, os.cpu_count() or 1))) as ex:
+        parts = list(ex.map(one, starts))
+    return sampler.Sample(np.concatenate([p.ids for p in parts]), np.concatenate([p.zmax for p in parts]),
+                          np.concatenate([p.gap for p in parts]))
 
 
 def to_device(arr_bits_or_f32, torch):
@@ -42,6 +75,7 @@ def compare(ids_gpu, max_gpu, ref, rows=None, what=""):
                            f"rows {np.nonzero(bad)[0][:10]}, gpu {ids_gpu[bad][:10]}, "
                            f"oracle {ref.ids[bad][:10]}, gaps {ref.gap[bad][:10]}")
     n_mis = int(mism.sum())
+    BAND_LOG.append((what, n, int(np.sum(ref.gap < BAND)), n_mis))
     assert n_mis == 0 or n_mis < 1e-3 * n, f"{what}: {n_mis} near-tie mismatches in {n} rows"
     ok = ~none_ref
     err = np.abs(max_gpu[ok] - ref.zmax[ok])

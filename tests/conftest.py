@@ -50,3 +50,23 @@ def torch_cuda():
     import torch
     assert torch.cuda.is_available(), "GPU test run without a CUDA device"
     return torch
+
+
+def pytest_terminal_summary(terminalreporter):
+    """Near-tie statistics of the oracle comparisons run by this session:
+    rows compared, rows whose oracle top-two gap is inside the band, and id
+    mismatches (all of which must be inside the band)."""
+    try:
+        from _helpers import BAND_LOG
+    except ImportError:
+        return
+    big = [r for r in BAND_LOG if r[1] >= 256]
+    if not big:
+        return
+    tr = terminalreporter
+    tr.write_sep("-", "oracle comparisons of >= 256 rows: rows / in-band rows / id mismatches")
+    for what, n, n_band, n_mis in big:
+        tr.write_line(f"{what}: {n} rows, {n_band} in band, {n_mis} mismatches")
+    tot = sum(r[1] for r in BAND_LOG)
+    tr.write_line(f"all comparisons: {tot} rows, {sum(r[2] for r in BAND_LOG)} in band, "
+                  f"{sum(r[3] for r in BAND_LOG)} mismatches")

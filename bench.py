@@ -525,6 +525,15 @@ def run_ours(args):
             topk.append({"workload": "llama3_8b", "B": b, "k": k, "us_per_step": round(us, 2), "frac": rf["frac"],
                          "bound": rf["bound"], "launches_per_step": 2})
 
+    # the decode loop: a random-weight Llama-3-8B-shaped decoder body (32
+    # layers of projections + SwiGLU MLP) then the LM head, fused vs unfused
+    # sampling; the LM head's share of the decode step
+    decode = []
+    if want("decode"):
+        from lm_head_exact_gb300 import decode_loop
+        decode = decode_loop.measure(Wd, batches=(1, 16, 256), layers=32, steps=10, warmup=3)
+        torch.cuda.empty_cache()
+
     # the unfused comparison pipeline on the same workload: GEMM -> fp32
     # logits in HBM -> softmax -> sample (the traffic fusion removes)
     unfused = None
@@ -574,9 +583,22 @@ def run_ours(args):
             "chunked": chunked,
             "early_finalization": early,
             "topk": topk,
+            "decode_loop": decode,
         }
         if not args.no_cpu_baseline:
             result["cpu_baseline"] = cpu_baseline(B, args.cpu_seconds)
+        # compact table of every timed configuration, kept LAST so that a
+        # reader of the line's tail sees it: [workload, B, us/step, fraction
+        # of roofline, bound]; chunked entries name their chunk count
+        short = {"llama3_8b": "8b", "qwen3_8b": "qwen3", "llama3_70b": "70b+bias"}
+        summ = [["8b", B, round(us, 1), rf["frac"], rf["bound"][0]]]
+        summ += [[short[p["workload"]], p["B"], round(p["us_per_step"], 1), p["frac"], p["bound"][0]]
+                 for p in sweep]
+        summ += [[f"chunk{c['chunks']}", c["B"], round(c["us_per_step"], 1), c["frac"], c["bound"][0]]
+                 for c in chunked]
+        summ += [[f"decode{r['B']}", r["B"], r["fused_step_us"], r["fused_head_share"], "share"]
+                 for r in decode]
+        result["sweep_summary"] = summ
     if dist is not None:
         dist.destroy_process_group()
     return result
@@ -598,10 +620,47 @@ def cpu_cores():
         return os.cpu_count() or 1
 
 
-def cpu_baseline(B, seconds=20.0):
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else platform)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+def cpu_baseline_single_thread(B, seconds):
+    """The same oracle measurement in a child process whose BLAS and OpenMP
+    pools have one thread (the pools are sized when numpy loads, hence the
+    fresh process).  Returns its cpu_baseline dict, or None on failure."""
+    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    code = ("import json, sys; sys.path.insert(0, %r); import bench; "
+            "print(json.dumps(bench.cpu_baseline(%d, %r, single=False)))" % (ROOT, B, seconds))
+    try:
+        r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env,
+                           timeout=30 * seconds + 120)
+        return json.loads(r.stdout.strip().splitlines()[-1])
+    except (OSError, subprocess.SubprocessError, ValueError, IndexError):
+        return None
+
+
+def cpu_baseline(B, seconds=20.0, single=True):
     """The fp64 oracle, as it stands, timed on this host's cores on a bounded
     sample: all B rows against a slice of the vocabulary, scaled to the full
-    vocabulary (the oracle's cost is linear in V)."""
+    vocabulary (the oracle's cost is linear in V).  With ``single`` the same
+    measurement is repeated with one thread (a child process) and reported
+    beside it, with the CPU model."""
     from lm_head_exact_gb300 import synthetic
     kind = "llama3_8b"
     V = synthetic.SHAPES[kind]["V"]
@@ -619,9 +678,16 @@ def cpu_baseline(B, seconds=20.0):
         total += _oracle_step(h, W, temp, synthetic.SAMPLING_SEED, reps, rows)
         reps += 1
     per_step_us = total / reps * (V / rows) * 1e6
-    return {"value": round(per_step_us, 1), "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
-            "sample": f"{reps} oracle steps of B={B} rows x {rows} of {V} vocabulary rows, "
-                      f"scaled x{V / rows:.2f} to the full vocabulary; numpy fp64 (BLAS threads = cores)"}
+    threads = os.environ.get("OPENBLAS_NUM_THREADS") or str(cpu_cores())
+    out = {"value": round(per_step_us, 1), "unit": UNIT, "cores": cpu_cores() if threads != "1" else 1,
+           "kind": "oracle", "cpu_model": cpu_model(),
+           "sample": f"{reps} oracle steps of B={B} rows x {rows} of {V} vocabulary rows, "
+                     f"scaled x{V / rows:.2f} to the full vocabulary; numpy fp64 (BLAS threads = {threads})"}
+    if single:
+        one = cpu_baseline_single_thread(B, seconds / 2)
+        if one is not None:
+            out["single_thread"] = {"value": one["value"], "unit": UNIT, "cores": 1, "sample": one["sample"]}
+    return out
 
 
 def run_reference(args):
@@ -670,7 +736,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--path", choices=["auto", "simt", "vocab", "batch", "pair"], default="auto",
                     help="force a kernel family (profiling)")
-    ap.add_argument("--only", default="", help="comma list of extra sections: sweep,chunked,early,topk,unfused")
+    ap.add_argument("--only", default="",
+                    help="comma list of extra sections: sweep,chunked,early,topk,decode,unfused")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
     args = ap.parse_args(argv)

@@ -55,14 +55,28 @@ fs_status cuda_fail(cudaError_t e, const char* what) {
 }
 
 // ---------------------------------------------------------------- workspace
-// Per (device, stream): the finish area of the fused kernels -- a ticket
-// counter (at offset 0, padded to 256 bytes) followed by one packed 64-bit
-// candidate key per batch row; all zero between calls (zeroed on allocation,
-// re-zeroed by the last CTA of every call) -- plus staging for the host entry
-// point and the unfused pipeline's logits / probabilities.
+// Per (device, stream): the finish area of the fused kernels -- kKeySets
+// ticket counters (a 256-byte header) followed by kKeySets sets of one packed
+// 64-bit candidate key per batch row; all zero between uses (zeroed on
+// allocation, re-zeroed by the last CTA of every launch that used them) --
+// plus staging for the host entry point and the unfused pipeline's logits /
+// probabilities.
+//
+// One-shot calls use set 0.  The chunks of a chunked step use sets 0, 1, 2,
+// ... in turn (the chunk's sequence number since FS_CHUNK_FIRST, modulo
+// kKeySets), so consecutive chunks, which overlap on the GPU, never share
+// keys or a ticket and their CTAs need not wait for each other.  Each chunk
+// completes only after the previous one (its last CTA waits for it), and a
+// chunk that would reuse set 0 after the first is launched without overlap,
+// so every earlier chunk has completed -- and left its set zeroed -- before
+// any set is reused.
+constexpr int kKeySets = 32;
+
 struct Workspace {
   void* finish = nullptr;
   size_t finish_bytes = 0;
+  int64_t finish_rows = 0;      // rows per key set
+  int64_t chunk_seq = 0;        // sequence number of the last chunk call since FS_CHUNK_FIRST
   void* staging = nullptr;      // device staging of fs_sample_host
   size_t staging_bytes = 0;
   void* unfused = nullptr;      // logits + probabilities of fs_sample_unfused
@@ -81,8 +95,10 @@ std::map<int, int*> g_error_words;   // per device: kernels' bounded-wait error 
 constexpr size_t kFinishHeader = 256;
 
 size_t finish_bytes_for(int64_t B) {
-  return kFinishHeader + static_cast<size_t>(std::max<int64_t>(B, 1)) * sizeof(unsigned long long);
+  return kFinishHeader + static_cast<size_t>(kKeySets) * static_cast<size_t>(std::max<int64_t>(B, 1)) *
+                             sizeof(unsigned long long);
 }
+static_assert(kKeySets * sizeof(unsigned int) <= kFinishHeader, "ticket counters fit in the header");
 
 bool capturing(cudaStream_t stream) {
   cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
@@ -122,8 +138,24 @@ fs_status current_device(int* dev) {
   return FS_OK;
 }
 
-// The finish area of (current device, stream) for batches up to B rows.
-fs_status get_finish(cudaStream_t stream, int64_t B, Finish* f) {
+// Key set of a chunk call: FS_CHUNK_FIRST starts the sequence at 0, every
+// later chunk call on the stream takes the next number.  *overlap_ok is false
+// when the set wraps around to 0 (the call must then launch without overlap).
+fs_status next_chunk_set(cudaStream_t stream, bool first, int* set, bool* overlap_ok) {
+  int dev;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  std::lock_guard<std::mutex> lock(g_ws_mutex);
+  Workspace& ws = g_workspaces[{dev, stream}];
+  ws.chunk_seq = first ? 0 : ws.chunk_seq + 1;
+  *set = static_cast<int>(ws.chunk_seq % kKeySets);
+  *overlap_ok = first || *set != 0;
+  return FS_OK;
+}
+
+// The finish area of (current device, stream) for batches up to B rows:
+// key set `set` and its ticket counter.
+fs_status get_finish(cudaStream_t stream, int64_t B, Finish* f, int set = 0) {
   int dev;
   fs_status s = current_device(&dev);
   if (s != FS_OK) return s;
@@ -142,8 +174,10 @@ fs_status get_finish(cudaStream_t stream, int64_t B, Finish* f) {
       return fail(FS_ERR_WORKSPACE, "zeroing the workspace failed: %s", cudaGetErrorString(e));
     }
   }
-  f->counter = static_cast<unsigned int*>(ws.finish);
-  f->keys = reinterpret_cast<unsigned long long*>(static_cast<char*>(ws.finish) + kFinishHeader);
+  ws.finish_rows = static_cast<int64_t>((ws.finish_bytes - kFinishHeader) / (kKeySets * sizeof(unsigned long long)));
+  f->counter = static_cast<unsigned int*>(ws.finish) + set;
+  f->keys = reinterpret_cast<unsigned long long*>(static_cast<char*>(ws.finish) + kFinishHeader) +
+            static_cast<int64_t>(set) * ws.finish_rows;
   return FS_OK;
 }
 
@@ -305,8 +339,9 @@ int resolve_path(int64_t B, int64_t d) {
   return path;
 }
 
-// One fused launch (kernel + in-kernel cross-CTA finish) for one problem.
-fs_status run(Problem p, Finish f, cudaStream_t stream) {
+// One fused launch (kernel + in-kernel cross-CTA finish) for one problem,
+// finishing through key set `key_set` of the stream's workspace.
+fs_status run(Problem p, Finish f, cudaStream_t stream, int key_set = 0) {
   if (p.B == 0) return FS_OK;
   if (p.V_local == 0) {                 // no vocabulary: every row gets "no sample"
     f.partials = nullptr;
@@ -315,7 +350,7 @@ fs_status run(Problem p, Finish f, cudaStream_t stream) {
     if (e != cudaSuccess) return cuda_fail(e, "reduction kernel launch");
     return FS_OK;
   }
-  FS_TRY(get_finish(stream, p.B, &f));
+  FS_TRY(get_finish(stream, p.B, &f, key_set));
   const int path = resolve_path(p.B, p.d);
   // The tensor-core kernels defer their input reads (interleaved A/B runs on
   // GB300: the overlap saves 4-8 us per back-to-back step at every B from 2
@@ -413,7 +448,11 @@ fs_status sample_chunk(const void* h, const void* W_chunk, int64_t B, int64_t d,
     cudaError_t e = cudaMemsetAsync(early.done, 0, sizeof(int), static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(done)");
   }
-  return run(p, f, static_cast<cudaStream_t>(stream));
+  int set = 0;
+  bool overlap_ok = true;
+  if (B > 0) FS_TRY(next_chunk_set(static_cast<cudaStream_t>(stream), (flags & FS_CHUNK_FIRST) != 0, &set, &overlap_ok));
+  if (!overlap_ok) p.pdl = false;
+  return run(p, f, static_cast<cudaStream_t>(stream), set);
 }
 
 }  // namespace

@@ -7,9 +7,16 @@
 //      candidates, so the result does not depend on which CTA comes first);
 //   2. the CTA that finishes last -- counted with an atomic ticket -- reads
 //      and zeroes every key, merges the chunked variant's carry and writes the
-//      outputs, then zeroes the ticket for the next call.
+//      outputs, then zeroes the ticket for the next user of these keys.
 //
-// No CTA ever waits for another: there is no spin on a flag, only the ticket.
+// No CTA ever waits for another CTA of its grid: there is no spin on a flag,
+// only the ticket.  Every launch owns its keys and ticket while it runs (the
+// host gives each chunk of a chunked step its own set, rotating), so the
+// CTAs push without waiting for the previous launch; only the last CTA waits
+// for the previous kernel of the stream to complete (griddepcontrol.wait; a
+// no-op without a programmatic launch) before it reads the carry the
+// previous chunk wrote.  Hence a chunk completes only after the previous one
+// has, and the CTAs of consecutive chunks overlap freely.
 #pragma once
 
 #include "fs_internal.h"
@@ -92,6 +99,7 @@ __device__ __forceinline__ void finish_grid(const Finish& f, int64_t B, int tid,
   }
   bar_and(true);
   if (*flag) {
+    pdl_wait();                    // the previous chunk's carry (and its completion)
     __threadfence();
     bool all_final = true;
     for (int64_t b = tid; b < B; b += n) {
@@ -137,8 +145,8 @@ __device__ __forceinline__ bool early_done_cta(const Finish& f, int* slot) {
 // last chunk, the outputs.  Called by all threads of the CTA before any
 // warp-role split; `flag` is a shared-memory int.
 __device__ __forceinline__ void early_skip_cta(const Finish& f, int64_t B, bool pdl, int* flag) {
+  (void)pdl;
   pdl_launch_dependents();
-  if (pdl) pdl_wait();                         // the finish area is shared with the previous launch
   finish_grid(f, B, threadIdx.x, blockDim.x, flag, cta_bar_and);
 }
 

@@ -140,7 +140,6 @@ simt_fused_kernel(Problem p, Finish f) {
 
     if (lane < BG) warp_best[warp][lane] = best;
     __syncthreads();
-    pdl_wait();                                // the finish area is shared with the previous launch
     if (threadIdx.x < BG && b0 + threadIdx.x < p.B) {
       Best r = warp_best[0][threadIdx.x];
 #pragma unroll

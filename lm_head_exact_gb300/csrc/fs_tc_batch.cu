@@ -332,7 +332,8 @@ tc_batch_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_constan
 #pragma unroll
         for (int src = 1; src < kColParts; ++src) best = combine(best, part_best[(src - 1) * kBM + row_in_tile]);
       }
-      pdl_wait();                 // the finish area is shared with the previous launch
+      // no dependency wait before the push: this launch's keys and ticket are
+      // its own (only the grid's last CTA waits, in finish_grid)
       if (part == 0 && row_ok) push_candidate(args.f, b, best);
       finish_grid(args.f, p.B, threadIdx.x, kEpiWarps * 32, last_flag,
                   named_bar1_and<kEpiWarps * 32>);

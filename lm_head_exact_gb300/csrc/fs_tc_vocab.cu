@@ -377,7 +377,8 @@ tc_vocab_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
         for (int j = 0; j < kTopK; ++j) dst[j] = Partial{m.z[j], m.id[j]};
       }
     } else {
-      pdl_wait();                 // the finish area is shared with the previous launch
+      // no dependency wait before the push: this launch's keys and ticket are
+      // its own (only the grid's last CTA waits, in finish_grid)
 #pragma unroll
       for (int c = 0; c < C::kChunks; ++c) {
         const int b = c * C::kChunk + lane;

@@ -14,9 +14,11 @@ The body is a stand-in for the weight traffic and GEMMs of a decoder layer:
 RMSNorm, the q/k/v/o projections (no attention mixing: there is no KV cache
 here, so its reads, which depend on the context length, are left out) and the
 SwiGLU MLP.  Its kernels are PyTorch's (cuBLAS GEMMs, elementwise); only the
-LM head and the sampling run this library's kernels.  Timing: CUDA events on
-one stream, around the whole loop for the step time and around each step's
-LM-head call for the head time (see ``DecodeLoop.run``).
+LM head and the sampling run this library's kernels.  The embedding and body
+of a step are one CUDA-graph replay, so the step is bound by the GPU, not by
+the host's launch rate.  Timing: CUDA events on one stream, around the whole
+loop for the step time and around each step's LM-head call for the head time
+(see ``DecodeLoop.run``).
 """
 
 from dataclasses import dataclass
@@ -87,37 +89,59 @@ class DecodeLoop:
         else:
             fs.sample_unfused(x, self.W, temp, seed, step, out=(ids, mx), stream=stream)
 
+    def _body_graph(self, ids, stream):
+        """The embedding of ``ids`` and the body, captured once as a CUDA graph
+        (hundreds of small launches per step would otherwise be bound by the
+        host's launch rate, not by the GPU).  Replaying it reads the current
+        contents of ``ids`` and leaves the hidden state in the returned
+        tensor."""
+        torch = self.torch
+        with torch.cuda.stream(stream):
+            x = self.body(self.W[ids])                  # warm-up outside the capture
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            x = self.body(self.W[ids])
+        return graph, x
+
     def run(self, ids0, temp, steps, fused=True, seed=1234, warmup=3, stream=None):
         """``warmup`` + ``steps`` decode steps from token ids ``ids0`` [B]
-        (int64, device): embed (rows of W), body, LM head + sampling.
+        (int64, device): embed (rows of W), body, LM head + sampling; each
+        step's sampled ids are the next step's input.
 
-        Two timed passes on one stream: the whole loop between two events
-        (nothing recorded between the launches, so consecutive kernels keep
-        their launch overlap) gives the step time; a second pass with events
-        right before and after each step's LM-head call gives the head time.
-        Returns (StepTiming, the last step's ids)."""
+        The embedding and body are one CUDA-graph replay per step; the LM head
+        is this library's call, with the step counter advancing.  Two timed
+        passes on one stream: the whole loop between two events (nothing
+        recorded between the launches) gives the step time; a second pass with
+        events right before and after each step's LM-head call gives the head
+        time.  Returns (StepTiming, the last step's ids)."""
         torch = self.torch
-        stream = stream or torch.cuda.current_stream()
+        stream = stream or torch.cuda.Stream()
         B = ids0.shape[0]
         ids = ids0.clone()
         mx = torch.empty(B, dtype=torch.float32, device=ids.device)
+        graph, x = self._body_graph(ids, stream)
+        ids.copy_(ids0)
         with torch.cuda.stream(stream):
             for i in range(warmup):
-                self._head(self.body(self.W[ids]), temp, seed, i, ids, mx, fused, stream)
+                graph.replay()
+                self._head(x, temp, seed, i, ids, mx, fused, stream)
             t0 = torch.cuda.Event(enable_timing=True)
             t1 = torch.cuda.Event(enable_timing=True)
             t0.record(stream)
             for i in range(steps):
-                self._head(self.body(self.W[ids]), temp, seed, warmup + i, ids, mx, fused, stream)
+                graph.replay()
+                self._head(x, temp, seed, warmup + i, ids, mx, fused, stream)
             t1.record(stream)
             ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                   for _ in range(steps)]
             for i, (a, b) in enumerate(ev):
-                x = self.body(self.W[ids])
+                graph.replay()
                 a.record(stream)
                 self._head(x, temp, seed, warmup + steps + i, ids, mx, fused, stream)
                 b.record(stream)
         torch.cuda.synchronize()
+        del graph
         step_us = t0.elapsed_time(t1) / steps * 1e3
         head_us = sum(a.elapsed_time(b) for a, b in ev) / steps * 1e3
         return StepTiming(step_us, head_us), ids

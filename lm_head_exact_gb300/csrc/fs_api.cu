@@ -423,6 +423,7 @@ fs_status sample_chunk(const void* h, const void* W_chunk, int64_t B, int64_t d,
   // previous chunk's kernel is still running (programmatic dependent launch);
   // they wait for it only before merging into the shared carry.
   p.pdl = (flags & (FS_CHUNK_FIRST | FS_CHUNK_SERIAL)) == 0;
+  p.chunk = true;
   FS_TRY(check_problem(p, last, out_ids, out_max));
   if (B > 0) {
     FS_TRY(check_device_ptr(carry_max, "carry_max"));

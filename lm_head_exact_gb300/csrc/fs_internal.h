@@ -45,6 +45,10 @@ struct Problem {
   // dbg_logits[b * V_local + v] for rows b < B of this launch, from the same
   // accumulator values its epilogue scans.
   float* dbg_logits = nullptr;
+  // A vocabulary chunk of a chunked step (fs_sample_chunked): the CTA-pair
+  // kernel then runs its lean instantiation, two CTAs per SM, which overlaps
+  // consecutive chunks (same arithmetic, so the same results bit for bit).
+  bool chunk = false;
 };
 
 // Launch `kernel` on `stream`, as a programmatic dependent launch when `pdl`.

@@ -264,11 +264,13 @@ tc_batch_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_constan
         tmem_ld_wait();
         const int64_t v0 = col0 + c;                       // local id of r[0]
         if (p.dbg_logits != nullptr && row_ok) {          // parity inspection only
-#pragma unroll 1
-          for (int j = 0; j < 32 && v0 + j < p.V_local; ++j) {
-            float logit = __uint_as_float(r[j]);
-            if (p.bias != nullptr) logit += p.bias[b * p.bias_stride + v0 + j];
-            p.dbg_logits[b * p.V_local + v0 + j] = logit;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {                   // unrolled: r stays in registers
+            if (v0 + j < p.V_local) {
+              float logit = __uint_as_float(r[j]);
+              if (p.bias != nullptr) logit += p.bias[b * p.bias_stride + v0 + j];
+              p.dbg_logits[b * p.V_local + v0 + j] = logit;
+            }
           }
         }
         if constexpr (kStoreLogits) {
@@ -401,6 +403,9 @@ static cudaError_t launch_batch_impl(const Problem& p, const Finish* f, float* l
     if (p.bias != nullptr) ps.bias = p.bias + b0 * p.bias_stride;
     ps.row_offset = p.row_offset + b0;
     if (p.dbg_logits != nullptr) ps.dbg_logits = p.dbg_logits + b0 * p.V_local;
+    // The slices of one call share the ticket counter: a later slice starts
+    // after the previous one has completed (and left the counter at zero).
+    ps.pdl = p.pdl && b0 == 0;
     Finish fs_slice{};
     if (!store) {            // this launch finishes rows [b0, b0 + ps.B)
       fs_slice = *f;

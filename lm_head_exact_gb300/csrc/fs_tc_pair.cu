@@ -49,9 +49,17 @@ using namespace sm100;
 // warps leave 96 registers a thread (the register file is split between the
 // four schedulers), which made the top-k lists spill and the B = 256, k = 8
 // call 2.5% slower, so the top-k variants keep 8.
-template <int kTopK>
+//
+// kLean: the instantiation for vocabulary chunks (fs_sample_chunked), whose
+// few tiles give each pair one or two: 3 stages, ONE 256-column accumulator
+// and 8 epilogue warps, so that two CTAs fit on an SM (shared memory, TMEM
+// and registers) and the next chunk's pairs stream and multiply while this
+// chunk's run their epilogues.  Its MMAs (shapes, K order) and its scan are
+// those of the full instantiation, so every logit and every sample is the
+// same bit for bit; only the overlap differs.
+template <int kTopK, bool kLean = false>
 struct PairWarps {
-  static constexpr int kEpi = kTopK > 0 ? 8 : 16;
+  static constexpr int kEpi = (kTopK > 0 || kLean) ? 8 : 16;
   static constexpr int kParts = kEpi / 4;
   static constexpr int kProducer = kEpi;
   static constexpr int kMma = kEpi + 1;
@@ -61,24 +69,32 @@ constexpr int kMaxColParts = 4;
 constexpr int kRowsPerCta = 128;    // batch rows of one CTA (half of the MMA M = 256)
 constexpr int kBN = 256;            // vocabulary rows per tile (MMA N); each CTA loads 128
 constexpr int kBK = 64;
-constexpr int kStages = 7;
 constexpr int kATileBytes = kRowsPerCta * kBK * 2;     // 16 KB: this CTA's h rows
 constexpr int kBTileBytes = (kBN / 2) * kBK * 2;       // 16 KB: this CTA's half of the W tile
-constexpr int kTmemCols = 512;
-constexpr int kOffA = 0;
-constexpr int kOffB = kOffA + kStages * kATileBytes;
-constexpr int kOffBars = kOffB + kStages * kBTileBytes;
-constexpr int kNumBars = 2 * kStages + 5;
-constexpr int kOffMisc = kOffBars + kNumBars * 8;
-// The epilogue's merge buffers are used only after the CTA's last tile has
-// been waited for, when every MMA has completed and every TMA load has
-// landed, so they alias the first stages; that leaves room for a seventh
-// stage (230.6 KB of the 232 KB a CTA may use).
-constexpr int kOffHalf = kOffA;                                              // Best[parts - 1][128]
-constexpr int kOffTopK = kOffHalf + (kMaxColParts - 1) * kRowsPerCta * 8;   // top-k mode: Partial[128][K]
-constexpr int kSmemBytes = kOffMisc + 16 + 1024;
-static_assert(kOffTopK + kRowsPerCta * 16 * 8 <= kOffBars, "merge buffers must fit in the stage memory");
-static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+
+template <bool kLean>
+struct PairCfg {
+  static constexpr int kStages = kLean ? 3 : 7;
+  static constexpr int kAccs = kLean ? 1 : 2;          // 256-column TMEM accumulators
+  static constexpr int kTmemCols = kAccs * kBN;
+  static constexpr int kCtasPerSm = kLean ? 2 : 1;
+  static constexpr int kOffA = 0;
+  static constexpr int kOffB = kOffA + kStages * kATileBytes;
+  static constexpr int kOffBars = kOffB + kStages * kBTileBytes;
+  static constexpr int kNumBars = 2 * kStages + 5;
+  static constexpr int kOffMisc = kOffBars + kNumBars * 8;
+  // The epilogue's merge buffers are used only after the CTA's last tile has
+  // been waited for, when every MMA has completed and every TMA load has
+  // landed, so they alias the first stages; that leaves room for a seventh
+  // stage in the full instantiation (230.6 KB of the 232 KB a CTA may use).
+  static constexpr int kOffHalf = kOffA;                                              // Best[parts - 1][128]
+  static constexpr int kOffTopK = kOffHalf + (kMaxColParts - 1) * kRowsPerCta * 8;   // top-k mode: Partial[128][K]
+  static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
+  static_assert(kOffHalf + (kMaxColParts - 1) * kRowsPerCta * 8 <= kOffBars, "merge buffers fit in the stages");
+  static_assert(kLean || kOffTopK + kRowsPerCta * 16 * 8 <= kOffBars, "top-k buffers fit in the stages");
+  static_assert(kSmemBytes * kCtasPerSm <= 232448, "shared memory per SM");
+};
+constexpr int kSmemBytes = PairCfg<false>::kSmemBytes;
 constexpr int smem_bytes(int) { return kSmemBytes; }
 constexpr uint16_t kPairMask = 0x3;
 
@@ -92,21 +108,33 @@ struct PairArgs {
   int* err;
 };
 
-template <int kTopK = 0>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairWarps<kTopK>::kThreads, 1)
+template <int kTopK = 0, bool kLean = false>
+__global__ void __cluster_dims__(2, 1, 1)
+__launch_bounds__(PairWarps<kTopK, kLean>::kThreads, PairCfg<kLean>::kCtasPerSm)
 tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_constant__ CUtensorMap tmap_w,
                const PairArgs args) {
-  constexpr int kEpiWarps = PairWarps<kTopK>::kEpi;
-  constexpr int kColParts = PairWarps<kTopK>::kParts;
-  constexpr int kProducerWarp = PairWarps<kTopK>::kProducer;
-  constexpr int kMmaWarp = PairWarps<kTopK>::kMma;
+  static_assert(!(kLean && kTopK > 0), "the lean instantiation samples only");
+  using Cfg = PairCfg<kLean>;
+  constexpr int kStages = Cfg::kStages;
+  constexpr int kAccs = Cfg::kAccs;
+  constexpr int kTmemCols = Cfg::kTmemCols;
+  constexpr int kOffA = Cfg::kOffA;
+  constexpr int kOffB = Cfg::kOffB;
+  constexpr int kOffBars = Cfg::kOffBars;
+  constexpr int kOffMisc = Cfg::kOffMisc;
+  constexpr int kOffHalf = Cfg::kOffHalf;
+  constexpr int kOffTopK = Cfg::kOffTopK;
+  constexpr int kEpiWarps = PairWarps<kTopK, kLean>::kEpi;
+  constexpr int kColParts = PairWarps<kTopK, kLean>::kParts;
+  constexpr int kProducerWarp = PairWarps<kTopK, kLean>::kProducer;
+  constexpr int kMmaWarp = PairWarps<kTopK, kLean>::kMma;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + kOffBars);   // used in the even CTA
   uint64_t* empty_bar = full_bar + kStages;                            // both CTAs
   uint64_t* tfull_bar = empty_bar + kStages;                           // both CTAs
   uint64_t* tempty_bar = tfull_bar + 2;                                // used in the even CTA
-  uint64_t* drain_bar = tempty_bar + 2;
+  uint64_t* drain_bar = tempty_bar + 2;                                // (2 + 2 slots; kAccs used)
   uint32_t* tmem_base_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
   int* last_flag = reinterpret_cast<int*>(smem + kOffMisc + 8);
@@ -143,7 +171,7 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_constant
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], 1);
     }
-    for (int a = 0; a < 2; ++a) {
+    for (int a = 0; a < kAccs; ++a) {
       mbar_init(&tfull_bar[a], 1);
       mbar_init(&tempty_bar[a], 2 * kEpiWarps);        // one arrival per epilogue warp of both CTAs
     }
@@ -216,8 +244,8 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_constant
       uint32_t phase = 0;
       bool ok = true;
       for (int t = 0; t < n_tiles && ok; ++t) {
-        const int acc = t & 1;
-        const uint32_t acc_phase = (t >> 1) & 1;
+        const int acc = t % kAccs;
+        const uint32_t acc_phase = (t / kAccs) & 1;
         if (!mbar_wait(&tempty_bar[acc], acc_phase ^ 1, args.err, abort_flag)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * kBN;
@@ -268,8 +296,8 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_constant
     TopList<(kTopK > 0 ? kTopK : 1)> list;
     topk_init(list);
     for (int t = 0; t < n_tiles; ++t) {
-      const int acc = t & 1;
-      const uint32_t acc_phase = (t >> 1) & 1;
+      const int acc = t % kAccs;
+      const uint32_t acc_phase = (t / kAccs) & 1;
       if (!mbar_wait(&tfull_bar[acc], acc_phase, args.err, abort_flag)) break;
       tc_fence_after();
       const int vt = q + t * args.n_groups;
@@ -281,11 +309,13 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_constant
         tmem_ld_wait();
         const int64_t v0 = col0 + c;
         if (p.dbg_logits != nullptr && row_ok) {          // parity inspection only
-#pragma unroll 1
-          for (int j = 0; j < 32 && v0 + j < p.V_local; ++j) {
-            float logit = __uint_as_float(r[j]);
-            if (p.bias != nullptr) logit += p.bias[b * p.bias_stride + v0 + j];
-            p.dbg_logits[b * p.V_local + v0 + j] = logit;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {                   // unrolled: r stays in registers
+            if (v0 + j < p.V_local) {
+              float logit = __uint_as_float(r[j]);
+              if (p.bias != nullptr) logit += p.bias[b * p.bias_stride + v0 + j];
+              p.dbg_logits[b * p.V_local + v0 + j] = logit;
+            }
           }
         }
         if (active && v0 < p.V_local) {
@@ -357,27 +387,32 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_constant
 }  // namespace
 
 // CTA pairs that can be resident at once: a pair needs two SMs of one GPC,
-// so with GPCs of odd SM counts this can be below SMs / 2.  A persistent grid
-// larger than that would run its last pairs as a second wave.
+// so with GPCs of odd SM counts this can be below SMs / 2 (per SM slot: the
+// lean instantiation fits two CTAs on an SM).  A persistent grid larger than
+// that would run its last pairs as a second wave.
+template <bool kLean>
 static int resident_pairs(int dev, int sms) {
   static std::atomic<int> cached[64];         // zero-initialized (static storage)
   if (dev >= 0 && dev < 64) {
     const int c = cached[dev].load(std::memory_order_relaxed);
     if (c > 0) return c;
   }
+  constexpr int per_sm = PairCfg<kLean>::kCtasPerSm;
   int n = 0;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(2 * (sms / 2)));
-  cfg.blockDim = dim3(PairWarps<0>::kThreads);
-  cfg.dynamicSmemBytes = kSmemBytes;
-  if (cudaOccupancyMaxActiveClusters(&n, tc_pair_kernel<0>, &cfg) != cudaSuccess || n <= 0) {
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * per_sm * (sms / 2)));
+  cfg.blockDim = dim3(PairWarps<0, kLean>::kThreads);
+  cfg.dynamicSmemBytes = PairCfg<kLean>::kSmemBytes;
+  if (cudaOccupancyMaxActiveClusters(&n, tc_pair_kernel<0, kLean>, &cfg) != cudaSuccess || n <= 0) {
     cudaGetLastError();
-    n = sms / 2;
+    n = per_sm * (sms / 2);
   }
-  n = std::min(n, sms / 2);
+  n = std::min(n, per_sm * (sms / 2));
   if (dev >= 0 && dev < 64) cached[dev].store(n, std::memory_order_relaxed);
   return n;
 }
+
+static int resident_pairs(int dev, int sms) { return resident_pairs<false>(dev, sms); }
 
 // Geometry of one launch over a batch slice of B rows: npt pair tiles, then
 // at most pairs / npt groups, as few as give every group the same number of
@@ -403,13 +438,15 @@ static int device_sms(int* dev) {
   return sms > 0 ? sms : 148;
 }
 
-cudaError_t launch_tc_pair(const Problem& p, const Finish& f, int* err, cudaStream_t stream) {
-  if (p.d < kBK || p.V_local <= 0) return cudaErrorNotSupported;
+template <bool kLean>
+static cudaError_t launch_pair_sampler(const Problem& p, const Finish& f, int* err, cudaStream_t stream) {
+  using Cfg = PairCfg<kLean>;
   int dev = 0;
   const int sms = device_sms(&dev);
-  cudaError_t e = cudaFuncSetAttribute(tc_pair_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  cudaError_t e = cudaFuncSetAttribute(tc_pair_kernel<0, kLean>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       Cfg::kSmemBytes);
   if (e != cudaSuccess) return e;
-  const int pairs = resident_pairs(dev, sms);
+  const int pairs = resident_pairs<kLean>(dev, sms);
   CUtensorMap tw;
   if (!encode_kmajor_bf16(&tw, p.W, p.V_local, p.d, kBK, kBN / 2)) return cudaErrorInvalidValue;
   const int64_t slice = static_cast<int64_t>(pairs) * 2 * kRowsPerCta;
@@ -421,6 +458,9 @@ cudaError_t launch_tc_pair(const Problem& p, const Finish& f, int* err, cudaStre
     if (p.bias != nullptr) ps.bias = p.bias + b0 * p.bias_stride;
     ps.row_offset = p.row_offset + b0;
     if (p.dbg_logits != nullptr) ps.dbg_logits = p.dbg_logits + b0 * p.V_local;
+    // The slices of one call share the ticket counter: a later slice starts
+    // after the previous one has completed (and left the counter at zero).
+    ps.pdl = p.pdl && b0 == 0;
     Finish fs_slice = f;
     fs_slice.keys = f.keys + b0;
     if (f.carry_max != nullptr) {
@@ -436,12 +476,16 @@ cudaError_t launch_tc_pair(const Problem& p, const Finish& f, int* err, cudaStre
     CUtensorMap th;
     if (!encode_kmajor_bf16(&th, ps.h, ps.B, p.d, kBK, kRowsPerCta)) return cudaErrorInvalidValue;
     PairArgs a{ps, fs_slice, g.npt, g.n_groups, n_vt, err};
-    e = launch_kernel(tc_pair_kernel<0>, dim3(2 * g.npt * g.n_groups), dim3(PairWarps<0>::kThreads), kSmemBytes,
-                      stream, ps.pdl,
-                      th, tw, a);
+    e = launch_kernel(tc_pair_kernel<0, kLean>, dim3(2 * g.npt * g.n_groups), dim3(PairWarps<0, kLean>::kThreads),
+                      Cfg::kSmemBytes, stream, ps.pdl, th, tw, a);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
+}
+
+cudaError_t launch_tc_pair(const Problem& p, const Finish& f, int* err, cudaStream_t stream) {
+  if (p.d < kBK || p.V_local <= 0) return cudaErrorNotSupported;
+  return p.chunk ? launch_pair_sampler<true>(p, f, err, stream) : launch_pair_sampler<false>(p, f, err, stream);
 }
 
 int64_t tc_pair_topk_max_rows(int device) {

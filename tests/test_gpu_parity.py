@@ -398,6 +398,35 @@ def test_batch_larger_than_one_launch(fs, torch_cuda, forced):
     compare(ids, mx, sampler.sample(h, W, temp, 8, 2), what=f"B=20000 {forced}")
 
 
+@pytest.mark.parametrize("forced", ["tc_batch", "tc_pair"])
+def test_chunked_batch_larger_than_one_launch(fs, torch_cuda, forced):
+    """A chunked step whose batch needs several launches per chunk (the
+    batch-major kernel covers SMs x 128 rows per launch, the lean CTA-pair
+    instantiation of chunks two pairs per SM pair x 256): the launches of one
+    chunk share its ticket, consecutive chunks overlap, and the result must
+    still equal the one-shot sample bit for bit and match the oracle."""
+    torch = torch_cuda
+    B, V, d = 40000, 1000, 64
+    h, W, temp = _problem(B, V, d, seed=93)
+    code = {"tc_batch": fs.FS_PATH_TC_BATCH, "tc_pair": fs.FS_PATH_TC_PAIR}[forced]
+    fs.set_path(code)
+    try:
+        hd, Wd, td = to_device(h, torch), to_device(W, torch), to_device(temp, torch)
+        ids1, mx1 = fs.sample(hd, Wd, td, 8, 3)
+        cm = torch.empty(B, device="cuda")
+        ci = torch.empty(B, dtype=torch.int64, device="cuda")
+        bounds = [0, 333, 700, V]
+        for i, (lo, hi) in enumerate(zip(bounds[:-1], bounds[1:])):
+            res = fs.sample_chunked(hd, Wd[lo:hi], lo, td, 8, 3, cm, ci, i == 0, i == len(bounds) - 2)
+        torch.cuda.synchronize()
+    finally:
+        fs.set_path(fs.FS_PATH_AUTO)
+    np.testing.assert_array_equal(res[0].cpu().numpy(), ids1.cpu().numpy())
+    np.testing.assert_array_equal(res[1].cpu().numpy(), mx1.cpu().numpy())
+    compare(res[0].cpu().numpy(), res[1].cpu().numpy(), sampler.sample(h, W, temp, 8, 3),
+            what=f"chunked B={B} {forced}")
+
+
 def test_epilogue_warp_splits_agree(fs, torch_cuda):
     """The batch-major kernel scans a tile with 16 epilogue warps when one
     batch tile covers the batch (B <= 128) and with 8 above; the CTA-pair

@@ -6,7 +6,8 @@ CUDA runtime linked statically, so the library loads without a GPU (the
 symbol check runs on CPU-only machines).  Rebuilds only when a source or
 header is newer than the library.
 
-Usage: ``python -m lm_head_exact_gb300.build [--force] [--debug]``.
+Usage: ``python -m lm_head_exact_gb300.build [--force] [-v]`` (``-v`` prints
+ptxas' register and shared-memory report of every kernel).
 """
 
 import glob
@@ -52,13 +53,13 @@ def up_to_date():
     return all(os.path.getmtime(p) <= t for p in _deps())
 
 
-def build(force=False, debug=False, verbose=False):
+def build(force=False, verbose=False):
     """Compile and link the library; return its path."""
-    if not force and not debug and up_to_date():
+    if not force and up_to_date():
         return LIB
     os.makedirs(BUILD, exist_ok=True)
     cc = nvcc()
-    flags = list(NVCC_FLAGS) + (["-DFS_DEBUG=1"] if debug else [])
+    flags = list(NVCC_FLAGS)
 
     def compile_one(src):
         obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
@@ -87,5 +88,4 @@ def build(force=False, debug=False, verbose=False):
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, debug="--debug" in sys.argv,
-                verbose="-v" in sys.argv or "--verbose" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv or "--verbose" in sys.argv))

@@ -122,3 +122,37 @@ def test_signed_zero_scores_tie_to_the_smaller_id(fs, torch_cuda, path):
     np.testing.assert_array_equal(ids[:7], ref.ids[:7])
     assert np.all(mx.cpu().numpy()[:7] == 0.0)
     compare(ids, mx.cpu().numpy(), ref, what=f"signed zero {path}")
+
+
+@pytest.mark.parametrize("B,V,d", [(64, 4097, 4096), (128, 8192, 4096), (200, 3000, 1024), (32, 1000, 8192),
+                                   (256, 16032, 4096)])
+def test_tensor_core_families_form_identical_logits(fs, torch_cuda, B, V, d):
+    """The three tensor-core kernel families -- vocabulary-major (W as the
+    MMA's A operand, M = 128 vocabulary rows), batch-major (h as A, one CTA)
+    and the CTA pair (cta_group::2, M = 256) -- run the same K order of
+    bf16 x bf16 -> fp32 MMAs, and their logits agree BIT FOR BIT: the
+    MMA's rounding does not depend on the tile shape, the operand roles or
+    the CTA pairing.  So which tensor-core family samples a batch cannot
+    change a sample (the scan over the logits is the same arithmetic in every
+    family), the property that lets chunked and one-shot calls agree exactly."""
+    torch = torch_cuda
+    rng = np.random.default_rng(B + V + d)
+    h = synthetic.bf16_bits(rng.standard_normal((B, d)).astype(np.float32))
+    W = synthetic.bf16_bits((rng.standard_normal((V, d)) * 0.02).astype(np.float32))
+    temp = np.ones(B, np.float32)
+    hd, Wd, td = to_device(h, torch), to_device(W, torch), to_device(temp, torch)
+    bits = {}
+    try:
+        for name, code in [("tc_vocab", fs.FS_PATH_TC_VOCAB), ("tc_batch", fs.FS_PATH_TC_BATCH),
+                           ("tc_pair", fs.FS_PATH_TC_PAIR)]:
+            fs.set_path(code)
+            ids, mx, lg = fs.debug_fused_logits(hd, Wd, td, 21, 4)
+            torch.cuda.synchronize()
+            bits[name] = (lg.cpu().numpy().view(np.uint32).copy(), ids.cpu().numpy(), mx.cpu().numpy())
+    finally:
+        fs.set_path(fs.FS_PATH_AUTO)
+    ref = bits["tc_pair"]
+    for name, (lb, ids, mx) in bits.items():
+        assert np.array_equal(lb, ref[0]), f"{name}: {(lb != ref[0]).sum()} logits differ from tc_pair's"
+        np.testing.assert_array_equal(ids, ref[1])
+        np.testing.assert_array_equal(mx, ref[2])

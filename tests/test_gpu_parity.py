@@ -511,6 +511,38 @@ def test_sample_host_pinned_and_pageable_agree(fs, torch_cuda):
         np.testing.assert_array_equal(mx_q, mx_d)
 
 
+def test_gumbel_transform_on_the_whole_uniform_grid(fs, tmp_path):
+    """The device noise transform is checked on EVERY value it can see: the
+    sampler's u is one of the 2^23 grid points (m + 1/2) 2^-23, and the
+    library's own gumbel_from_word, compiled into a small helper from the
+    library's device header, is compared with the fp64 -log(-log u) of the
+    oracle at all of them.  The largest error bounds the noise error of every
+    score the kernels form (the parity tolerance assumes < 1e-5)."""
+    import shutil
+    import subprocess
+    nvcc = shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
+    here = os.path.dirname(__file__)
+    src = os.path.join(here, "gpu_helpers", "gumbel_grid.cu")
+    inc = os.path.join(os.path.dirname(here), "lm_head_exact_gb300", "csrc")
+    exe = str(tmp_path / "gumbel_grid")
+    r = subprocess.run([nvcc, "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-std=c++17", "-I", inc,
+                        "-o", exe, src], capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    out = str(tmp_path / "grid.f32")
+    run = subprocess.run([exe, out], capture_output=True, text=True, timeout=120)
+    assert run.returncode == 0, run.stderr
+    g = np.fromfile(out, dtype=np.float32)
+    assert g.size == 1 << 23
+    words = np.arange(1 << 23, dtype=np.uint32) << np.uint32(9)
+    ref = sampler.gumbel_from_uniform(sampler.uniform_from_word(words))
+    err = np.abs(g.astype(np.float64) - ref)
+    worst = int(np.argmax(err))
+    print(f"device Gumbel over the whole u grid: max |error| {err.max():.3g} at u = {(worst + 0.5) * 2.0 ** -23!r}")
+    assert np.isfinite(g).all()
+    assert err.max() < 1e-5, (err.max(), worst)
+    assert g[0] == g.min() and g[-1] == g.max()          # monotone ends: the support's extremes
+
+
 def test_noise_words_match_curand_philox(fs, torch_cuda, tmp_path):
     """The library's noise words equal cuRAND's device-API Philox-4x32-10
     (curandStatePhilox4_32_10_t, curand4) run as a library, with the

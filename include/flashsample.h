@@ -274,10 +274,13 @@ FS_API fs_status fs_sample_host(const void* h_host, const void* W, int64_t B, in
  * sampled distribution as fs_sample, but it always runs the vocabulary-major
  * tensor-core kernel, whatever B and fs_set_path say (fs_sample picks the
  * kernel family from B: the CUDA-core kernel at B = 1, the batch-major or
- * CTA-pair kernels above B = 64).  Its results therefore equal fs_sample's
- * bit for bit for 2 <= B <= 64 under FS_PATH_AUTO, and otherwise agree with
- * them within the parity tolerance (ids may differ only on rows whose two
- * best perturbed scores are within rounding of each other).  The
+ * CTA-pair kernels above B = 64).  The three tensor-core families form the
+ * same fp32 logits bit for bit, so its results equal fs_sample's bit for bit
+ * whenever fs_sample runs a tensor-core family (every 2 <= B <= 256 under
+ * FS_PATH_AUTO); at B = 1, or with FS_PATH_SIMT forced, fs_sample runs the
+ * CUDA-core kernel and the two agree within the parity tolerance (ids may
+ * differ only on rows whose two best perturbed scores are within rounding of
+ * each other).  The
  * cross-tile finish area (ticket counter + one candidate key per row) lives
  * in a fixed static device array inside the library (2.3 KB per GPU, held
  * until the process exits) instead of a workspace the library cudaMalloc's
@@ -318,7 +321,10 @@ FS_API fs_status fs_workspace_reserve(int64_t B, int64_t V, void* stream);
 FS_API fs_status fs_workspace_release(void);
 
 /* Force a kernel family for later calls (FS_PATH_*); FS_PATH_AUTO restores
- * the batch-size rule.  Process-wide. */
+ * the batch-size rule.  Process-wide.  The tensor-core families
+ * (FS_PATH_TC_VOCAB, FS_PATH_TC_BATCH, FS_PATH_TC_PAIR) form identical
+ * logits and samples; only the CUDA-core family (FS_PATH_SIMT, fp32 FFMA
+ * accumulation) differs from them, within the parity tolerance. */
 FS_API fs_status fs_set_path(int path);
 
 /*

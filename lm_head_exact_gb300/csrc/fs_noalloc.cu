@@ -1,9 +1,11 @@
 // fs_sample_noalloc: the tensor-core sampling path with its scratch memory in
 // a fixed, statically allocated device array instead of the library's
 // cudaMalloc'ed workspace.  It always runs the vocabulary-major tensor-core
-// kernel, whatever the batch size (fs_sample picks the family from B), so
-// its results agree with fs_sample's within the parity tolerance, and bit
-// for bit where fs_sample runs that kernel too (2 <= B <= 64).
+// kernel, whatever the batch size (fs_sample picks the family from B).  The
+// tensor-core families form the same logits bit for bit, so its results
+// equal fs_sample's wherever fs_sample runs a tensor-core kernel (every
+// 2 <= B <= 256 under the automatic rule) and agree with them within the
+// parity tolerance at B = 1, where fs_sample runs the CUDA-core kernel.
 //
 // Why it exists: fs_sample finishes the sample through a small workspace (a
 // ticket counter and one packed candidate key per batch row) that the

@@ -381,6 +381,41 @@ def test_many_small_chunks_overlapping_launches(fs, torch_cuda, path):
         np.testing.assert_array_equal(res[1].cpu().numpy(), ref_mx.cpu().numpy())
 
 
+def test_chunked_step_interleaved_with_one_shot_calls(fs, torch_cuda, path):
+    """One-shot calls of another batch size, and a Gumbel-top-k call, enqueued
+    on the same stream between the chunk calls of a step: they finish through
+    the stream's first key set while earlier chunks may still be running
+    (programmatic launches), and the chunked step must still equal its
+    one-shot sample bit for bit, and the interleaved calls their own."""
+    torch = torch_cuda
+    B, V, d, n = 24, 20011, 128, 6
+    h, W, temp = _problem(B, V, d, seed=91)
+    h2, _, temp2 = _problem(7, V, d, seed=92)
+    hd, Wd, td = to_device(h, torch), to_device(W, torch), to_device(temp, torch)
+    h2d, t2d = to_device(h2, torch), to_device(temp2, torch)
+    bounds = synthetic.chunk_bounds(V, n)
+    cm = torch.empty(B, device="cuda")
+    ci = torch.empty(B, dtype=torch.int64, device="cuda")
+    ref_ids, ref_mx = fs.sample(hd, Wd, td, 5, 2)
+    ref2_ids, ref2_mx = fs.sample(h2d, Wd, t2d, 6, 9)
+    ref_k = fs.sample_topk(h2d, Wd, t2d, 6, 9, 4)
+    torch.cuda.synchronize()
+    between = []
+    for i, (lo, hi) in enumerate(zip(bounds[:-1], bounds[1:])):
+        res = fs.sample_chunked(hd, Wd[lo:hi], lo, td, 5, 2, cm, ci, i == 0, i == n - 1)
+        if i == 1:
+            between.append(fs.sample(h2d, Wd, t2d, 6, 9))
+        if i == 3:
+            between.append(fs.sample_topk(h2d, Wd, t2d, 6, 9, 4))
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(res[0].cpu().numpy(), ref_ids.cpu().numpy())
+    np.testing.assert_array_equal(res[1].cpu().numpy(), ref_mx.cpu().numpy())
+    np.testing.assert_array_equal(between[0][0].cpu().numpy(), ref2_ids.cpu().numpy())
+    np.testing.assert_array_equal(between[0][1].cpu().numpy(), ref2_mx.cpu().numpy())
+    np.testing.assert_array_equal(between[1][0].cpu().numpy(), ref_k[0].cpu().numpy())
+    np.testing.assert_array_equal(between[1][1].cpu().numpy(), ref_k[1].cpu().numpy())
+
+
 @pytest.mark.parametrize("forced", ["tc_batch", "tc_pair", "auto"])
 def test_batch_larger_than_one_launch(fs, torch_cuda, forced):
     """B = 20000 exceeds what one batch-major launch covers (SMs x 128 rows),

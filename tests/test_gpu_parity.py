@@ -416,6 +416,36 @@ def test_chunked_step_interleaved_with_one_shot_calls(fs, torch_cuda, path):
     np.testing.assert_array_equal(between[1][1].cpu().numpy(), ref_k[1].cpu().numpy())
 
 
+def test_chunked_steps_on_two_streams_at_once(fs, torch_cuda, path):
+    """Two chunked steps enqueued alternately on two unordered streams: each
+    stream finishes through its own workspace (key sets, tickets), so the
+    kernels of the two steps may overlap freely and both results stay equal
+    to their one-shot samples bit for bit."""
+    torch = torch_cuda
+    V, d, n = 16411, 128, 5
+    ha, W, ta = _problem(33, V, d, seed=101)
+    hb, _, tb = _problem(200, V, d, seed=102)
+    Wd = to_device(W, torch)
+    args = [(to_device(ha, torch), to_device(ta, torch), 7), (to_device(hb, torch), to_device(tb, torch), 8)]
+    refs = [fs.sample(h_, Wd, t_, 4, s_) for h_, t_, s_ in args]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    carries = [(torch.empty(h_.shape[0], device="cuda"), torch.empty(h_.shape[0], dtype=torch.int64, device="cuda"))
+               for h_, _, _ in args]
+    for st, (h_, _, _) in zip(streams, args):
+        fs.workspace_reserve(h_.shape[0], V, stream=st)
+    torch.cuda.synchronize()
+    bounds = synthetic.chunk_bounds(V, n)
+    outs = [None, None]
+    for i, (lo, hi) in enumerate(zip(bounds[:-1], bounds[1:])):
+        for k, ((h_, t_, s_), st, (cm, ci)) in enumerate(zip(args, streams, carries)):
+            with torch.cuda.stream(st):
+                outs[k] = fs.sample_chunked(h_, Wd[lo:hi], lo, t_, 4, s_, cm, ci, i == 0, i == n - 1, stream=st)
+    torch.cuda.synchronize()
+    for (ids, mx), (rid, rmx) in zip(outs, refs):
+        np.testing.assert_array_equal(ids.cpu().numpy(), rid.cpu().numpy())
+        np.testing.assert_array_equal(mx.cpu().numpy(), rmx.cpu().numpy())
+
+
 @pytest.mark.parametrize("forced", ["tc_batch", "tc_pair", "auto"])
 def test_batch_larger_than_one_launch(fs, torch_cuda, forced):
     """B = 20000 exceeds what one batch-major launch covers (SMs x 128 rows),

@@ -815,16 +815,18 @@ fs_status fs_sample_unfused(const void* h, const void* W, int64_t B, int64_t d, 
   {
     std::lock_guard<std::mutex> lock(g_ws_mutex);
     Workspace& ws = g_workspaces[{dev, stream}];
-    FS_TRY(grow(&ws.unfused, &ws.unfused_bytes, logits_out ? plane : 2 * plane, stream));
+    FS_TRY(grow(&ws.unfused, &ws.unfused_bytes, (logits_out ? plane : 2 * plane) + unfused_partial_bytes(B),
+                stream));
     buf = static_cast<char*>(ws.unfused);
   }
   float* logits = logits_out ? logits_out : reinterpret_cast<float*>(buf);
   float* probs = reinterpret_cast<float*>(logits_out ? buf : buf + plane);
+  void* partials = logits_out ? buf + plane : buf + 2 * plane;
   int* err = nullptr;
   FS_TRY(error_word(&err, stream));
   cudaError_t e = launch_tc_logits(p, logits, err, stream);
   if (e != cudaSuccess) return cuda_fail(e, "logits GEMM launch");
-  e = launch_unfused_tail(p, logits, probs, out_ids, out_max, stream);
+  e = launch_unfused_tail(p, logits, probs, partials, out_ids, out_max, stream);
   if (e != cudaSuccess) return cuda_fail(e, "softmax / sample launch");
   return FS_OK;
 }

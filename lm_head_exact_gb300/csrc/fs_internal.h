@@ -120,7 +120,10 @@ cudaError_t launch_tc_pair(const Problem& p, const Finish& f, int* err, cudaStre
 // Unfused comparison pipeline: tensor-core GEMM storing fp32 logits [B, V]
 // (+ bias) to HBM, then row softmax into probs [B, V], then the sample.
 cudaError_t launch_tc_logits(const Problem& p, float* logits, int* err, cudaStream_t stream);
-cudaError_t launch_unfused_tail(const Problem& p, float* logits, float* probs, int64_t* out_ids,
+// `partials`: unfused_partial_bytes(B) bytes of scratch for the per-range
+// softmax sums and candidates (each row is split over several blocks).
+size_t unfused_partial_bytes(int64_t B);
+cudaError_t launch_unfused_tail(const Problem& p, float* logits, float* probs, void* partials, int64_t* out_ids,
                                 float* out_max, cudaStream_t stream);
 
 // Failure-path check of the bounded waits: one wait that runs out after

@@ -122,6 +122,54 @@ def test_degenerate_rows(fs, torch_cuda, path):
     assert 10 not in ids
 
 
+def test_masked_vocabulary(fs, torch_cuda, path):
+    """Constrained decoding through the bias: -inf outside an allowed set
+    (a few ids, or one), NaN entries (never chosen), and +inf at two ids (the
+    smaller wins the tie at +inf, in every kernel family and across CTAs),
+    one-shot and chunked, against the oracle."""
+    torch = torch_cuda
+    B, V, d = 8, 5003, 64
+    h, W, temp = _problem(B, V, d, seed=33)
+    temp[:] = 1.0
+    temp[3] = 0.0                                      # a greedy row under a mask
+    rng = np.random.default_rng(34)
+    bias = np.full((B, V), -np.inf, np.float32)
+    allowed = {}
+    for b in (0, 3, 4):
+        allowed[b] = np.sort(rng.choice(V, size=7, replace=False))
+        bias[b, allowed[b]] = 0.0
+    allowed[1] = np.array([4321])
+    bias[1, 4321] = 0.0                                # a single allowed id
+    bias[2, :] = 0.0
+    bias[2, [4000, 77]] = np.inf                       # +inf twice: the smaller id wins
+    bias[5, :] = 0.0
+    nan_ids = rng.choice(V, size=500, replace=False)
+    bias[5, nan_ids] = np.nan                          # NaN scores never win
+    bias[6, :] = 0.0
+    bias[7, :] = -np.inf                               # nothing allowed: no sample
+    ids, mx = _run(fs, torch, h, W, temp, 9, 2, bias=bias)
+    ref = sampler.sample(h, W, temp, 9, 2, bias=bias)
+    finite = [0, 1, 3, 4, 5, 6, 7]
+    compare(ids[finite], mx[finite], sampler.Sample(ref.ids[finite], ref.zmax[finite], ref.gap[finite]),
+            what=f"masked {path}")
+    for b, ok in allowed.items():
+        assert ids[b] in ok, (b, ids[b])
+    assert ids[1] == 4321
+    assert ids[2] == 77 and ref.ids[2] == 77 and mx[2] == np.inf
+    assert ids[5] not in set(nan_ids.tolist())
+    assert ids[7] == -1 and mx[7] == -np.inf
+    # the same masks through the chunked variant (chunk bounds cut the allowed sets)
+    hd, Wd, td, bd = to_device(h, torch), to_device(W, torch), to_device(temp, torch), to_device(bias, torch)
+    bounds = synthetic.chunk_bounds(V, 5)
+    cm = torch.empty(B, device="cuda")
+    ci = torch.empty(B, dtype=torch.int64, device="cuda")
+    for i, (lo, hi) in enumerate(zip(bounds[:-1], bounds[1:])):
+        res = fs.sample_chunked(hd, Wd[lo:hi], lo, td, 9, 2, cm, ci, i == 0, i == 4, bias_chunk=bd[:, lo:hi])
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(res[0].cpu().numpy(), ids)
+    np.testing.assert_array_equal(res[1].cpu().numpy(), mx)
+
+
 def test_empty_batch_and_empty_vocab(fs, torch_cuda, path):
     torch = torch_cuda
     h = torch.zeros((0, 64), dtype=torch.bfloat16, device="cuda")

@@ -170,6 +170,27 @@ def test_masked_vocabulary(fs, torch_cuda, path):
     np.testing.assert_array_equal(res[1].cpu().numpy(), mx)
 
 
+def test_extreme_temperatures(fs, torch_cuda, path):
+    """Temperatures from 1e-6 (scores ~1e6: the sample is the greedy argmax
+    up to fp32 rounding of the scaled logits) to 1e30 (1/T ~ 1e-30: the
+    noise alone decides), and subnormal-free ends in between, against the
+    oracle."""
+    B, V, d = 9, 4099, 64
+    h, W, _ = _problem(B, V, d, seed=44)
+    temp = np.array([1e-6, 1e-3, 0.05, 1.0, 20.0, 1e3, 1e6, 1e30, 3e-7], np.float32)
+    # the parity tolerances hold on the logits: at 1/T > 1 they scale with 1/T
+    scale = np.maximum(1.0, 1.0 / temp.astype(np.float64))
+    greedy = np.argmax(sampler.logits(h, W), axis=1)
+    for step in (0, 3):
+        ids, mx = _run(fs, torch_cuda, h, W, temp, 17, step)
+        ref = sampler.sample(h, W, temp, 17, step)
+        near = ref.gap < 2e-3 * scale
+        assert np.all((ids == ref.ids) | near), (ids, ref.ids, ref.gap)
+        same = ids == ref.ids
+        assert np.all(np.abs(mx[same] - ref.zmax[same]) <= 2e-3 * scale[same]), (mx, ref.zmax)
+        assert ids[0] == greedy[0] and ids[8] == greedy[8]
+
+
 def test_empty_batch_and_empty_vocab(fs, torch_cuda, path):
     torch = torch_cuda
     h = torch.zeros((0, 64), dtype=torch.bfloat16, device="cuda")

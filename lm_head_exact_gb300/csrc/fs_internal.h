@@ -46,8 +46,10 @@ struct Problem {
   // accumulator values its epilogue scans.
   float* dbg_logits = nullptr;
   // A vocabulary chunk of a chunked step (fs_sample_chunked): the CTA-pair
-  // kernel then runs its lean instantiation, two CTAs per SM, which overlaps
-  // consecutive chunks (same arithmetic, so the same results bit for bit).
+  // kernel then runs its lean instantiation (two CTAs per SM) for chunks of
+  // few tiles, or its full one with at least 4 tiles per pair for larger
+  // chunks; either overlaps consecutive chunks (same arithmetic, so the same
+  // results bit for bit).
   bool chunk = false;
 };
 

@@ -50,8 +50,8 @@ using namespace sm100;
 // four schedulers), which made the top-k lists spill and the B = 256, k = 8
 // call 2.5% slower, so the top-k variants keep 8.
 //
-// kLean: the instantiation for vocabulary chunks (fs_sample_chunked), whose
-// few tiles give each pair one or two: 3 stages, ONE 256-column accumulator
+// kLean: the instantiation for vocabulary chunks with few tiles
+// (fs_sample_chunked; see launch_tc_pair), which give each pair one or two: 3 stages, ONE 256-column accumulator
 // and 8 epilogue warps, so that two CTAs fit on an SM (shared memory, TMEM
 // and registers) and the next chunk's pairs stream and multiply while this
 // chunk's run their epilogues.  Its MMAs (shapes, K order) and its scan are
@@ -421,12 +421,12 @@ struct PairGeometry {
   int npt, n_groups;
 };
 
-static PairGeometry pair_geometry(int64_t B, int pairs, int64_t n_vt) {
+static PairGeometry pair_geometry(int64_t B, int pairs, int64_t n_vt, int min_per = 1) {
   PairGeometry g;
   g.npt = static_cast<int>((B + 2 * kRowsPerCta - 1) / (2 * kRowsPerCta));
   g.n_groups = std::max(1, pairs / g.npt);
   const int64_t tiles = std::max<int64_t>(n_vt, 1);
-  const int64_t per = (tiles + g.n_groups - 1) / g.n_groups;
+  const int64_t per = std::max<int64_t>(min_per, (tiles + g.n_groups - 1) / g.n_groups);
   g.n_groups = static_cast<int>(std::max<int64_t>(1, (tiles + per - 1) / per));
   return g;
 }
@@ -439,7 +439,8 @@ static int device_sms(int* dev) {
 }
 
 template <bool kLean>
-static cudaError_t launch_pair_sampler(const Problem& p, const Finish& f, int* err, cudaStream_t stream) {
+static cudaError_t launch_pair_sampler(const Problem& p, const Finish& f, int* err, cudaStream_t stream,
+                                       int min_tiles_per_pair) {
   using Cfg = PairCfg<kLean>;
   int dev = 0;
   const int sms = device_sms(&dev);
@@ -472,7 +473,7 @@ static cudaError_t launch_pair_sampler(const Problem& p, const Finish& f, int* e
       fs_slice.out_max = f.out_max + b0;
     }
     const int n_vt = static_cast<int>((p.V_local + kBN - 1) / kBN);
-    const PairGeometry g = pair_geometry(ps.B, pairs, n_vt);
+    const PairGeometry g = pair_geometry(ps.B, pairs, n_vt, min_tiles_per_pair);
     CUtensorMap th;
     if (!encode_kmajor_bf16(&th, ps.h, ps.B, p.d, kBK, kRowsPerCta)) return cudaErrorInvalidValue;
     PairArgs a{ps, fs_slice, g.npt, g.n_groups, n_vt, err};
@@ -483,9 +484,22 @@ static cudaError_t launch_pair_sampler(const Problem& p, const Finish& f, int* e
   return cudaSuccess;
 }
 
+// Chunk calls with many tiles (8 chunks of the 8B head at B = 256: 63 tiles)
+// run the full instantiation with at least 4 tiles per pair: a pair's
+// epilogues overlap its next tiles' MMAs and the chunks in flight take
+// disjoint pairs (GB300, 8 chunks at B = 256: 287 -> 271 and 312 -> 297 us in
+// two interleaved runs).  Chunks with fewer tiles (32 chunks: 16) keep the
+// lean instantiation, where 4 tiles per pair measured 7% slower.  Either
+// way the MMAs and the scan are the same, so the samples are too.
+constexpr int64_t kChunkFullMinTiles = 48;
+constexpr int kChunkTilesPerPair = 4;
+
 cudaError_t launch_tc_pair(const Problem& p, const Finish& f, int* err, cudaStream_t stream) {
   if (p.d < kBK || p.V_local <= 0) return cudaErrorNotSupported;
-  return p.chunk ? launch_pair_sampler<true>(p, f, err, stream) : launch_pair_sampler<false>(p, f, err, stream);
+  if (!p.chunk) return launch_pair_sampler<false>(p, f, err, stream, 1);
+  const int64_t n_vt = (p.V_local + kBN - 1) / kBN;
+  if (n_vt >= kChunkFullMinTiles) return launch_pair_sampler<false>(p, f, err, stream, kChunkTilesPerPair);
+  return launch_pair_sampler<true>(p, f, err, stream, 1);
 }
 
 int64_t tc_pair_topk_max_rows(int device) {

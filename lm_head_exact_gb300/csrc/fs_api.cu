@@ -77,6 +77,7 @@ struct Workspace {
   size_t finish_bytes = 0;
   int64_t finish_rows = 0;      // rows per key set
   int64_t chunk_seq = 0;        // sequence number of the last chunk call since FS_CHUNK_FIRST
+  int last_step_chunks = 0;     // chunk calls of the last step completed with FS_CHUNK_LAST
   void* staging = nullptr;      // device staging of fs_sample_host
   size_t staging_bytes = 0;
   void* unfused = nullptr;      // logits + probabilities of fs_sample_unfused
@@ -141,7 +142,11 @@ fs_status current_device(int* dev) {
 // Key set of a chunk call: FS_CHUNK_FIRST starts the sequence at 0, every
 // later chunk call on the stream takes the next number.  *overlap_ok is false
 // when the set wraps around to 0 (the call must then launch without overlap).
-fs_status next_chunk_set(cudaStream_t stream, bool first, int* set, bool* overlap_ok) {
+//
+// *step_chunks receives the chunk count of the previous step on the stream
+// (0 before the first step ends); a call with FS_CHUNK_LAST records its own.
+fs_status next_chunk_set(cudaStream_t stream, bool first, bool last, int* set, bool* overlap_ok,
+                         int* step_chunks) {
   int dev;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
@@ -150,6 +155,8 @@ fs_status next_chunk_set(cudaStream_t stream, bool first, int* set, bool* overla
   ws.chunk_seq = first ? 0 : ws.chunk_seq + 1;
   *set = static_cast<int>(ws.chunk_seq % kKeySets);
   *overlap_ok = first || *set != 0;
+  *step_chunks = ws.last_step_chunks;
+  if (last) ws.last_step_chunks = static_cast<int>(std::min<int64_t>(ws.chunk_seq + 1, 1 << 20));
   return FS_OK;
 }
 
@@ -451,7 +458,9 @@ fs_status sample_chunk(const void* h, const void* W_chunk, int64_t B, int64_t d,
   }
   int set = 0;
   bool overlap_ok = true;
-  if (B > 0) FS_TRY(next_chunk_set(static_cast<cudaStream_t>(stream), (flags & FS_CHUNK_FIRST) != 0, &set, &overlap_ok));
+  if (B > 0)
+    FS_TRY(next_chunk_set(static_cast<cudaStream_t>(stream), (flags & FS_CHUNK_FIRST) != 0, last, &set, &overlap_ok,
+                          &p.step_chunks));
   if (!overlap_ok) p.pdl = false;
   return run(p, f, static_cast<cudaStream_t>(stream), set);
 }

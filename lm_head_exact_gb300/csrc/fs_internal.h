@@ -47,10 +47,14 @@ struct Problem {
   float* dbg_logits = nullptr;
   // A vocabulary chunk of a chunked step (fs_sample_chunked): the CTA-pair
   // kernel then runs its lean instantiation (two CTAs per SM) for chunks of
-  // few tiles, or its full one with at least 4 tiles per pair for larger
-  // chunks; either overlaps consecutive chunks (same arithmetic, so the same
-  // results bit for bit).
+  // few tiles, or its full one with several tiles per pair for larger chunks;
+  // either overlaps consecutive chunks (same arithmetic, so the same results
+  // bit for bit).
   bool chunk = false;
+  // Chunks per step in the previous chunked step on this stream (0: none
+  // yet); sizes the tiles per pair of the full instantiation (see
+  // launch_tc_pair).  Never changes a result.
+  int step_chunks = 0;
 };
 
 // Launch `kernel` on `stream`, as a programmatic dependent launch when `pdl`.

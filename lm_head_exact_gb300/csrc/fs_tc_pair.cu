@@ -484,22 +484,52 @@ static cudaError_t launch_pair_sampler(const Problem& p, const Finish& f, int* e
   return cudaSuccess;
 }
 
-// Chunk calls with many tiles (8 chunks of the 8B head at B = 256: 63 tiles)
-// run the full instantiation with at least 4 tiles per pair: a pair's
-// epilogues overlap its next tiles' MMAs and the chunks in flight take
-// disjoint pairs (GB300, 8 chunks at B = 256: 287 -> 271 and 312 -> 297 us in
-// two interleaved runs).  Chunks with fewer tiles (32 chunks: 16) keep the
-// lean instantiation, where 4 tiles per pair measured 7% slower.  Either
-// way the MMAs and the scan are the same, so the samples are too.
-constexpr int64_t kChunkFullMinTiles = 48;
-constexpr int kChunkTilesPerPair = 4;
+// Chunk calls.  A chunk of few tiles (fewer than 24: 32 chunks of a 128K
+// vocabulary) runs the lean instantiation, two CTAs per SM, so that the next
+// chunks' pairs stream while this chunk's scan.  Larger chunks run the full
+// instantiation with k >= 4 tiles per pair: a pair's epilogues overlap its
+// next tiles' MMAs and the chunks in flight take disjoint pairs.  Their cost
+// follows waves of pairs: the step's chunks need n * ceil(T / k) * npt pairs
+// (n chunks of T tiles, npt pair tiles of batch rows), run in
+// ceil(pairs / resident) waves of k tile-times each, so k is the one in
+// [4, 16] that minimizes waves * k (the smaller on ties), with n taken from
+// the previous chunked step on the stream (k = 4 before there is one).
+// Measured on GB300 (us per step, interleaved runs of one build, B = 256):
+// 8B head, 8 chunks: k = 7 243, 8 244, 4 250, 2 273, 3 284, 5 296, 6 325
+// (the model ranks them 7 < 4 = 8 < 3 < 5 < 6); Qwen3 head, 8 chunks: k = 4
+// 266, 10 299, 7 397, 8 403 (model: 4 < 10 < 7 < 8); lean: 281 and 312.  The
+// MMAs and the scan are the same in both instantiations, so the samples are
+// too.
+constexpr int64_t kChunkLeanMaxTiles = 24;
+constexpr int kChunkMinTilesPerPair = 4;
+constexpr int kChunkMaxTilesPerPair = 16;
+
+static int chunk_tiles_per_pair(int64_t n_vt, int64_t B, int step_chunks, int pairs) {
+  if (step_chunks <= 0) return kChunkMinTilesPerPair;
+  const int64_t npt = (std::min<int64_t>(B, static_cast<int64_t>(pairs) * 2 * kRowsPerCta) + 2 * kRowsPerCta - 1) /
+                      (2 * kRowsPerCta);
+  int best_k = kChunkMinTilesPerPair;
+  int64_t best_cost = -1;
+  for (int k = kChunkMinTilesPerPair; k <= kChunkMaxTilesPerPair; ++k) {
+    const int64_t need = static_cast<int64_t>(step_chunks) * ((n_vt + k - 1) / k) * npt;
+    const int64_t cost = (need + pairs - 1) / pairs * k;
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best_k = k;
+    }
+  }
+  return best_k;
+}
 
 cudaError_t launch_tc_pair(const Problem& p, const Finish& f, int* err, cudaStream_t stream) {
   if (p.d < kBK || p.V_local <= 0) return cudaErrorNotSupported;
   if (!p.chunk) return launch_pair_sampler<false>(p, f, err, stream, 1);
   const int64_t n_vt = (p.V_local + kBN - 1) / kBN;
-  if (n_vt >= kChunkFullMinTiles) return launch_pair_sampler<false>(p, f, err, stream, kChunkTilesPerPair);
-  return launch_pair_sampler<true>(p, f, err, stream, 1);
+  if (n_vt < kChunkLeanMaxTiles) return launch_pair_sampler<true>(p, f, err, stream, 1);
+  int dev = 0;
+  const int sms = device_sms(&dev);
+  const int k = chunk_tiles_per_pair(n_vt, p.B, p.step_chunks, resident_pairs<false>(dev, sms));
+  return launch_pair_sampler<false>(p, f, err, stream, k);
 }
 
 int64_t tc_pair_topk_max_rows(int device) {

@@ -435,7 +435,9 @@ def run_ours(args):
 
     chunked = []
     if want("chunked"):
-        for b in synthetic.SHAPES["chunked"]["batches"]:
+        # B = 64 besides the chunked workload's batches: chunk calls there run
+        # another tensor-core family than the one-shot call
+        for b in sorted(set(synthetic.SHAPES["chunked"]["batches"]) | {64}):
             for n in (8, 32):
                 bounds = synthetic.chunk_bounds(V, n)
                 cm = torch.empty(b, device="cuda")
@@ -452,7 +454,8 @@ def run_ours(args):
                 us = graph_us(chunk_step)
                 rf = roofline(b, d, V, us, peaks)
                 chunked.append({"workload": "chunked", "B": b, "chunks": n, "us_per_step": round(us, 2),
-                                "frac": rf["frac"], "bound": rf["bound"], "path": fs.path_for_batch(b),
+                                "frac": rf["frac"], "bound": rf["bound"],
+                                "path": fs.path_for_chunks(b, bounds[1] - bounds[0], n),
                                 "launches_per_step": n, "cuda_graph": True})
 
     # online early finalization (8 chunks): rows without a dominant winner

@@ -113,8 +113,11 @@ FS_API fs_status fs_sample_ex(const void* h, const void* W, int64_t B, int64_t d
  * for it only before merging the carry -- so between the chunk calls of one
  * step, enqueue nothing on the stream that writes h, temp, W or bias.  The result of a full
  * sequence of calls equals fs_sample on the whole vocabulary bit for bit,
- * because the noise of (b, v) depends on the global id v only and the same
- * kernel family (chosen from B) computes every logit.
+ * because the noise of (b, v) depends on the global id v only and every
+ * logit is formed in the same arithmetic: at B = 1 both run the CUDA-core
+ * kernel; otherwise a chunk call may run another tensor-core family than the
+ * one-shot call (chosen from B, the chunk size and the chunk count of the
+ * previous step on the stream), and all of them form the same fp32 logits.
  *   W_chunk: rows [v_begin, v_end) of W, i.e. W + v_begin * d (device).
  *   bias_chunk: bias columns of the chunk (element (b, j) for global id
  *     v_begin + j at bias_chunk[b * bias_row_stride + j]) or NULL.
@@ -339,9 +342,15 @@ FS_API fs_status fs_set_path(int path);
  */
 FS_API fs_status fs_set_launch_overlap(int enable);
 
-/* The kernel family a call with batch size B would use under the current
- * setting (FS_PATH_SIMT / FS_PATH_TC_VOCAB / FS_PATH_TC_BATCH). */
+/* The kernel family a one-shot call with batch size B would use under the
+ * current setting (FS_PATH_SIMT / FS_PATH_TC_VOCAB / FS_PATH_TC_BATCH /
+ * FS_PATH_TC_PAIR). */
 FS_API int fs_path_for_batch(int64_t B);
+
+/* The kernel family a chunk call of B rows and V_chunk vocabulary rows would
+ * use under the current setting, when the previous chunked step on its stream
+ * had step_chunks chunk calls (0: none yet). */
+FS_API int fs_path_for_chunks(int64_t B, int64_t V_chunk, int step_chunks);
 
 /*
  * Timing hook: when both are non-NULL, every later sampling call on this

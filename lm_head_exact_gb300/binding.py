@@ -56,6 +56,7 @@ SIGNATURES = {
     "fs_set_path": (_int, [_int]),
     "fs_set_launch_overlap": (_int, [_int]),
     "fs_path_for_batch": (_int, [_i64]),
+    "fs_path_for_chunks": (_int, [_i64, _i64, _int]),
     "fs_profile_events": (_int, [_c_void_p, _c_void_p]),
     "fs_device_error": (_int, [ctypes.POINTER(_int)]),
     "fs_debug_wait_timeout": (_int, [_u64, _c_void_p]),
@@ -405,6 +406,10 @@ def set_launch_overlap(enable):
 
 def path_for_batch(B):
     return library().fs_path_for_batch(B)
+
+
+def path_for_chunks(B, V_chunk, step_chunks):
+    return library().fs_path_for_chunks(B, V_chunk, step_chunks)
 
 
 def workspace_reserve(B, V, stream=None):

@@ -313,9 +313,10 @@ fs_status check_problem(const Problem& p, bool need_out, const void* out_ids, co
 }
 
 // Kernel family for a call.  Auto: chosen from the batch size (and the
-// model width, identical for every chunk of a chunked run) only -- never from
-// V or the chunk range -- so one-shot and chunked runs compute every logit
-// with the same kernel and agree bit for bit.
+// model width, identical for every chunk of a chunked run), so one-shot and
+// chunked runs compute every logit in the same arithmetic and agree bit for
+// bit; chunk calls may take another tensor-core family (resolve_call_path),
+// since all of them form the same logits.
 constexpr int64_t kVocabMajorMaxBatch = 64;
 
 // Auto rule, measured on GB300 (Llama-3-8B head, fused kernel µs):
@@ -346,6 +347,29 @@ int resolve_path(int64_t B, int64_t d) {
   return path;
 }
 
+// Chunk calls of batches that fit one 128-row batch tile but not the two-
+// CTAs-per-SM vocabulary-major instantiation (32 < B <= 128) run the CTA-pair
+// kernel when the chunked step fits one wave of pairs with few tiles per pair,
+// else the batch-major kernel.  Every tensor-core family forms the same fp32
+// logits bit for bit and runs the same scan, so the samples still equal the
+// one-shot call's.  Measured on GB300 (8B head, µs per chunked step, 8 / 16 /
+// 32 chunks): B = 48 vocabulary-major 272 / - / 285, batch-major 242 / - /
+// 234, pair 219 / - / 266; B = 64 vocabulary-major 272 / 277 / 285, batch-
+// major 242 / 237 / 234; B = 128 batch-major 242 / 237 / 234, pair 223 / 252 /
+// 275.  At B <= 32 (two vocabulary-major CTAs per SM: 191-202) and B = 1
+// (CUDA-core logits) chunks keep the batch-size family.
+constexpr int64_t kChunkVocabMaxBatch = 32;
+
+int resolve_call_path(const Problem& p) {
+  const int path = resolve_path(p.B, p.d);
+  if (!p.chunk || g_forced_path.load() != kPathAuto) return path;
+  if (path != kPathTcVocab && path != kPathTcBatch) return path;
+  if (p.B <= kChunkVocabMaxBatch || p.B > 128) return path;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  return tc_pair_chunk_one_wave(p.V_local, p.B, p.step_chunks, dev) ? kPathTcPair : kPathTcBatch;
+}
+
 // One fused launch (kernel + in-kernel cross-CTA finish) for one problem,
 // finishing through key set `key_set` of the stream's workspace.
 fs_status run(Problem p, Finish f, cudaStream_t stream, int key_set = 0) {
@@ -358,7 +382,7 @@ fs_status run(Problem p, Finish f, cudaStream_t stream, int key_set = 0) {
     return FS_OK;
   }
   FS_TRY(get_finish(stream, p.B, &f, key_set));
-  const int path = resolve_path(p.B, p.d);
+  const int path = resolve_call_path(p);
   // The tensor-core kernels defer their input reads (interleaved A/B runs on
   // GB300: the overlap saves 4-8 us per back-to-back step at every B from 2
   // to 512); the CUDA-core kernel launches plainly.
@@ -895,6 +919,16 @@ fs_status fs_set_launch_overlap(int enable) {
 }
 
 int fs_path_for_batch(int64_t B) { return resolve_path(B, 4096); }
+
+int fs_path_for_chunks(int64_t B, int64_t V_chunk, int step_chunks) {
+  Problem p{};
+  p.B = B;
+  p.d = 4096;
+  p.V_local = V_chunk;
+  p.chunk = true;
+  p.step_chunks = step_chunks;
+  return resolve_call_path(p);
+}
 
 fs_status fs_profile_events(void* start, void* stop) {
   if ((start == nullptr) != (stop == nullptr))

@@ -122,6 +122,9 @@ cudaError_t launch_tc_batch(const Problem& p, const Finish& f, int* err, cudaStr
 // Tensor-core batch-major path over CTA pairs (tcgen05 cta_group::2; any B,
 // d >= 64).
 cudaError_t launch_tc_pair(const Problem& p, const Finish& f, int* err, cudaStream_t stream);
+// Whether a chunked step of step_chunks such chunks fits one wave of CTA
+// pairs with few tiles per pair (the chunk family rule of fs_api.cu).
+bool tc_pair_chunk_one_wave(int64_t V_local, int64_t B, int step_chunks, int device);
 
 // Unfused comparison pipeline: tensor-core GEMM storing fp32 logits [B, V]
 // (+ bias) to HBM, then row softmax into probs [B, V], then the sample.

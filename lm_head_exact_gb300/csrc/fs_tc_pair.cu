@@ -521,6 +521,30 @@ static int chunk_tiles_per_pair(int64_t n_vt, int64_t B, int step_chunks, int pa
   return best_k;
 }
 
+// Whether a chunked step of step_chunks chunks like this one (V_local rows,
+// B batch rows) runs on the pairs in ONE wave with at most
+// kChunkFastTilesPerPair tiles per pair, which is where the pair kernel beats
+// the single-CTA batch-major kernel for chunks of batches that fit one
+// 128-row batch tile (8B head, B = 64 and 128, µs per step, pair vs batch-
+// major: 4 chunks 215 / 218 vs 241, 6 chunks 217 / 221 vs 243, 8 chunks 219 /
+// 223 vs 241, 12 chunks 229 / 232 vs 242 -- one wave of k = 7; 10 chunks
+// 264 / 265 vs 242, 16 chunks 249 / 252 vs 237, 20 chunks 272 / 273 vs
+// 249, 32 chunks 266 / 275 vs 233 -- two waves or the lean instantiation).
+constexpr int kChunkFastTilesPerPair = 7;
+
+bool tc_pair_chunk_one_wave(int64_t V_local, int64_t B, int step_chunks, int device) {
+  const int64_t n_vt = (V_local + kBN - 1) / kBN;
+  if (step_chunks <= 0 || n_vt < kChunkLeanMaxTiles || B <= 0) return false;
+  int sms = 0;
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
+  const int pairs = resident_pairs<false>(device, sms > 0 ? sms : 148);
+  const int64_t npt = (std::min<int64_t>(B, static_cast<int64_t>(pairs) * 2 * kRowsPerCta) + 2 * kRowsPerCta - 1) /
+                      (2 * kRowsPerCta);
+  for (int k = kChunkMinTilesPerPair; k <= kChunkFastTilesPerPair; ++k)
+    if (static_cast<int64_t>(step_chunks) * ((n_vt + k - 1) / k) * npt <= pairs) return true;
+  return false;
+}
+
 cudaError_t launch_tc_pair(const Problem& p, const Finish& f, int* err, cudaStream_t stream) {
   if (p.d < kBK || p.V_local <= 0) return cudaErrorNotSupported;
   if (!p.chunk) return launch_pair_sampler<false>(p, f, err, stream, 1);

@@ -141,3 +141,29 @@ def test_auto_dispatch_rule(built_library):
     finally:
         fs.set_path(fs.FS_PATH_AUTO)
     assert fs.path_for_batch(16) == fs.FS_PATH_TC_VOCAB
+
+
+def test_chunk_dispatch_rule(built_library):
+    """Chunk calls (host logic, no GPU): B = 1, B <= 32 and B > 128 keep the
+    batch-size family; 32 < B <= 128 take the CTA-pair kernel when the step
+    (the previous step's chunk count) fits one wave of pairs with at most 7
+    tiles per pair and every chunk has at least 24 pair tiles, else the batch-
+    major kernel; a forced family is honoured.  Chunks of the 128256-row
+    vocabulary: 8 chunks of 16032 rows (63 tiles: 8 x 9 = 72 pairs at k = 7),
+    10 of 12826 (51 tiles: 80 pairs), 32 of 4008 (16 tiles)."""
+    from lm_head_exact_gb300 import binding as fs
+    V = 128256
+    for B in (1, 16, 32, 129, 256):
+        for n in (0, 8, 32):
+            assert fs.path_for_chunks(B, -(-V // max(n, 8)), n) == fs.path_for_batch(B), (B, n)
+    for B in (33, 64, 100, 128):
+        assert fs.path_for_chunks(B, 16032, 8) == fs.FS_PATH_TC_PAIR, B
+        assert fs.path_for_chunks(B, 16032, 0) == fs.FS_PATH_TC_BATCH, B    # first step: no count yet
+        assert fs.path_for_chunks(B, 12826, 10) == fs.FS_PATH_TC_BATCH, B
+        assert fs.path_for_chunks(B, 4008, 32) == fs.FS_PATH_TC_BATCH, B
+        assert fs.path_for_chunks(B, 5888, 8) == fs.FS_PATH_TC_BATCH, B     # 23 pair tiles per chunk
+    try:
+        fs.set_path(fs.FS_PATH_TC_VOCAB)
+        assert fs.path_for_chunks(64, 16032, 8) == fs.FS_PATH_TC_VOCAB
+    finally:
+        fs.set_path(fs.FS_PATH_AUTO)

@@ -450,6 +450,35 @@ def test_many_small_chunks_overlapping_launches(fs, torch_cuda, path):
         np.testing.assert_array_equal(res[1].cpu().numpy(), ref_mx.cpu().numpy())
 
 
+@pytest.mark.parametrize("B", [40, 64, 128])
+@pytest.mark.parametrize("n", [8, 32])
+def test_chunk_family_rule_keeps_one_shot_samples(fs, torch_cuda, B, n):
+    """Under the automatic rule, chunk calls at 32 < B <= 128 run the batch-
+    major kernel, or the CTA-pair kernel once the previous step's chunk count
+    shows that the step fits one wave of pairs (here from the second 8-chunk
+    step on: 25 pair tiles per chunk); the one-shot call at B <= 64 runs the
+    vocabulary-major kernel.  Every step must equal its one-shot sample bit
+    for bit, and the oracle within the comparison rule."""
+    torch = torch_cuda
+    V, d = 50000, 256
+    h, W, temp = _problem(B, V, d, seed=97 + B)
+    hd, Wd, td = to_device(h, torch), to_device(W, torch), to_device(temp, torch)
+    bounds = synthetic.chunk_bounds(V, n)
+    cm = torch.empty(B, device="cuda")
+    ci = torch.empty(B, dtype=torch.int64, device="cuda")
+    stream = torch.cuda.Stream()      # a stream with no chunked history
+    stream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(stream):
+        for step in (4, 5, 6):
+            ref_ids, ref_mx = fs.sample(hd, Wd, td, 13, step)
+            for i, (lo, hi) in enumerate(zip(bounds[:-1], bounds[1:])):
+                res = fs.sample_chunked(hd, Wd[lo:hi], lo, td, 13, step, cm, ci, i == 0, i == n - 1)
+            stream.synchronize()
+            np.testing.assert_array_equal(res[0].cpu().numpy(), ref_ids.cpu().numpy())
+            np.testing.assert_array_equal(res[1].cpu().numpy(), ref_mx.cpu().numpy())
+    compare(res[0].cpu().numpy(), res[1].cpu().numpy(), sampler.sample(h, W, temp, 13, 6), what="chunked")
+
+
 def test_chunked_step_interleaved_with_one_shot_calls(fs, torch_cuda, path):
     """One-shot calls of another batch size, and a Gumbel-top-k call, enqueued
     on the same stream between the chunk calls of a step: they finish through

@@ -125,7 +125,7 @@ def test_signed_zero_scores_tie_to_the_smaller_id(fs, torch_cuda, path):
 
 
 @pytest.mark.parametrize("B,V,d", [(64, 4097, 4096), (128, 8192, 4096), (200, 3000, 1024), (32, 1000, 8192),
-                                   (256, 16032, 4096)])
+                                   (256, 16032, 4096), (48, 3001, 200), (100, 2000, 72), (160, 5000, 328)])
 def test_tensor_core_families_form_identical_logits(fs, torch_cuda, B, V, d):
     """The three tensor-core kernel families -- vocabulary-major (W as the
     MMA's A operand, M = 128 vocabulary rows), batch-major (h as A, one CTA)

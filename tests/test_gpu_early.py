@@ -138,12 +138,14 @@ def test_early_empty_first_chunk_clears_stale_flag(fs, torch_cuda):
 
 
 # ------------------------------------------------------------------ full size (chunked workload shape)
-@pytest.mark.parametrize("B", [1, 32, 256])
+@pytest.mark.parametrize("B", [1, 32, 64, 256])
 def test_early_full_size_spiked_and_flat(fs, torch_cuda, B):
     """d 4096, V 128256 in 8 chunks.  Without spikes no row is ever final
     (the bound |h||W|/T + 16.6 is far above the winning scores) and every
     chunk runs; with a +200 spike in the first chunk of every row, the first
-    call finalizes all rows.  Both equal the one-shot sample bit for bit."""
+    call finalizes all rows.  Both equal the one-shot sample bit for bit.
+    (At B = 64 the second step's chunks run on the CTA-pair kernel, the
+    one-shot call on the vocabulary-major kernel.)"""
     torch = torch_cuda
     wl = synthetic.workload("chunked", B)
     V = wl.W.shape[0]

@@ -391,13 +391,14 @@ def test_back_to_back_calls_of_different_batch_sizes(fs, torch_cuda, path):
                 what=f"B={B}")
 
 
-@pytest.mark.parametrize("B", [1, 32, 256])
+@pytest.mark.parametrize("B", [1, 32, 64, 128, 256])
 def test_chunked_sequence_captured_in_cuda_graph(fs, torch_cuda, B):
     """After fs_workspace_reserve, a whole chunked decode step (8 launches)
     can be captured into a CUDA graph; every replay reproduces the one-shot
-    sample bit for bit."""
+    sample bit for bit.  The captured step follows an eager one, so at B = 64
+    and 128 it runs on the CTA-pair kernel (25 pair tiles per chunk)."""
     torch = torch_cuda
-    V, d, n = 20011, 256, 8
+    V, d, n = 50021, 256, 8
     h, W, temp = _problem(B, V, d, seed=40 + B)
     hd, Wd, td = to_device(h, torch), to_device(W, torch), to_device(temp, torch)
     bounds = synthetic.chunk_bounds(V, n)

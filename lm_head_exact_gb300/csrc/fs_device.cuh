@@ -79,6 +79,12 @@ __device__ __forceinline__ float gumbel_from_word(uint32_t x) {
   return gumbel_from_uniform(uniform_from_word(x));
 }
 
+// Upper bound of every value gumbel_from_word returns: the largest Gumbel
+// value of the uniform grid, -log(-log(1 - 2^-24)) = 16.63553..., rounded up
+// (the device transform is within 2e-6 of it and largest at the top grid
+// point, checked over the whole grid).
+constexpr float kGumbelMax = 16.6356f;
+
 // -------------------------------------------------------------------------
 // Per-row temperature mode.  T > 0: z = logit * (1/T) + g.  T == 0: greedy,
 // z = logit.  T < 0 or NaN: the row has no valid sample (id -1).

@@ -39,13 +39,31 @@ __device__ __forceinline__ void scan32(const uint32_t (&r)[32], int64_t v0, int6
                                        const RowScan& s, Best& best) {
   const int64_t vg0 = v_offset + v0;
   if (v0 + 32 <= v_local_end && (vg0 & 3) == 0) {
-    // fast path: 8 whole counter quads, every id in range
+    // fast path: 8 whole counter quads, every id in range.  A quad whose
+    // largest scaled logit plus the largest Gumbel value cannot beat its row's
+    // best cannot change the row's result (fmaf is monotone in each of its
+    // scaled and added operands, and the best is replaced only by a strictly
+    // larger score); when that holds on every lane, the warp skips the quad's
+    // noise.  Rows whose logits sit far above the rest (large biases, peaked
+    // distributions) skip most quads; the samples are the same.
     const uint32_t q0 = static_cast<uint32_t>(vg0 >> 2);
     const int32_t id0 = static_cast<int32_t>(vg0);
+    const unsigned lanes = __activemask();
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
-      const uint4 w = noise_words(s.key, q0 + q, s.row, s.step_lo, s.step_hi);
       const int j = 4 * q;
+      float l0 = __uint_as_float(r[j + 0]), l1 = __uint_as_float(r[j + 1]);
+      float l2 = __uint_as_float(r[j + 2]), l3 = __uint_as_float(r[j + 3]);
+      if constexpr (kHasBias) {
+        l0 += __ldg(s.bias_row + v0 + j + 0);
+        l1 += __ldg(s.bias_row + v0 + j + 1);
+        l2 += __ldg(s.bias_row + v0 + j + 2);
+        l3 += __ldg(s.bias_row + v0 + j + 3);
+      }
+      const float lmax = fmaxf(fmaxf(l0, l1), fmaxf(l2, l3));
+      const float bound = s.greedy ? lmax : fmaf(lmax, s.inv_t, kGumbelMax);
+      if (!__any_sync(lanes, bound > best.z)) continue;
+      const uint4 w = noise_words(s.key, q0 + q, s.row, s.step_lo, s.step_hi);
       keep_best(best, perturbed<kHasBias>(s, __uint_as_float(r[j + 0]), w.x, v0 + j + 0), id0 + j + 0);
       keep_best(best, perturbed<kHasBias>(s, __uint_as_float(r[j + 1]), w.y, v0 + j + 1), id0 + j + 1);
       keep_best(best, perturbed<kHasBias>(s, __uint_as_float(r[j + 2]), w.z, v0 + j + 2), id0 + j + 2);

@@ -23,10 +23,6 @@
 
 namespace fs {
 
-// Largest Gumbel value the uniform grid can produce, -log(-log(1 - 2^-24)) =
-// 16.63553..., rounded up.
-constexpr float kGumbelMax = 16.6356f;
-
 // Row b can no longer be overtaken by the later chunks: its best perturbed
 // score is at least their upper bound (Cauchy-Schwarz on the logit, the
 // largest bias, the largest Gumbel value), with a margin for fp32 rounding.

@@ -433,6 +433,23 @@ def run_ours(args):
         del graph
         return e0.elapsed_time(e1) / reps * 1e3
 
+    def direct_us(step_fn, reps=20):
+        """Back-to-back steps launched directly on the stream (as the one-shot
+        rows are timed): 3 untimed, then µs per step over `reps`."""
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                step_fn()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        with torch.cuda.stream(stream):
+            for _ in range(reps):
+                step_fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps * 1e3
+
     chunked = []
     if want("chunked"):
         # B = 64 besides the chunked workload's batches: chunk calls there run
@@ -446,17 +463,30 @@ def run_ours(args):
                 cmx = torch.empty(b, dtype=torch.float32, device="cuda")
                 fs.workspace_reserve(b, V, stream=stream)
 
+                bounds_np = np.asarray(bounds, np.int64)
+
                 def chunk_step():
                     for i, (lo, hi) in enumerate(zip(bounds[:-1], bounds[1:])):
                         fs.sample_chunked(hd_all[:b], Wd[lo:hi], lo, temp_all[:b],
                                           seed, 5, cm, ci, i == 0, i == n - 1, out=(cids, cmx), stream=stream)
 
-                us = graph_us(chunk_step)
+                def chunk_step_one_call():
+                    fs.sample_chunked_step(hd_all[:b], Wd, bounds_np, temp_all[:b], seed, 5, cm, ci,
+                                           out=(cids, cmx), stream=stream)
+
+                # the step's chunk calls issued from C, steps back to back on the
+                # stream (as the one-shot rows); beside it the per-chunk calls
+                # replayed as a CUDA graph of one step, which measures 5-14%
+                # slower on GB300 (graph-launched kernels overlap their
+                # neighbours less than stream-launched ones)
+                us = direct_us(chunk_step_one_call)
+                us_graph = graph_us(chunk_step)
                 rf = roofline(b, d, V, us, peaks)
                 chunked.append({"workload": "chunked", "B": b, "chunks": n, "us_per_step": round(us, 2),
                                 "frac": rf["frac"], "bound": rf["bound"],
                                 "path": fs.path_for_chunks(b, bounds[1] - bounds[0], n),
-                                "launches_per_step": n, "cuda_graph": True})
+                                "launches_per_step": n, "launch": "fs_sample_chunked_step, back to back",
+                                "graph_us_per_step": round(us_graph, 2)})
 
     # online early finalization (8 chunks): rows without a dominant winner
     # ("flat", every chunk runs) and rows with a +200 spike in the first

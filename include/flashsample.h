@@ -136,6 +136,28 @@ FS_API fs_status fs_sample_chunked(const void* h, const void* W_chunk, int64_t B
                             int64_t* out_ids, float* out_max, void* stream);
 
 /*
+ * One whole chunked step: the fs_sample_chunked calls of chunks
+ * [bounds[i], bounds[i+1]) for i = 0 .. n_chunks - 1 (FS_CHUNK_FIRST on the
+ * first, FS_CHUNK_LAST on the last), issued from C in one call, so that a
+ * host loop's per-call overhead does not bound a step of many small chunks.
+ * Same kernels, launches and results as the sequence of calls (equal to
+ * fs_sample on the whole vocabulary bit for bit).
+ *   W: the full [bounds[n_chunks], d] matrix (device); chunk i is rows
+ *     [bounds[i], bounds[i+1]).
+ *   bounds: host array of n_chunks + 1 non-decreasing row offsets, bounds[0]
+ *     = 0; empty chunks are allowed.
+ *   bias: NULL or the [B, V] (row stride bias_row_stride, or 0 for a shared
+ *     [V]) bias of the whole vocabulary; chunk i reads columns bounds[i] ...
+ *   carry_max / carry_ids / out_ids / out_max / stream: as fs_sample_chunked.
+ * Returns the first failing chunk call's status (later chunks not launched).
+ */
+FS_API fs_status fs_sample_chunked_step(const void* h, const void* W, int64_t B, int64_t d, const int64_t* bounds,
+                                        int n_chunks, const float* temp, const float* bias,
+                                        int64_t bias_row_stride, uint64_t seed, uint64_t step,
+                                        float* carry_max, int64_t* carry_ids,
+                                        int64_t* out_ids, float* out_max, void* stream);
+
+/*
  * Chunked variant with online early finalization (summary page, "Method",
  * last paragraph: the streaming sampler may stop once the later tiles can no
  * longer overtake the running maximum).  Same arguments and result as

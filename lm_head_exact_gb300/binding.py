@@ -56,6 +56,9 @@ SIGNATURES = {
     "fs_set_path": (_int, [_int]),
     "fs_set_launch_overlap": (_int, [_int]),
     "fs_path_for_batch": (_int, [_i64]),
+    "fs_sample_chunked_step": (_int, [_c_void_p, _c_void_p, _i64, _i64, _c_void_p, _int, _c_void_p, _c_void_p,
+                                      _i64, _u64, _u64, _c_void_p, _c_void_p, _c_void_p, _c_void_p,
+                                      _c_void_p]),
     "fs_path_for_chunks": (_int, [_i64, _i64, _int]),
     "fs_profile_events": (_int, [_c_void_p, _c_void_p]),
     "fs_device_error": (_int, [ctypes.POINTER(_int)]),
@@ -293,6 +296,28 @@ def sample_chunked(h, W_chunk, v_begin, temp, seed, step, carry_max, carry_ids, 
         flags, _dev(ids, "out_ids") if last else ctypes.c_void_p(0),
         _dev(mx, "out_max") if last else ctypes.c_void_p(0), _stream_ptr(stream)))
     return (ids, mx) if last else None
+
+
+def sample_chunked_step(h, W, bounds, temp, seed, step, carry_max, carry_ids, bias=None, out=None,
+                        stream=None):
+    """One whole chunked step over chunks [bounds[i], bounds[i+1]) of W in
+    one C call (the per-chunk calls of ``sample_chunked`` issued from C).
+    ``bounds`` may be a list or an int64 numpy array (kept by the caller to
+    reuse).  Returns (ids, max)."""
+    torch = _torch()
+    B, d = h.shape
+    b = bounds if isinstance(bounds, np.ndarray) and bounds.dtype == np.int64 else np.asarray(bounds, np.int64)
+    n = len(b) - 1
+    if n < 1 or b[-1] != W.shape[0]:
+        raise FlashSampleError("FS_ERR_INVALID_ARG", "bounds must have >= 2 entries ending at W.shape[0]")
+    ids, mx = _outs(B, h.device, out)
+    bptr, bstride = _bias_args(bias, B, W.shape[0])
+    check(library().fs_sample_chunked_step(
+        _dev(h, "h", torch.bfloat16, 2), _dev(W, "W", torch.bfloat16, 2), B, d, ctypes.c_void_p(b.ctypes.data), n,
+        _dev(temp, "temp", torch.float32, 1), bptr, bstride, seed, step,
+        _dev(carry_max, "carry_max", torch.float32), _dev(carry_ids, "carry_ids", torch.int64),
+        _dev(ids, "out_ids"), _dev(mx, "out_max"), _stream_ptr(stream)))
+    return ids, mx
 
 
 def sample_chunked_early(h, W_chunk, v_begin, temp, seed, step, carry_max, carry_ids, first, last,

@@ -438,10 +438,20 @@ struct EarlyArgs {
   int* done = nullptr;
 };
 
+fs_status check_carry(int64_t B, const float* carry_max, const int64_t* carry_ids) {
+  if (B > 0) {
+    FS_TRY(check_device_ptr(carry_max, "carry_max"));
+    FS_TRY(check_aligned(carry_max, 4, "carry_max"));
+    FS_TRY(check_device_ptr(carry_ids, "carry_ids"));
+    FS_TRY(check_aligned(carry_ids, 8, "carry_ids"));
+  }
+  return FS_OK;
+}
+
 fs_status sample_chunk(const void* h, const void* W_chunk, int64_t B, int64_t d, int64_t v_begin, int64_t v_end,
                        const float* temp, const float* bias_chunk, int64_t bias_row_stride, uint64_t seed,
                        uint64_t step, float* carry_max, int64_t* carry_ids, int flags, const EarlyArgs& early,
-                       int64_t* out_ids, float* out_max, void* stream) {
+                       int64_t* out_ids, float* out_max, void* stream, bool checked = false) {
   if (v_begin < 0 || v_end < v_begin)
     return fail(FS_ERR_INVALID_ARG, "need 0 <= v_begin <= v_end (got %lld, %lld)",
                 (long long)v_begin, (long long)v_end);
@@ -455,12 +465,9 @@ fs_status sample_chunk(const void* h, const void* W_chunk, int64_t B, int64_t d,
   // they wait for it only before merging into the shared carry.
   p.pdl = (flags & (FS_CHUNK_FIRST | FS_CHUNK_SERIAL)) == 0;
   p.chunk = true;
-  FS_TRY(check_problem(p, last, out_ids, out_max));
-  if (B > 0) {
-    FS_TRY(check_device_ptr(carry_max, "carry_max"));
-    FS_TRY(check_aligned(carry_max, 4, "carry_max"));
-    FS_TRY(check_device_ptr(carry_ids, "carry_ids"));
-    FS_TRY(check_aligned(carry_ids, 8, "carry_ids"));
+  if (!checked) {   // (fs_sample_chunked_step checks its pointers once per step)
+    FS_TRY(check_problem(p, last, out_ids, out_max));
+    FS_TRY(check_carry(B, carry_max, carry_ids));
   }
   Finish f{};
   f.carry_max = carry_max;
@@ -555,6 +562,35 @@ fs_status fs_sample_chunked(const void* h, const void* W_chunk, int64_t B, int64
   g_last_error[0] = '\0';
   return sample_chunk(h, W_chunk, B, d, v_begin, v_end, temp, bias_chunk, bias_row_stride, seed, step, carry_max,
                       carry_ids, flags, EarlyArgs{}, out_ids, out_max, stream);
+}
+
+fs_status fs_sample_chunked_step(const void* h, const void* W, int64_t B, int64_t d, const int64_t* bounds,
+                                 int n_chunks, const float* temp, const float* bias, int64_t bias_row_stride,
+                                 uint64_t seed, uint64_t step, float* carry_max, int64_t* carry_ids,
+                                 int64_t* out_ids, float* out_max, void* stream) {
+  g_last_error[0] = '\0';
+  if (n_chunks < 1) return fail(FS_ERR_INVALID_ARG, "need n_chunks >= 1 (got %d)", n_chunks);
+  if (bounds == nullptr) return fail(FS_ERR_INVALID_ARG, "bounds is NULL");
+  if (bounds[0] != 0) return fail(FS_ERR_INVALID_ARG, "bounds[0] must be 0 (got %lld)", (long long)bounds[0]);
+  for (int i = 0; i < n_chunks; ++i)
+    if (bounds[i + 1] < bounds[i])
+      return fail(FS_ERR_INVALID_ARG, "bounds must not decrease (bounds[%d] = %lld > bounds[%d] = %lld)", i,
+                  (long long)bounds[i], i + 1, (long long)bounds[i + 1]);
+  if (d < 0) return fail(FS_ERR_INVALID_ARG, "need d >= 0 (got %lld)", (long long)d);
+  if (bounds[n_chunks] >= (int64_t(1) << 31)) return fail(FS_ERR_UNSUPPORTED, "bounds[n_chunks] must be < 2^31");
+  // the pointers and shapes of the whole step are checked once: every
+  // chunk's W rows, bias columns and outputs lie inside them
+  Problem whole{h, W, B, d, bounds[n_chunks], 0, temp, bias, bias_row_stride, seed, step};
+  FS_TRY(check_problem(whole, true, out_ids, out_max));
+  FS_TRY(check_carry(B, carry_max, carry_ids));
+  for (int i = 0; i < n_chunks; ++i) {
+    const int flags = (i == 0 ? FS_CHUNK_FIRST : 0) | (i == n_chunks - 1 ? FS_CHUNK_LAST : 0);
+    const void* W_chunk = static_cast<const uint16_t*>(W) + bounds[i] * d;
+    const float* bias_chunk = bias != nullptr ? bias + bounds[i] : nullptr;
+    FS_TRY(sample_chunk(h, W_chunk, B, d, bounds[i], bounds[i + 1], temp, bias_chunk, bias_row_stride, seed, step,
+                        carry_max, carry_ids, flags, EarlyArgs{}, out_ids, out_max, stream, true));
+  }
+  return FS_OK;
 }
 
 fs_status fs_sample_chunked_early(const void* h, const void* W_chunk, int64_t B, int64_t d,

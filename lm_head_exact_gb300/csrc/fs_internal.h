@@ -2,6 +2,7 @@
 // the C ABI to the kernel launchers, and the launchers themselves.
 #pragma once
 
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 #include <utility>
@@ -58,6 +59,24 @@ struct Problem {
 };
 
 // Launch `kernel` on `stream`, as a programmatic dependent launch when `pdl`.
+// Raises a kernel's dynamic shared memory limit to at least `bytes` on
+// device `dev`, calling the runtime only when the limit this process set
+// before is lower: the attribute persists, and setting it on every launch
+// costs host time in chunked steps of many launches.
+template <auto kKernel>
+cudaError_t raise_smem_limit(int dev, int bytes) {
+  static std::atomic<int> set_bytes[64];   // zero-initialized (static storage)
+  const bool cached = dev >= 0 && dev < 64;
+  if (cached && set_bytes[dev].load(std::memory_order_acquire) >= bytes) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(kKernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && cached) {
+    int cur = set_bytes[dev].load(std::memory_order_relaxed);
+    while (cur < bytes && !set_bytes[dev].compare_exchange_weak(cur, bytes, std::memory_order_release)) {
+    }
+  }
+  return e;
+}
+
 template <typename... KArgs, typename... Args>
 cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
                           bool pdl, Args&&... args) {

@@ -163,12 +163,10 @@ int pick_group(int64_t B, int64_t d) {
 template <int BG, bool kEarly>
 cudaError_t launch_variant(const Problem& p, const Finish& f, cudaStream_t stream) {
   const size_t smem = static_cast<size_t>(BG) * p.d * 2;
-  cudaError_t e = cudaFuncSetAttribute(simt_fused_kernel<BG, kEarly>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
-  if (e != cudaSuccess) return e;
   int dev = 0, sms = 0, per_sm = 0;
   cudaGetDevice(&dev);
+  cudaError_t e = raise_smem_limit<simt_fused_kernel<BG, kEarly>>(dev, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, simt_fused_kernel<BG, kEarly>, kSimtThreads, smem);
   if (e != cudaSuccess) return e;

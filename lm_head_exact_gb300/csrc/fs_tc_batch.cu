@@ -385,11 +385,10 @@ static cudaError_t launch_batch_impl(const Problem& p, const Finish* f, float* l
   const bool store = logits != nullptr;
   cudaError_t e = cudaSuccess;
   if (store) {
-    e = cudaFuncSetAttribute(tc_batch_kernel<true, 0, 16>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    e = raise_smem_limit<tc_batch_kernel<true, 0, 16>>(dev, kSmemBytes);
   } else {
-    e = cudaFuncSetAttribute(tc_batch_kernel<false, 0, 16>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(tc_batch_kernel<false, 0, 8>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    e = raise_smem_limit<tc_batch_kernel<false, 0, 16>>(dev, kSmemBytes);
+    if (e == cudaSuccess) e = raise_smem_limit<tc_batch_kernel<false, 0, 8>>(dev, kSmemBytes);
   }
   if (e != cudaSuccess) return e;
   CUtensorMap tw;
@@ -461,8 +460,7 @@ static cudaError_t launch_topk_k(const Problem& p, Partial* partials, int* err, 
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (sms <= 0) sms = 148;
   if (p.B > static_cast<int64_t>(sms) * kBM) return cudaErrorNotSupported;   // one launch
-  cudaError_t e = cudaFuncSetAttribute(tc_batch_kernel<false, K, 8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       smem_bytes(K));
+  cudaError_t e = raise_smem_limit<tc_batch_kernel<false, K, 8>>(dev, smem_bytes(K));
   if (e != cudaSuccess) return e;
   CUtensorMap tw, th;
   if (!encode_kmajor_bf16(&tw, p.W, p.V_local, p.d, kBK, kBN)) return cudaErrorInvalidValue;

@@ -444,8 +444,7 @@ static cudaError_t launch_pair_sampler(const Problem& p, const Finish& f, int* e
   using Cfg = PairCfg<kLean>;
   int dev = 0;
   const int sms = device_sms(&dev);
-  cudaError_t e = cudaFuncSetAttribute(tc_pair_kernel<0, kLean>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       Cfg::kSmemBytes);
+  cudaError_t e = raise_smem_limit<tc_pair_kernel<0, kLean>>(dev, Cfg::kSmemBytes);
   if (e != cudaSuccess) return e;
   const int pairs = resident_pairs<kLean>(dev, sms);
   CUtensorMap tw;
@@ -575,7 +574,7 @@ static cudaError_t launch_pair_topk_k(const Problem& p, Partial* partials, int* 
   const int sms = device_sms(&dev);
   const int pairs = resident_pairs(dev, sms);
   if (p.B > static_cast<int64_t>(pairs) * 2 * kRowsPerCta) return cudaErrorNotSupported;   // one launch
-  cudaError_t e = cudaFuncSetAttribute(tc_pair_kernel<K>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes(K));
+  cudaError_t e = raise_smem_limit<tc_pair_kernel<K>>(dev, smem_bytes(K));
   if (e != cudaSuccess) return e;
   CUtensorMap tw, th;
   if (!encode_kmajor_bf16(&tw, p.W, p.V_local, p.d, kBK, kBN / 2)) return cudaErrorInvalidValue;

@@ -426,11 +426,10 @@ cudaError_t launch_bn(const Problem& p, const Finish& f, int* err, cudaStream_t 
   CUtensorMap tw, th;
   if (!encode_kmajor_bf16(&tw, p.W, p.V_local, p.d, kBK, kBM)) return cudaErrorInvalidValue;
   if (!encode_kmajor_bf16(&th, p.h, p.B, p.d, kBK, BN)) return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(tc_vocab_kernel<BN, kTopK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       C::kSmemBytes);
-  if (e != cudaSuccess) return e;
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
+  cudaError_t e = raise_smem_limit<tc_vocab_kernel<BN, kTopK>>(dev, C::kSmemBytes);
+  if (e != cudaSuccess) return e;
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (sms <= 0) sms = 148;
   const int64_t n_vt = (p.V_local + kBM - 1) / kBM;

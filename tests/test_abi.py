@@ -88,6 +88,16 @@ def test_host_side_argument_checks(built_library):
     assert lib.fs_row_norms(z, 0, 64, z, z) == 0
     assert lib.fs_row_norms(z, 3, 12, z, z) == 2
     assert lib.fs_debug_noise(0, 0, -1, 1, 0, 1, z, z, z) == 1
+    # one-call chunked step: chunk count and bounds are checked before any chunk runs
+    ok = (ctypes.c_int64 * 3)(0, 5, 10)
+    assert lib.fs_sample_chunked_step(z, z, 4, 64, ok, 0, z, z, 0, 0, 0, z, z, z, z, z) == 1
+    assert "n_chunks" in lib.fs_last_error().decode()
+    assert lib.fs_sample_chunked_step(z, z, 4, 64, z, 2, z, z, 0, 0, 0, z, z, z, z, z) == 1
+    assert lib.fs_sample_chunked_step(z, z, 4, 64, bounds, 2, z, z, 0, 0, 0, z, z, z, z, z) == 1
+    assert "must not decrease" in lib.fs_last_error().decode()
+    shifted = (ctypes.c_int64 * 3)(3, 5, 10)
+    assert lib.fs_sample_chunked_step(z, z, 4, 64, shifted, 2, z, z, 0, 0, 0, z, z, z, z, z) == 1
+    assert "bounds[0]" in lib.fs_last_error().decode()
     # B == 0 is a no-op
     assert lib.fs_sample(z, z, 0, 64, 10, z, 0, 0, z, z, z) == 0
 

@@ -480,6 +480,36 @@ def test_chunk_family_rule_keeps_one_shot_samples(fs, torch_cuda, B, n):
     compare(res[0].cpu().numpy(), res[1].cpu().numpy(), sampler.sample(h, W, temp, 13, 6), what="chunked")
 
 
+@pytest.mark.parametrize("B", [1, 32, 64, 256])
+def test_one_call_chunked_step(fs, torch_cuda, B):
+    """fs_sample_chunked_step issues a whole step's chunk calls from C: on
+    ragged bounds with an empty chunk, with a per-row bias, it equals the
+    one-shot sample and the per-chunk call sequence bit for bit, over steps
+    in a row (the later ones with the chunk count of the previous step)."""
+    torch = torch_cuda
+    V, d = 30011, 256
+    h, W, temp = _problem(B, V, d, seed=131 + B)
+    bias = np.zeros((B, V), np.float32)
+    bias[:, ::97] = 0.5
+    hd, Wd, td, bd = to_device(h, torch), to_device(W, torch), to_device(temp, torch), to_device(bias, torch)
+    bounds = np.array([0, 7001, 7001, 15000, 15013, 26000, V], np.int64)
+    cm = torch.empty(B, device="cuda")
+    ci = torch.empty(B, dtype=torch.int64, device="cuda")
+    for step in (2, 3):
+        ref_ids, ref_mx = fs.sample(hd, Wd, td, 17, step, bias=bd)
+        ids, mx = fs.sample_chunked_step(hd, Wd, bounds, td, 17, step, cm, ci, bias=bd)
+        n = len(bounds) - 1
+        for i, (lo, hi) in enumerate(zip(bounds[:-1], bounds[1:])):
+            res = fs.sample_chunked(hd, Wd[lo:hi], int(lo), td, 17, step, cm, ci, i == 0, i == n - 1,
+                                    bias_chunk=bd[:, lo:hi])
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(ids.cpu().numpy(), ref_ids.cpu().numpy())
+        np.testing.assert_array_equal(mx.cpu().numpy(), ref_mx.cpu().numpy())
+        np.testing.assert_array_equal(res[0].cpu().numpy(), ref_ids.cpu().numpy())
+        np.testing.assert_array_equal(res[1].cpu().numpy(), ref_mx.cpu().numpy())
+    compare(ids.cpu().numpy(), mx.cpu().numpy(), sampler.sample(h, W, temp, 17, 3, bias=bias), what="chunked step")
+
+
 def test_chunked_step_interleaved_with_one_shot_calls(fs, torch_cuda, path):
     """One-shot calls of another batch size, and a Gumbel-top-k call, enqueued
     on the same stream between the chunk calls of a step: they finish through

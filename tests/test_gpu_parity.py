@@ -510,6 +510,31 @@ def test_one_call_chunked_step(fs, torch_cuda, B):
     compare(ids.cpu().numpy(), mx.cpu().numpy(), sampler.sample(h, W, temp, 17, 3, bias=bias), what="chunked step")
 
 
+@pytest.mark.parametrize("B", [1, 48, 200])
+def test_one_call_chunked_step_with_many_chunks(fs, torch_cuda, B):
+    """A one-call step of 70 uneven chunks (more than the workspace's 32 key
+    sets, so some chunk calls launch without overlap) equals the one-shot
+    sample bit for bit, twice in a row on a fresh stream."""
+    torch = torch_cuda
+    V, d = 12007, 128
+    h, W, temp = _problem(B, V, d, seed=151 + B)
+    hd, Wd, td = to_device(h, torch), to_device(W, torch), to_device(temp, torch)
+    g = np.random.default_rng(B)
+    bounds = np.unique(np.r_[0, np.sort(g.integers(0, V, size=69)), V]).astype(np.int64)
+    cm = torch.empty(B, device="cuda")
+    ci = torch.empty(B, dtype=torch.int64, device="cuda")
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(stream):
+        for step in (8, 9):
+            ref_ids, ref_mx = fs.sample(hd, Wd, td, 23, step)
+            ids, mx = fs.sample_chunked_step(hd, Wd, bounds, td, 23, step, cm, ci)
+            stream.synchronize()
+            np.testing.assert_array_equal(ids.cpu().numpy(), ref_ids.cpu().numpy())
+            np.testing.assert_array_equal(mx.cpu().numpy(), ref_mx.cpu().numpy())
+    assert len(bounds) - 1 > 32
+
+
 def test_chunked_step_interleaved_with_one_shot_calls(fs, torch_cuda, path):
     """One-shot calls of another batch size, and a Gumbel-top-k call, enqueued
     on the same stream between the chunk calls of a step: they finish through

@@ -50,8 +50,8 @@ using namespace sm100;
 // four schedulers), which made the top-k lists spill and the B = 256, k = 8
 // call 2.5% slower, so the top-k variants keep 8.
 //
-// kLean: the instantiation for vocabulary chunks with few tiles
-// (fs_sample_chunked; see launch_tc_pair), which give each pair one or two: 3 stages, ONE 256-column accumulator
+// kLean: the instantiation for small vocabulary chunks of batches of several
+// pair tiles (fs_sample_chunked; see launch_tc_pair): 3 stages, ONE 256-column accumulator
 // and 8 epilogue warps, so that two CTAs fit on an SM (shared memory, TMEM
 // and registers) and the next chunk's pairs stream and multiply while this
 // chunk's run their epilogues.  Its MMAs (shapes, K order) and its scan are
@@ -483,9 +483,20 @@ static cudaError_t launch_pair_sampler(const Problem& p, const Finish& f, int* e
   return cudaSuccess;
 }
 
-// Chunk calls.  A chunk of few tiles (fewer than 24: 32 chunks of a 128K
-// vocabulary) runs the lean instantiation, two CTAs per SM, so that the next
-// chunks' pairs stream while this chunk's scan.  Larger chunks run the full
+// Chunk calls.  Chunks of fewer than 24 tiles (32 chunks of a 128K
+// vocabulary) run the full instantiation with 2 tiles per pair from 12 tiles
+// on and 1 below; only chunks of fewer than 12 tiles of batches of several
+// pair tiles run the lean instantiation (two CTAs per SM).  Measured on GB300
+// (8B head, µs per step; one fs_sample_chunked_step call per step, steps back
+// to back / the per-chunk calls replayed from a CUDA graph): B = 256, 24
+// chunks (21 tiles): lean 254.8 / 282.5, k = 2 244.9 / 275.3; 32 chunks (16
+// tiles): lean 299.1 / 277.4, k = 2 271.7 / 275.9, k = 1 274.5 / 303.8; 48
+// chunks (11 tiles): lean 434.2 / 339.3, k = 1 319.9 / 349.2, k = 2 412.1 /
+// 338.4; 64 chunks (8 tiles): lean 499.6 / 349.9, k = 1 364.9 / 340.7; 128
+// chunks (4 tiles): lean 1201 / 681, k = 1 834 / 546.  B = 512, 32 chunks:
+// lean 427.2 / 484.6, k = 2 414.4 / 471.7; 64 chunks: lean 580.9 / 528.8,
+// k = 1 513.0 / 577.2.
+// Larger chunks run the full
 // instantiation with k >= 4 tiles per pair: a pair's epilogues overlap its
 // next tiles' MMAs and the chunks in flight take disjoint pairs.  Their cost
 // follows waves of pairs: the step's chunks need n * ceil(T / k) * npt pairs
@@ -500,6 +511,7 @@ static cudaError_t launch_pair_sampler(const Problem& p, const Finish& f, int* e
 // MMAs and the scan are the same in both instantiations, so the samples are
 // too.
 constexpr int64_t kChunkLeanMaxTiles = 24;
+constexpr int64_t kChunkPairOfTwoMinTiles = 12;
 constexpr int kChunkMinTilesPerPair = 4;
 constexpr int kChunkMaxTilesPerPair = 16;
 
@@ -548,7 +560,11 @@ cudaError_t launch_tc_pair(const Problem& p, const Finish& f, int* err, cudaStre
   if (p.d < kBK || p.V_local <= 0) return cudaErrorNotSupported;
   if (!p.chunk) return launch_pair_sampler<false>(p, f, err, stream, 1);
   const int64_t n_vt = (p.V_local + kBN - 1) / kBN;
-  if (n_vt < kChunkLeanMaxTiles) return launch_pair_sampler<true>(p, f, err, stream, 1);
+  if (n_vt < kChunkLeanMaxTiles) {
+    if (n_vt >= kChunkPairOfTwoMinTiles) return launch_pair_sampler<false>(p, f, err, stream, 2);
+    if (p.B <= 2 * kRowsPerCta) return launch_pair_sampler<false>(p, f, err, stream, 1);
+    return launch_pair_sampler<true>(p, f, err, stream, 1);
+  }
   int dev = 0;
   const int sms = device_sms(&dev);
   const int k = chunk_tiles_per_pair(n_vt, p.B, p.step_chunks, resident_pairs<false>(dev, sms));

@@ -371,7 +371,8 @@ FS_API int fs_path_for_batch(int64_t B);
 
 /* The kernel family a chunk call of B rows and V_chunk vocabulary rows would
  * use under the current setting, when the previous chunked step on its stream
- * had step_chunks chunk calls (0: none yet). */
+ * had step_chunks chunk calls (0: none yet), launched on a stream (a call
+ * made during CUDA-graph capture may choose differently). */
 FS_API int fs_path_for_chunks(int64_t B, int64_t V_chunk, int step_chunks);
 
 /*

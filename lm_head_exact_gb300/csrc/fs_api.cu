@@ -367,7 +367,7 @@ int resolve_call_path(const Problem& p) {
   if (p.B <= kChunkVocabMaxBatch || p.B > 128) return path;
   int dev = 0;
   cudaGetDevice(&dev);
-  return tc_pair_chunk_one_wave(p.V_local, p.B, p.step_chunks, dev) ? kPathTcPair : kPathTcBatch;
+  return tc_pair_chunk_one_wave(p.V_local, p.B, p.step_chunks, p.in_graph, dev) ? kPathTcPair : kPathTcBatch;
 }
 
 // One fused launch (kernel + in-kernel cross-CTA finish) for one problem,
@@ -493,6 +493,7 @@ fs_status sample_chunk(const void* h, const void* W_chunk, int64_t B, int64_t d,
     FS_TRY(next_chunk_set(static_cast<cudaStream_t>(stream), (flags & FS_CHUNK_FIRST) != 0, last, &set, &overlap_ok,
                           &p.step_chunks));
   if (!overlap_ok) p.pdl = false;
+  p.in_graph = capturing(static_cast<cudaStream_t>(stream));
   return run(p, f, static_cast<cudaStream_t>(stream), set);
 }
 

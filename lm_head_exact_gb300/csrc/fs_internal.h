@@ -56,6 +56,7 @@ struct Problem {
   // yet); sizes the tiles per pair of the full instantiation (see
   // launch_tc_pair).  Never changes a result.
   int step_chunks = 0;
+  bool in_graph = false;  // chunk call made while its stream is captured into a CUDA graph
 };
 
 // Launch `kernel` on `stream`, as a programmatic dependent launch when `pdl`.
@@ -143,7 +144,7 @@ cudaError_t launch_tc_batch(const Problem& p, const Finish& f, int* err, cudaStr
 cudaError_t launch_tc_pair(const Problem& p, const Finish& f, int* err, cudaStream_t stream);
 // Whether a chunked step of step_chunks such chunks fits one wave of CTA
 // pairs with few tiles per pair (the chunk family rule of fs_api.cu).
-bool tc_pair_chunk_one_wave(int64_t V_local, int64_t B, int step_chunks, int device);
+bool tc_pair_chunk_one_wave(int64_t V_local, int64_t B, int step_chunks, bool in_graph, int device);
 
 // Unfused comparison pipeline: tensor-core GEMM storing fp32 logits [B, V]
 // (+ bias) to HBM, then row softmax into probs [B, V], then the sample.

@@ -515,7 +515,22 @@ constexpr int64_t kChunkPairOfTwoMinTiles = 12;
 constexpr int kChunkMinTilesPerPair = 4;
 constexpr int kChunkMaxTilesPerPair = 16;
 
-static int chunk_tiles_per_pair(int64_t n_vt, int64_t B, int step_chunks, int pairs) {
+// Chunk grids launched on a stream (not from a CUDA graph) run at most 8 at a
+// time on GB300, however many pairs stay idle: with 12 chunks of 6 pairs (72
+// of the 76), a per-CTA timeline showed chunks 0-7 starting within 21 us and
+// chunk 8 only when chunk 0 had exited, 180 us later (343 us per step against
+// 216 on the batch-major kernel; 9 chunks of 8 pairs at B = 256: 357 us).
+// Replayed from a graph the same 12 chunks ran side by side (229 us).  The
+// waves of a step count both the pairs and, for stream launches, the grids.
+constexpr int kStreamChunkGrids = 8;
+
+static int64_t chunk_waves(int64_t need_pairs, int64_t pairs, int step_chunks, bool in_graph) {
+  int64_t waves = (need_pairs + pairs - 1) / pairs;
+  if (!in_graph) waves = std::max<int64_t>(waves, (step_chunks + kStreamChunkGrids - 1) / kStreamChunkGrids);
+  return waves;
+}
+
+static int chunk_tiles_per_pair(int64_t n_vt, int64_t B, int step_chunks, bool in_graph, int pairs) {
   if (step_chunks <= 0) return kChunkMinTilesPerPair;
   const int64_t npt = (std::min<int64_t>(B, static_cast<int64_t>(pairs) * 2 * kRowsPerCta) + 2 * kRowsPerCta - 1) /
                       (2 * kRowsPerCta);
@@ -523,7 +538,7 @@ static int chunk_tiles_per_pair(int64_t n_vt, int64_t B, int step_chunks, int pa
   int64_t best_cost = -1;
   for (int k = kChunkMinTilesPerPair; k <= kChunkMaxTilesPerPair; ++k) {
     const int64_t need = static_cast<int64_t>(step_chunks) * ((n_vt + k - 1) / k) * npt;
-    const int64_t cost = (need + pairs - 1) / pairs * k;
+    const int64_t cost = chunk_waves(need, pairs, step_chunks, in_graph) * k;
     if (best_cost < 0 || cost < best_cost) {
       best_cost = cost;
       best_k = k;
@@ -543,9 +558,10 @@ static int chunk_tiles_per_pair(int64_t n_vt, int64_t B, int step_chunks, int pa
 // 249, 32 chunks 266 / 275 vs 233 -- two waves or the lean instantiation).
 constexpr int kChunkFastTilesPerPair = 7;
 
-bool tc_pair_chunk_one_wave(int64_t V_local, int64_t B, int step_chunks, int device) {
+bool tc_pair_chunk_one_wave(int64_t V_local, int64_t B, int step_chunks, bool in_graph, int device) {
   const int64_t n_vt = (V_local + kBN - 1) / kBN;
   if (step_chunks <= 0 || n_vt < kChunkLeanMaxTiles || B <= 0) return false;
+  if (!in_graph && step_chunks > kStreamChunkGrids) return false;
   int sms = 0;
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
   const int pairs = resident_pairs<false>(device, sms > 0 ? sms : 148);
@@ -567,7 +583,7 @@ cudaError_t launch_tc_pair(const Problem& p, const Finish& f, int* err, cudaStre
   }
   int dev = 0;
   const int sms = device_sms(&dev);
-  const int k = chunk_tiles_per_pair(n_vt, p.B, p.step_chunks, resident_pairs<false>(dev, sms));
+  const int k = chunk_tiles_per_pair(n_vt, p.B, p.step_chunks, p.in_graph, resident_pairs<false>(dev, sms));
   return launch_pair_sampler<false>(p, f, err, stream, k);
 }
 

@@ -172,6 +172,9 @@ def test_chunk_dispatch_rule(built_library):
         assert fs.path_for_chunks(B, 12826, 10) == fs.FS_PATH_TC_BATCH, B
         assert fs.path_for_chunks(B, 4008, 32) == fs.FS_PATH_TC_BATCH, B
         assert fs.path_for_chunks(B, 5888, 8) == fs.FS_PATH_TC_BATCH, B     # 23 pair tiles per chunk
+        # 12 chunks of 42 tiles would fit one wave of pairs, but stream-launched
+        # chunk grids run at most 8 at a time
+        assert fs.path_for_chunks(B, 10688, 12) == fs.FS_PATH_TC_BATCH, B
     try:
         fs.set_path(fs.FS_PATH_TC_VOCAB)
         assert fs.path_for_chunks(64, 16032, 8) == fs.FS_PATH_TC_VOCAB

@@ -496,8 +496,8 @@ static cudaError_t launch_pair_sampler(const Problem& p, const Finish& f, int* e
 // chunks (4 tiles): lean 1201 / 681, k = 1 834 / 546.  B = 512, 32 chunks:
 // lean 427.2 / 484.6, k = 2 414.4 / 471.7; 64 chunks: lean 580.9 / 528.8,
 // k = 1 513.0 / 577.2.
-// Larger chunks run the full
-// instantiation with k >= 4 tiles per pair: a pair's epilogues overlap its
+// Chunks of at least 24 tiles run the full instantiation with k >= 4 tiles
+// per pair: a pair's epilogues overlap its
 // next tiles' MMAs and the chunks in flight take disjoint pairs.  Their cost
 // follows waves of pairs: the step's chunks need n * ceil(T / k) * npt pairs
 // (n chunks of T tiles, npt pair tiles of batch rows), run in
@@ -555,7 +555,9 @@ static int chunk_tiles_per_pair(int64_t n_vt, int64_t B, int step_chunks, bool i
 // major: 4 chunks 215 / 218 vs 241, 6 chunks 217 / 221 vs 243, 8 chunks 219 /
 // 223 vs 241, 12 chunks 229 / 232 vs 242 -- one wave of k = 7; 10 chunks
 // 264 / 265 vs 242, 16 chunks 249 / 252 vs 237, 20 chunks 272 / 273 vs
-// 249, 32 chunks 266 / 275 vs 233 -- two waves or the lean instantiation).
+// 249, 32 chunks 266 / 275 vs 233 -- two waves or the lean instantiation;
+// times of per-chunk calls replayed from a CUDA graph).  Stream-launched
+// steps must also fit the kStreamChunkGrids limit.
 constexpr int kChunkFastTilesPerPair = 7;
 
 bool tc_pair_chunk_one_wave(int64_t V_local, int64_t B, int step_chunks, bool in_graph, int device) {

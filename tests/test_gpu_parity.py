@@ -535,6 +535,35 @@ def test_one_call_chunked_step_with_many_chunks(fs, torch_cuda, B):
     assert len(bounds) - 1 > 32
 
 
+@pytest.mark.parametrize("B,d", [(0, 128), (5, 40), (70, 40), (64, 256)])
+def test_one_call_chunked_step_edge_cases(fs, torch_cuda, B, d):
+    """fs_sample_chunked_step on the edges: B = 0 (a no-op), a model width
+    below 64 (every batch size on the CUDA-core family), bounds whose chunks
+    are all empty but one, greedy rows and a shared [V] bias.  Each result
+    equals the one-shot sample bit for bit (and the oracle's rule)."""
+    torch = torch_cuda
+    V = 3001
+    h, W, temp = _problem(max(B, 1), V, d, seed=171 + B + d)
+    h, temp = h[:B], temp[:B]
+    if B:
+        temp[1::3] = 0.0
+    shared = (np.random.default_rng(d).standard_normal(V) * 0.5).astype(np.float32)
+    hd, Wd, td, sd = to_device(h, torch), to_device(W, torch), to_device(temp, torch), to_device(shared, torch)
+    cm = torch.empty(max(B, 1), device="cuda")[:B]
+    ci = torch.empty(max(B, 1), dtype=torch.int64, device="cuda")[:B]
+    for bounds in ([0, 0, 0, V, V], [0, 1000, 1000, 2999, V]):
+        b = np.asarray(bounds, np.int64)
+        ids, mx = fs.sample_chunked_step(hd, Wd, b, td, 31, 4, cm, ci, bias=sd)
+        ref_ids, ref_mx = fs.sample(hd, Wd, td, 31, 4, bias=sd)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(ids.cpu().numpy(), ref_ids.cpu().numpy())
+        np.testing.assert_array_equal(mx.cpu().numpy(), ref_mx.cpu().numpy())
+    if B:
+        bias = np.broadcast_to(shared, (B, V))
+        compare(ids.cpu().numpy(), mx.cpu().numpy(), sampler.sample(h, W, temp, 31, 4, bias=bias),
+                what=f"chunked step edges B={B} d={d}")
+
+
 def test_chunked_step_interleaved_with_one_shot_calls(fs, torch_cuda, path):
     """One-shot calls of another batch size, and a Gumbel-top-k call, enqueued
     on the same stream between the chunk calls of a step: they finish through

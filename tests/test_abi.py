@@ -110,6 +110,11 @@ def test_product_path_refuses_cpu_tensors(built_library):
     t = torch.ones(2)
     with pytest.raises(binding.FlashSampleError, match="CUDA tensor"):
         binding.sample(h, W, t, 0, 0)
+    cm, ci = torch.zeros(2), torch.zeros(2, dtype=torch.int64)
+    with pytest.raises(binding.FlashSampleError, match="CUDA tensor"):
+        binding.sample_chunked_step(h, W, [0, 2, 4], t, 0, 0, cm, ci)
+    with pytest.raises(binding.FlashSampleError, match="bounds"):
+        binding.sample_chunked_step(h, W, [0, 2, 3], t, 0, 0, cm, ci)     # must end at W.shape[0]
 
 
 def test_binding_constants_match_the_header():

@@ -454,39 +454,41 @@ def run_ours(args):
     if want("chunked"):
         # B = 64 besides the chunked workload's batches: chunk calls there run
         # another tensor-core family than the one-shot call
-        for b in sorted(set(synthetic.SHAPES["chunked"]["batches"]) | {64}):
-            for n in (8, 32):
-                bounds = synthetic.chunk_bounds(V, n)
-                cm = torch.empty(b, device="cuda")
-                ci = torch.empty(b, dtype=torch.int64, device="cuda")
-                cids = torch.empty(b, dtype=torch.int64, device="cuda")
-                cmx = torch.empty(b, dtype=torch.float32, device="cuda")
-                fs.workspace_reserve(b, V, stream=stream)
+        configs = [(b, n) for b in sorted(set(synthetic.SHAPES["chunked"]["batches"]) | {64}) for n in (8, 32)]
+        if args.chunk_config:
+            cb, cn = (int(x) for x in args.chunk_config.split(":"))
+            configs = [(cb, cn)]
+        for b, n in configs:
+            bounds = synthetic.chunk_bounds(V, n)
+            cm = torch.empty(b, device="cuda")
+            ci = torch.empty(b, dtype=torch.int64, device="cuda")
+            cids = torch.empty(b, dtype=torch.int64, device="cuda")
+            cmx = torch.empty(b, dtype=torch.float32, device="cuda")
+            fs.workspace_reserve(b, V, stream=stream)
 
-                bounds_np = np.asarray(bounds, np.int64)
+            bounds_np = np.asarray(bounds, np.int64)
 
-                def chunk_step():
-                    for i, (lo, hi) in enumerate(zip(bounds[:-1], bounds[1:])):
-                        fs.sample_chunked(hd_all[:b], Wd[lo:hi], lo, temp_all[:b],
-                                          seed, 5, cm, ci, i == 0, i == n - 1, out=(cids, cmx), stream=stream)
+            def chunk_step():
+                for i, (lo, hi) in enumerate(zip(bounds[:-1], bounds[1:])):
+                    fs.sample_chunked(hd_all[:b], Wd[lo:hi], lo, temp_all[:b],
+                                      seed, 5, cm, ci, i == 0, i == n - 1, out=(cids, cmx), stream=stream)
 
-                def chunk_step_one_call():
-                    fs.sample_chunked_step(hd_all[:b], Wd, bounds_np, temp_all[:b], seed, 5, cm, ci,
-                                           out=(cids, cmx), stream=stream)
+            def chunk_step_one_call():
+                fs.sample_chunked_step(hd_all[:b], Wd, bounds_np, temp_all[:b], seed, 5, cm, ci,
+                                       out=(cids, cmx), stream=stream)
 
-                # the step's chunk calls issued from C, steps back to back on the
-                # stream (as the one-shot rows); beside it the per-chunk calls
-                # replayed as a CUDA graph of one step, which measures 5-14%
-                # slower on GB300 (graph-launched kernels overlap their
-                # neighbours less than stream-launched ones)
-                us = direct_us(chunk_step_one_call)
-                us_graph = graph_us(chunk_step)
-                rf = roofline(b, d, V, us, peaks)
-                chunked.append({"workload": "chunked", "B": b, "chunks": n, "us_per_step": round(us, 2),
-                                "frac": rf["frac"], "bound": rf["bound"],
-                                "path": fs.path_for_chunks(b, bounds[1] - bounds[0], n),
-                                "launches_per_step": n, "launch": "fs_sample_chunked_step, back to back",
-                                "graph_us_per_step": round(us_graph, 2)})
+            # the step's chunk calls issued from C, steps back to back on the
+            # stream (as the one-shot rows); beside it the per-chunk calls
+            # replayed as a CUDA graph of one step (graph replays measure
+            # slower on GB300 for any kernel, cuBLAS's GEMM included)
+            us = direct_us(chunk_step_one_call)
+            us_graph = graph_us(chunk_step)
+            rf = roofline(b, d, V, us, peaks)
+            chunked.append({"workload": "chunked", "B": b, "chunks": n, "us_per_step": round(us, 2),
+                            "frac": rf["frac"], "bound": rf["bound"],
+                            "path": fs.path_for_chunks(b, bounds[1] - bounds[0], n),
+                            "launches_per_step": n, "launch": "fs_sample_chunked_step, back to back",
+                            "graph_us_per_step": round(us_graph, 2)})
 
     # online early finalization (8 chunks): rows without a dominant winner
     # ("flat", every chunk runs) and rows with a +200 spike in the first
@@ -771,6 +773,8 @@ def parse_args(argv=None):
                     help="force a kernel family (profiling)")
     ap.add_argument("--only", default="",
                     help="comma list of extra sections: sweep,chunked,early,topk,decode,unfused")
+    ap.add_argument("--chunk-config", default="",
+                    help="B:chunks -- the chunked section runs only this configuration (for profiling)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
     args = ap.parse_args(argv)
